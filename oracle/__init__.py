@@ -1,0 +1,91 @@
+"""CPU oracle for the barrier-free small-message AllReduce.
+
+TEST INFRASTRUCTURE ONLY.  Only ``tests/``, ``__graft_entry__.smoke()`` and
+the CPU-baseline leg of ``bench.py`` may import this package.  It shares no
+code with the GPU library (``barrier_free_message_gb300``) and never imports
+it; the GPU library never imports this package.
+
+The arithmetic lives in ``sfar_oracle.c`` (plain C99): for every element the
+R ranks' values are widened to binary32, folded left to right in rank order
+0..R-1 with round-to-nearest-even binary32 adds, and rounded once to the
+output type; every rank receives the same result.  This module only loads the
+compiled object and marshals numpy arrays.
+
+Arrays: bf16 data is carried as ``numpy.uint16`` bit patterns, fp32 as
+``numpy.float32``.  ``x`` has shape ``[R, n]``.
+"""
+import ctypes
+import numpy as np
+
+from .build import build_oracle
+
+BF16 = 0
+FP32 = 1
+
+_libs = {}
+
+
+def _lib(mutant: int = 0):
+    if mutant not in _libs:
+        lib = ctypes.CDLL(build_oracle(mutant))
+        vpp = ctypes.POINTER(ctypes.c_void_p)
+        lib.sfar_oracle_allreduce.argtypes = [ctypes.c_int, ctypes.c_size_t, ctypes.c_int, vpp, vpp]
+        lib.sfar_oracle_allreduce.restype = ctypes.c_int
+        lib.sfar_oracle_allreduce_mt.argtypes = [ctypes.c_int, ctypes.c_size_t, ctypes.c_int, vpp, vpp,
+                                                 ctypes.c_int]
+        lib.sfar_oracle_allreduce_mt.restype = ctypes.c_int
+        lib.sfar_oracle_narrow_bf16.argtypes = [ctypes.c_float]
+        lib.sfar_oracle_narrow_bf16.restype = ctypes.c_uint16
+        lib.sfar_oracle_widen_bf16.argtypes = [ctypes.c_uint16]
+        lib.sfar_oracle_widen_bf16.restype = ctypes.c_float
+        lib.sfar_oracle_mutant.restype = ctypes.c_int
+        _libs[mutant] = lib
+    return _libs[mutant]
+
+
+def _dtype_code(x: np.ndarray) -> int:
+    if x.dtype == np.uint16:
+        return BF16
+    if x.dtype == np.float32:
+        return FP32
+    raise TypeError(f"oracle takes uint16 (bf16 bits) or float32 arrays, got {x.dtype}")
+
+
+def allreduce(x: np.ndarray, threads: int = 1, mutant: int = 0) -> np.ndarray:
+    """Reduce ``x[R, n]`` over its first axis; return ``[R, n]`` with the sum on every rank."""
+    x = np.ascontiguousarray(x)
+    if x.ndim != 2:
+        raise ValueError("x must have shape [R, n]")
+    R, n = x.shape
+    code = _dtype_code(x)
+    out = np.empty_like(x)
+    ins = (ctypes.c_void_p * R)(*[x[r].ctypes.data for r in range(R)])
+    outs = (ctypes.c_void_p * R)(*[out[r].ctypes.data for r in range(R)])
+    lib = _lib(mutant)
+    if threads > 1:
+        rc = lib.sfar_oracle_allreduce_mt(R, n, code, ins, outs, threads)
+    else:
+        rc = lib.sfar_oracle_allreduce(R, n, code, ins, outs)
+    if rc != 0:
+        raise ValueError(f"oracle rejected the arguments (R={R}, n={n})")
+    return out
+
+
+def allreduce_ptrs(R: int, n: int, code: int, in_ptrs, out_ptrs, threads: int = 1) -> None:
+    """Same as :func:`allreduce` on raw host addresses (used to time the oracle without copies)."""
+    ins = (ctypes.c_void_p * R)(*in_ptrs)
+    outs = (ctypes.c_void_p * R)(*out_ptrs)
+    lib = _lib()
+    rc = (lib.sfar_oracle_allreduce_mt(R, n, code, ins, outs, threads) if threads > 1
+          else lib.sfar_oracle_allreduce(R, n, code, ins, outs))
+    if rc != 0:
+        raise ValueError("oracle rejected the arguments")
+
+
+def narrow_bf16(f: float, mutant: int = 0) -> int:
+    """binary32 -> bf16 bits, round to nearest even (the oracle's own conversion)."""
+    return int(_lib(mutant).sfar_oracle_narrow_bf16(f))
+
+
+def widen_bf16(b: int, mutant: int = 0) -> float:
+    return float(_lib(mutant).sfar_oracle_widen_bf16(b))

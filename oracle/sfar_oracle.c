@@ -1,0 +1,246 @@
+/*
+ * sfar_oracle.c -- CPU oracle for the small-message AllReduce.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Only the test suite, the smoke check and the
+ * benchmark's CPU-baseline leg load this file.  It shares no code, header,
+ * table or helper with the GPU library, and the GPU library never calls it.
+ *
+ * What it computes (the plain definition of an AllReduce, with the order and
+ * rounding fixed):
+ *   "Every Microsecond Counts" (page 1), section "Unified primitives and API
+ *   design": recvReduce receives every peer's value and sums it in registers;
+ *   the one-shot kernel reads its local value, broadcasts it, reduces what it
+ *   receives and writes the result, so every rank ends with the same sum.
+ *   Section "Tensor parallelism and AllReduce": the partial results of all
+ *   GPUs are added and the total is handed back to every GPU.
+ * The pages do not fix an order or a precision.  This oracle takes the
+ * reading the hot path is held to: for each element i,
+ *     acc = widen(in[0][i]);  acc = acc (+) widen(in[q][i]) for q = 1..R-1
+ * with (+) an IEEE binary32 add rounded to nearest-even, then ONE rounding of
+ * acc to the output type (nearest-even), stored to out[r][i] for every r.
+ *
+ * dtype 0 = bf16 (stored as the upper 16 bits of a binary32), dtype 1 = fp32.
+ * Widening bf16 -> fp32 is exact (the bits shifted left by 16).  Narrowing
+ * fp32 -> bf16 is written out from the IEEE definition of round to nearest,
+ * ties to even, on the 16 dropped bits; a NaN stays a NaN of the same sign.
+ * Subnormals are kept (no flush to zero).
+ *
+ * Build with -O2 -ffp-contract=off -fno-fast-math (the only arithmetic is
+ * additions; the flags rule out contraction and value-changing rewrites).
+ *
+ * ORACLE_MUTANT (compile-time, tests only): 0 = the oracle.  Other values
+ * plant one plausible mistake each, so the tests can show that the pins on
+ * this oracle catch it.  The shipped object is always built with 0.
+ */
+#include <float.h>
+#include <pthread.h>
+#include <stddef.h>
+#include <stdint.h>
+#include <string.h>
+
+#if FLT_EVAL_METHOD != 0
+#error "the oracle needs binary32 arithmetic evaluated in binary32"
+#endif
+
+#ifndef ORACLE_MUTANT
+#define ORACLE_MUTANT 0
+#endif
+
+#define ORACLE_BF16 0
+#define ORACLE_FP32 1
+
+static float widen_bf16(uint16_t b)
+{
+    uint32_t u = (uint32_t)b << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+#if ORACLE_MUTANT == 10
+    /* mutant: flush subnormal inputs to zero */
+    if ((u & 0x7f800000u) == 0) { u &= 0x80000000u; memcpy(&f, &u, sizeof f); }
+#endif
+    return f;
+}
+
+/* binary32 -> bf16, round to nearest, ties to even (IEEE 754 roundTiesToEven
+ * applied to the 16 low-order significand bits that are dropped). */
+static uint16_t narrow_bf16(float f)
+{
+    uint32_t u;
+    memcpy(&u, &f, sizeof u);
+    if ((u & 0x7fffffffu) > 0x7f800000u)           /* NaN: keep sign, make quiet */
+        return (uint16_t)((u >> 16) | 0x0040u);
+    uint32_t kept = u >> 16;                         /* sign, exponent, 7 fraction bits */
+    uint32_t dropped = u & 0xffffu;
+#if ORACLE_MUTANT == 5
+    (void)dropped;                                   /* mutant: truncate */
+#elif ORACLE_MUTANT == 11
+    if (dropped >= 0x8000u) kept += 1;               /* mutant: ties away from zero */
+#else
+    if (dropped > 0x8000u || (dropped == 0x8000u && (kept & 1u)))
+        kept += 1;                                   /* a carry into the exponent is
+                                                        the correct result, up to inf */
+#endif
+    return (uint16_t)kept;
+}
+
+static float load_elem(const void *p, int dtype, size_t i)
+{
+    if (dtype == ORACLE_BF16)
+        return widen_bf16(((const uint16_t *)p)[i]);
+    float f;
+    memcpy(&f, (const unsigned char *)p + 4 * i, sizeof f);
+    return f;
+}
+
+static void store_elem(void *p, int dtype, size_t i, float v)
+{
+    if (dtype == ORACLE_BF16)
+        ((uint16_t *)p)[i] = narrow_bf16(v);
+    else
+        memcpy((unsigned char *)p + 4 * i, &v, sizeof v);
+}
+
+/* The reduction of element i over the R ranks, in the fixed order 0..R-1. */
+static float fold(int R, int dtype, const void *const *in, size_t n, size_t i)
+{
+    (void)n;
+#if ORACLE_MUTANT == 1
+    float acc = load_elem(in[R - 1], dtype, i);      /* mutant: reversed order */
+    for (int q = R - 2; q >= 0; --q)
+        acc = acc + load_elem(in[q], dtype, i);
+#elif ORACLE_MUTANT == 2
+    float acc = load_elem(in[0], dtype, i);          /* mutant: bf16 accumulator */
+    for (int q = 1; q < R; ++q) {
+        acc = acc + load_elem(in[q], dtype, i);
+        if (dtype == ORACLE_BF16) acc = widen_bf16(narrow_bf16(acc));
+    }
+#elif ORACLE_MUTANT == 3
+    float acc = 0.0f;                                /* mutant: start from +0 */
+    for (int q = 0; q < R; ++q)
+        acc = acc + load_elem(in[q], dtype, i);
+#elif ORACLE_MUTANT == 4
+    float acc = load_elem(in[0], dtype, i);          /* mutant: drops the last rank */
+    for (int q = 1; q < R - 1; ++q)
+        acc = acc + load_elem(in[q], dtype, i);
+#elif ORACLE_MUTANT == 7
+    /* mutant: pairwise tree instead of a left fold */
+    float v[64];
+    int m = R;
+    for (int q = 0; q < R; ++q) v[q] = load_elem(in[q], dtype, i);
+    while (m > 1) {
+        int h = 0;
+        for (int q = 0; q + 1 < m; q += 2) v[h++] = v[q] + v[q + 1];
+        if (m & 1) v[h++] = v[m - 1];
+        m = h;
+    }
+    float acc = v[0];
+#elif ORACLE_MUTANT == 8
+    float acc = load_elem(in[0], dtype, i);          /* mutant: reads a neighbour */
+    for (int q = 1; q < R; ++q)
+        acc = acc + load_elem(in[q], dtype, (i + 1 < n) ? i + 1 : i);
+#elif ORACLE_MUTANT == 9
+    float acc = load_elem(in[0], dtype, i);          /* mutant: subtracts the last rank */
+    for (int q = 1; q < R; ++q) {
+        float x = load_elem(in[q], dtype, i);
+        acc = (q == R - 1) ? acc - x : acc + x;
+    }
+#else
+    float acc = load_elem(in[0], dtype, i);
+    for (int q = 1; q < R; ++q)
+        acc = acc + load_elem(in[q], dtype, i);
+#endif
+    return acc;
+}
+
+static void allreduce_range(int R, int dtype, const void *const *in, void *const *out,
+                            size_t n, size_t lo, size_t hi)
+{
+    for (size_t i = lo; i < hi; ++i) {
+        float acc = fold(R, dtype, in, n, i);
+#if ORACLE_MUTANT == 6
+        store_elem(out[0], dtype, i, acc);           /* mutant: only rank 0 gets it */
+#else
+        for (int r = 0; r < R; ++r)
+            store_elem(out[r], dtype, i, acc);
+#endif
+    }
+}
+
+/*
+ * sfar_oracle_allreduce: R host arrays in[0..R-1] of n elements each (dtype
+ * as above) are reduced element by element; the result is written to every
+ * out[0..R-1].  Inputs and outputs are host memory owned by the caller and
+ * must not overlap.  Returns 0, or -1 for a bad argument (R < 1, R > 64,
+ * unknown dtype, a NULL pointer with n > 0).
+ */
+int sfar_oracle_allreduce(int R, size_t n, int dtype, const void *const *in, void *const *out)
+{
+    if (R < 1 || R > 64 || (dtype != ORACLE_BF16 && dtype != ORACLE_FP32))
+        return -1;
+    if (n == 0)
+        return 0;
+    if (!in || !out)
+        return -1;
+    for (int r = 0; r < R; ++r)
+        if (!in[r] || !out[r])
+            return -1;
+    allreduce_range(R, dtype, in, out, n, 0, n);
+    return 0;
+}
+
+struct oracle_job {
+    int R, dtype;
+    const void *const *in;
+    void *const *out;
+    size_t n, lo, hi;
+};
+
+static void *oracle_worker(void *arg)
+{
+    struct oracle_job *j = (struct oracle_job *)arg;
+    allreduce_range(j->R, j->dtype, j->in, j->out, j->n, j->lo, j->hi);
+    return NULL;
+}
+
+/*
+ * sfar_oracle_allreduce_mt: the same result as sfar_oracle_allreduce, with the
+ * element range split over `threads` POSIX threads (each element is still
+ * folded by one thread in the same order, so the bits are identical).  Used to
+ * time the oracle on several host cores.
+ */
+int sfar_oracle_allreduce_mt(int R, size_t n, int dtype, const void *const *in,
+                             void *const *out, int threads)
+{
+    if (threads <= 1 || n < 4096)
+        return sfar_oracle_allreduce(R, n, dtype, in, out);
+    if (R < 1 || R > 64 || (dtype != ORACLE_BF16 && dtype != ORACLE_FP32) || !in || !out)
+        return -1;
+    for (int r = 0; r < R; ++r)
+        if (!in[r] || !out[r])
+            return -1;
+    if (threads > 256)
+        threads = 256;
+    pthread_t tid[256];
+    struct oracle_job job[256];
+    size_t per = (n + (size_t)threads - 1) / (size_t)threads;
+    int started = 0;
+    for (int t = 0; t < threads; ++t) {
+        size_t lo = (size_t)t * per, hi = lo + per;
+        if (lo >= n) break;
+        if (hi > n) hi = n;
+        job[t] = (struct oracle_job){R, dtype, in, out, n, lo, hi};
+        if (pthread_create(&tid[t], NULL, oracle_worker, &job[t]) != 0) {
+            oracle_worker(&job[t]);
+            tid[t] = 0;
+        }
+        started = t + 1;
+    }
+    for (int t = 0; t < started; ++t)
+        if (tid[t]) pthread_join(tid[t], NULL);
+    return 0;
+}
+
+/* The two conversions on their own, so that tests can pin them directly. */
+uint16_t sfar_oracle_narrow_bf16(float f) { return narrow_bf16(f); }
+float sfar_oracle_widen_bf16(uint16_t b) { return widen_bf16(b); }
+int sfar_oracle_mutant(void) { return ORACLE_MUTANT; }
