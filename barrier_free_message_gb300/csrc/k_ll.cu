@@ -1,0 +1,115 @@
+// k_ll.cu -- one-shot AllReduce over LL packets.
+//
+// "Every Microsecond Counts" (page 1), section "Four barrier-free
+// mechanisms", part 1 (LL): data and flag travel together in one atomic
+// write, the receiver polls the flag half, and half of every slot is flag, so
+// payload efficiency is 50%.  Section "Unified primitives and API design": the
+// one-shot kernel has each thread read its local value, broadcast it to the
+// peers, receive-and-reduce everyone's value, write the result and advance
+// the epoch.  No barrier of any kind.
+//
+// Layout: receive region [receiver][parity][sender][2 * S bytes]; input
+// vector v (16 bytes) of sender q lands at bytes [32v, 32v + 32) of slot q as
+// two LL lines {w0,e,w1,e} {w2,e,w3,e}, written as 8-byte words (each word is
+// single-copy atomic, so flag == e proves its data word arrived).
+// Grid: R * K CTAs of 256 threads; CTA (r, k) = blockIdx r * K + k handles
+// vectors k*256 + t + j*K*256 of rank r.  Parity e & 1 double-buffers the
+// region: a sender can reach parity e & 1 again only at epoch e + 2, and its
+// CTA (r, k) of epoch e + 1 first received epoch e + 1 data from every peer's
+// CTA k, which each peer sends only after finishing epoch e (section part 3:
+// a received message is the licence to overwrite the previous buffer).
+#include "sfar_prims.cuh"
+
+template <int DT, int RB, bool TEST>
+__global__ void __launch_bounds__(SFAR_THREADS) k_ll(const __grid_constant__ SfarArgs a)
+{
+    constexpr int ES = DT == 0 ? 2 : 4;
+    const int R = a.R, K = a.K;
+    const int r = blockIdx.x / K, k = blockIdx.x - r * K;
+    SfarCall c;
+    if (!sfar_prologue<TEST>(a, r, k, c))
+        return;
+    const uint32_t e = c.e;
+    const unsigned long long nbytes = a.n * ES;
+    const unsigned long long nvec = (nbytes + 15ull) >> 4;
+    const unsigned long long stride = (unsigned long long)K * SFAR_THREADS;
+    const unsigned long long v0 = (unsigned long long)k * SFAR_THREADS + threadIdx.x;
+    const unsigned long long eh = (unsigned long long)e << 32;
+    const size_t slot = a.slot;
+
+    // send: pack each input vector once, store it into every peer's slot r
+    if (!c.drop) {
+        for (unsigned long long v = v0; v < nvec; v += stride) {
+            const uint4 x = load_vec<ES>(a.in[r], v, nbytes);
+            const unsigned long long p0 = x.x | eh, p1 = x.y | eh, p2 = x.z | eh, p3 = x.w | eh;
+#pragma unroll
+            for (int i = 0; i < RB - 1; ++i) {
+                if (i < R - 1) {
+                    const int p = peer_of(r, i);
+                    uint8_t *dst = a.region + ((size_t)(p * 2 + c.par) * R + r) * slot + v * 32ull;
+                    st_relaxed_v2u64(dst, p0, p1);
+                    st_relaxed_v2u64(dst + 16, p2, p3);
+                }
+            }
+        }
+    }
+
+    sfar_mid_delay<TEST>(c);
+
+    // receive and reduce: poll every peer's packets, fold in rank order
+    const uint8_t *mine = a.region + (size_t)(r * 2 + c.par) * R * slot;
+    bool ok = true;
+    for (unsigned long long v = v0; v < nvec && ok; v += stride) {
+        const uint4 own = load_vec<ES>(a.in[r], v, nbytes);
+        unsigned long long w0[RB], w1[RB], w2[RB], w3[RB];
+#pragma unroll
+        for (int q = 0; q < RB; ++q) {
+            if (q < R && q != r) {
+                const uint8_t *src = mine + (size_t)q * slot + v * 32ull;
+                ld_relaxed_v2u64(src, w0[q], w1[q]);
+                ld_relaxed_v2u64(src + 16, w2[q], w3[q]);
+            }
+        }
+#pragma unroll
+        for (int q = 0; q < RB; ++q) {
+            if (q < R && q != r && ok) {
+                SfarWaiter w;
+                const uint8_t *src = mine + (size_t)q * slot + v * 32ull;
+                while (!ll_ready(w0[q], w1[q], w2[q], w3[q], e)) {
+                    if (w.tick(a.ctl)) {
+                        sfar_record_fault(a.ctl, r, k, q, e, SFAR_WAIT_LL);
+                        ok = false;
+                        break;
+                    }
+                    ld_relaxed_v2u64(src, w0[q], w1[q]);
+                    ld_relaxed_v2u64(src + 16, w2[q], w3[q]);
+                }
+            }
+        }
+        if (!ok)
+            break;
+        SfarAcc<DT> acc;
+        acc.set(r == 0 ? own
+                       : make_uint4((uint32_t)w0[0], (uint32_t)w1[0], (uint32_t)w2[0], (uint32_t)w3[0]));
+#pragma unroll
+        for (int q = 1; q < RB; ++q) {
+            if (q < R)
+                acc.add(q == r ? own
+                               : make_uint4((uint32_t)w0[q], (uint32_t)w1[q], (uint32_t)w2[q],
+                                            (uint32_t)w3[q]));
+        }
+        store_vec<ES>(a.out[r], v, nbytes, acc.get());
+    }
+    sfar_epilogue(a, r, k, e);
+}
+
+const void *sfar_kernel_ll(int dt, int wide, int test)
+{
+#define SFAR_PICK(D, W, T)                                   \
+    if (dt == D && wide == W && test == T)                  \
+        return (const void *)k_ll<D, (W ? 16 : 8), (T != 0)>;
+    SFAR_PICK(0, 0, 0) SFAR_PICK(0, 0, 1) SFAR_PICK(0, 1, 0) SFAR_PICK(0, 1, 1)
+    SFAR_PICK(1, 0, 0) SFAR_PICK(1, 0, 1) SFAR_PICK(1, 1, 0) SFAR_PICK(1, 1, 1)
+#undef SFAR_PICK
+    return nullptr;
+}

@@ -1,0 +1,86 @@
+// k_misc.cu -- knob writes and the latency-floor probes.
+//
+// The floor a one-shot AllReduce of a few KB cannot beat on one GPU is one
+// kernel launch plus one flag hand-off through L2 between two SMs; it stands
+// in for the pages' speed-of-light bound ("Every Microsecond Counts"
+// (page 1), section "Tensor parallelism and AllReduce": the kernel came
+// within 7% of the hardware limit).  The probes measure the two parts.
+#include "sfar_prims.cuh"
+
+__global__ void k_set_knob(const SfarKnobArgs k)
+{
+    SfarCtl *c = k.ctl;
+    switch (k.which) {
+    case KNOB_TIMEOUT:
+        c->timeout_ns = k.value;
+        break;
+    case KNOB_STRAG:
+        c->strag_delays = k.ptr;
+        c->strag_len = k.len;
+        c->strag_rank = k.rank;
+        c->strag_phase = k.phase;
+        for (int i = 0; i < SFAR_KMAX; ++i)
+            c->strag_base[i] = k.epoch_row0[i];
+        break;
+    case KNOB_DROP:
+        c->drop_rank = k.rank;
+        break;
+    case KNOB_SINGLE:
+        c->single_buffer = (int)k.value;
+        break;
+    case KNOB_CLEAR_STATUS:
+        c->status = 0;
+        c->f_rank = c->f_cta = c->f_peer = -1;
+        c->f_epoch = 0;
+        c->f_where = 0;
+        break;
+    default:
+        break;
+    }
+}
+
+__global__ void k_empty() {}
+
+// Two CTAs (forced onto different SMs by their shared-memory size) pass a
+// token back and forth through two flags 128 bytes apart.
+__global__ void k_pingpong(uint32_t *flags, int trips, unsigned long long *ns_out)
+{
+    extern __shared__ uint8_t pad[];
+    if (threadIdx.x != 0)
+        return;
+    pad[0] = 0;
+    uint32_t *ping = flags, *pong = flags + 32;
+    const unsigned long long limit = 1000000000ull;
+    const unsigned long long start = globaltimer();
+    bool ok = true;
+    if (blockIdx.x == 0) {
+        for (int i = 1; i <= trips && ok; ++i) {
+            st_release_u32(ping, (uint32_t)i);
+            uint32_t it = 0;
+            while (ld_acquire_u32(pong) != (uint32_t)i)
+                if ((++it & 255u) == 0 && globaltimer() - start > limit) {
+                    ok = false;
+                    break;
+                }
+        }
+        *ns_out = ok ? globaltimer() - start : ~0ull;
+        if (!ok)
+            st_release_u32(ping, 0xffffffffu);
+    } else {
+        for (int i = 1; i <= trips && ok; ++i) {
+            uint32_t it = 0, v;
+            while ((v = ld_acquire_u32(ping)) != (uint32_t)i) {
+                if (v == 0xffffffffu || ((++it & 255u) == 0 && globaltimer() - start > limit)) {
+                    ok = false;
+                    break;
+                }
+            }
+            if (ok)
+                st_release_u32(pong, (uint32_t)i);
+        }
+    }
+}
+
+const void *sfar_kernel_set_knob() { return (const void *)k_set_knob; }
+const void *sfar_kernel_empty() { return (const void *)k_empty; }
+const void *sfar_kernel_pingpong() { return (const void *)k_pingpong; }

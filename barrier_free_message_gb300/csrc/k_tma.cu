@@ -1,0 +1,250 @@
+// k_tma.cu -- two-shot AllReduce for large messages with TMA bulk copies.
+//
+// "SiFAR" (page 3), section "Limits of existing algorithms": in two-shot
+// each rank owns one chunk, reduces it over all ranks (reduce-scatter) and
+// hands the reduced chunk to every rank (all-gather).  "Every Microsecond
+// Counts" (page 1), section "Tensor parallelism and AllReduce": for large
+// messages bandwidth, not latency, decides.  So this path moves the minimum
+// bytes: owner j reads its chunk of every rank's input once and writes the
+// reduced chunk once into every rank's output, with no staging buffers.
+//
+// Owner CTA (j, k) takes a contiguous range of chunk j and streams it in
+// tiles: one thread issues, per tile, R 1-D bulk copies
+// (cp.async.bulk global -> shared, completion on an mbarrier) into a ring of
+// stages; all threads fold the R tiles from shared memory in rank order,
+// round once, write the tile to a shared output buffer; one thread then
+// issues R bulk copies shared -> global, one per rank's output.  No
+// multicast and no bulk reduction (its order of additions is not fixed).
+//
+// Synchronisation between simulated ranks (the pages' counters reaching N,
+// page 1 section "Four barrier-free mechanisms", part 4, kept as flags):
+//   * arrival (top barrier): CTA (q, k) stores its epoch into arrive[q][k];
+//     owners read rank q's input and write rank q's output only once every
+//     rank has arrived at this call;
+//   * completion: after its bulk stores have completed, owner j stores the
+//     epoch into cmpl[p][j][k] for every rank p, and CTA (p, k) waits for
+//     all owners before it reports its call finished.
+// No receive buffers, so nothing to double-buffer and no bottom barrier.
+#include "sfar_prims.cuh"
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p)
+{
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t phase)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(phase)
+        : "memory");
+    return ok != 0;
+}
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar)
+{
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+                 "l"(src), "r"(bytes), "r"(bar)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_s2g(void *dst, uint32_t src, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst), "r"(src), "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+__device__ __forceinline__ void fence_proxy_async_smem()
+{
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+__device__ __forceinline__ void fence_proxy_async_global()
+{
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+template <int DT, bool TEST>
+__global__ void __launch_bounds__(SFAR_TMA_THREADS, 1) k_tma(const __grid_constant__ SfarArgs a)
+{
+    constexpr int ES = DT == 0 ? 2 : 4;
+    const int R = a.R, K = a.K;
+    const int r = blockIdx.x / K, k = blockIdx.x - r * K;
+    const int tid = threadIdx.x, lane = tid & 31;
+    SfarCall c;
+    if (!sfar_prologue<TEST>(a, r, k, c))
+        return;
+    const uint32_t e = c.e;
+    uint32_t *arrive = a.fa;      // [R][KMAX]
+    uint32_t *cmpl = a.fb;        // [receiver][owner][KMAX]
+    __shared__ int s_ok;
+
+    // arrival: this rank's input is ready and its output free for this call
+    if (tid < 32) {
+        if (tid == 0 && !c.drop)
+            st_release_u32(arrive + r * SFAR_KMAX + k, e);
+        int ok = 1;
+        for (int i = lane; i < R - 1 && ok; i += 32) {
+            const int q = peer_of(r, i);
+            if (!poll_flag_ge(arrive + q * SFAR_KMAX + k, e, a.ctl)) {
+                sfar_record_fault(a.ctl, r, k, q, e, SFAR_WAIT_ARRIVE);
+                ok = 0;
+            }
+        }
+        ok = __all_sync(SFAR_FULL, ok);
+        fence_acq_rel_gpu();
+        if (tid == 0)
+            s_ok = ok;
+    }
+    __syncthreads();
+    bool ok = s_ok != 0;
+    sfar_mid_delay<TEST>(c);
+
+    // this CTA's byte range [b0, b1) of chunk r
+    const unsigned long long nbytes = a.n * ES;
+    const unsigned long long cb0 = (unsigned long long)r * a.chunk * ES;
+    unsigned long long b0 = cb0 + (unsigned long long)k * a.sub * ES;
+    unsigned long long b1 = b0 + a.sub * ES;
+    const unsigned long long cb1 = cb0 + a.chunk * ES;
+    if (b1 > cb1) b1 = cb1;
+    if (b1 > nbytes) b1 = nbytes;
+    if (b0 > b1) b0 = b1;
+    const unsigned long long len16 = (b1 - b0) & ~15ull;
+    const uint32_t TB = (uint32_t)a.tile_bytes;
+    const int NS = a.stages;
+    const unsigned long long ntiles = (len16 + TB - 1) / TB;
+
+    extern __shared__ __align__(128) uint8_t smem[];
+    uint8_t *stage0 = smem;                                           // [NS][R][TB]
+    uint8_t *obuf = smem + (size_t)NS * R * TB;                       // [2][TB]
+    uint64_t *bars = reinterpret_cast<uint64_t *>(obuf + 2 * (size_t)TB);
+
+    if (ok && ntiles > 0) {
+        if (tid == 0) {
+            for (int s = 0; s < NS; ++s)
+                mbar_init(smem_u32(bars + s), 1);
+            asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+            fence_proxy_async_smem();
+        }
+        __syncthreads();
+        auto issue = [&](unsigned long long t) {
+            const int s = (int)(t % NS);
+            const unsigned long long off = t * TB;
+            const uint32_t tb = (uint32_t)((len16 - off) < TB ? (len16 - off) : TB);
+            const uint32_t bar = smem_u32(bars + s);
+            mbar_expect_tx(bar, tb * (uint32_t)R);
+            for (int q = 0; q < R; ++q)
+                bulk_g2s(smem_u32(stage0 + ((size_t)s * R + q) * TB), (const uint8_t *)a.in[q] + b0 + off, tb, bar);
+        };
+        if (tid == 0)
+            for (unsigned long long t = 0; t < ntiles && t < (unsigned long long)NS; ++t)
+                issue(t);
+
+        for (unsigned long long t = 0; t < ntiles; ++t) {
+            const int s = (int)(t % NS);
+            const uint32_t phase = (uint32_t)((t / NS) & 1ull);
+            const unsigned long long off = t * TB;
+            const uint32_t tb = (uint32_t)((len16 - off) < TB ? (len16 - off) : TB);
+            int tok = 1;
+            {
+                SfarWaiter w;
+                const uint32_t bar = smem_u32(bars + s);
+                while (!mbar_try_wait(bar, phase)) {
+                    if (w.tick(a.ctl)) {
+                        sfar_record_fault(a.ctl, r, k, -1, e, SFAR_WAIT_COPY);
+                        tok = 0;
+                        break;
+                    }
+                }
+            }
+            const uint8_t *st = stage0 + (size_t)s * R * TB;
+            uint8_t *ob = obuf + (size_t)(t & 1ull) * TB;
+            if (tok) {
+                for (uint32_t u = tid * 16u; u < tb; u += SFAR_TMA_THREADS * 16u) {
+                    SfarAcc<DT> acc;
+                    acc.set(*reinterpret_cast<const uint4 *>(st + u));
+                    for (int q = 1; q < R; ++q)
+                        acc.add(*reinterpret_cast<const uint4 *>(st + (size_t)q * TB + u));
+                    *reinterpret_cast<uint4 *>(ob + u) = acc.get();
+                }
+                fence_proxy_async_smem();
+            }
+            if (tid == 0)
+                bulk_wait_read0();    // the previous tile's stores have read their buffer
+            if (!__syncthreads_and(tok)) {
+                ok = false;
+                break;
+            }
+            if (tid == 0) {
+                for (int p = 0; p < R; ++p)
+                    bulk_s2g((uint8_t *)a.out[p] + b0 + off, smem_u32(ob), tb);
+                bulk_commit();
+                if (t + NS < ntiles)
+                    issue(t + NS);      // every thread has finished reading stage s
+            }
+        }
+        if (tid == 0) {
+            bulk_wait0();               // stores complete before completion is signalled
+            fence_proxy_async_global();
+        }
+    }
+    // a ragged end shorter than 16 bytes: element by element
+    if (ok && tid == 0 && b1 == nbytes && (b1 - b0) > len16) {
+        for (unsigned long long b = b0 + len16; b < b1; b += ES) {
+            float acc = 0.f;
+            for (int q = 0; q < R; ++q) {
+                float x;
+                if (ES == 2)
+                    x = __uint_as_float((uint32_t)(*(const uint16_t *)((const uint8_t *)a.in[q] + b)) << 16);
+                else
+                    x = *(const float *)((const uint8_t *)a.in[q] + b);
+                acc = q == 0 ? x : __fadd_rn(acc, x);
+            }
+            for (int p = 0; p < R; ++p) {
+                if (ES == 2) {
+                    __nv_bfloat16 h = __float2bfloat16_rn(acc);
+                    *(uint16_t *)((uint8_t *)a.out[p] + b) = *reinterpret_cast<uint16_t *>(&h);
+                } else {
+                    *(float *)((uint8_t *)a.out[p] + b) = acc;
+                }
+            }
+        }
+    }
+    __syncthreads();
+    // completion: tell every rank this owner's part of its output is written
+    if (tid < 32) {
+        fence_acq_rel_gpu();
+        if (ok && !c.drop)
+            for (int p = lane; p < R; p += 32)
+                if (p != r)
+                    st_relaxed_u32(cmpl + ((size_t)p * R + r) * SFAR_KMAX + k, e);
+        int wok = ok ? 1 : 0;
+        for (int i = lane; i < R - 1 && wok; i += 32) {
+            const int q = peer_of(r, i);
+            if (!poll_flag_ge(cmpl + ((size_t)r * R + q) * SFAR_KMAX + k, e, a.ctl)) {
+                sfar_record_fault(a.ctl, r, k, q, e, SFAR_WAIT_COMPLETE);
+                wok = 0;
+            }
+        }
+        __syncwarp();
+        fence_acq_rel_gpu();
+    }
+    sfar_epilogue(a, r, k, e);
+}
+
+const void *sfar_kernel_tma(int dt, int test)
+{
+    if (dt == 0)
+        return test ? (const void *)k_tma<0, true> : (const void *)k_tma<0, false>;
+    return test ? (const void *)k_tma<1, true> : (const void *)k_tma<1, false>;
+}

@@ -1,0 +1,170 @@
+// k_twoshot.cu -- two-shot AllReduce (reduce-scatter, then all-gather) over
+// LL128 lines with double-buffered epochs, for medium messages.
+//
+// "Every Microsecond Counts" (page 1), section "Unified primitives and API
+// design", table of variants: the two-shot LLBuffer variant (double
+// buffering, 64 KB to 1 MB) and the two-phase LL128 variant; section "Four
+// barrier-free mechanisms", part 4: reduce-scatter then all-gather over
+// 128-byte lines with a flag per line.  "SiFAR" (page 3), section "Limits of
+// existing algorithms": each rank owns one chunk, reduces it, and broadcasts
+// the reduced chunk.
+//
+// Chunks: owner j holds elements [j*c, min(n, (j+1)*c)); c is ceil(n / R)
+// rounded up to a whole warp iteration (4 lines = 496 payload bytes) so that
+// every chunk starts on a line group.  Chunking does not change any element's
+// fold.  Regions: RS [owner][parity][sender][lines], AG
+// [receiver][parity][owner][lines].  CTA (r, k), warp w handles iterations
+// k*8 + w + j*K*8 of every chunk, so each exchange is between the CTAs of
+// index k of two ranks.
+//   1. RS send: rank r's slice of every other chunk j -> owner j's slot r.
+//   2. Owner r polls its R - 1 slots, folds in rank order 0..R-1 (its own
+//      slice at position r), rounds once, writes the result to its own output
+//      and to every peer's AG slot r.
+//   3. Every rank polls the AG slots of the other owners and unpacks them.
+// Double buffering: parity e & 1; the argument of the one-shot kernels holds
+// for both regions because every CTA finishes all three phases of epoch e
+// before any of its epoch e + 1 sends.
+#include "sfar_prims.cuh"
+
+template <int DT, int RB, bool TEST>
+__global__ void __launch_bounds__(SFAR_THREADS) k_twoshot(const __grid_constant__ SfarArgs a)
+{
+    constexpr int ES = DT == 0 ? 2 : 4;
+    const int R = a.R, K = a.K;
+    const int r = blockIdx.x / K, k = blockIdx.x - r * K;
+    SfarCall c;
+    if (!sfar_prologue<TEST>(a, r, k, c))
+        return;
+    const uint32_t e = c.e;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, g = lane >> 3, m = lane & 7;
+    const unsigned long long nbytes = a.n * ES;
+    const unsigned long long cvec = a.chunk * ES / 16ull;       // vectors per chunk (multiple of 31)
+    const unsigned long long nitc = cvec / 31ull;              // iterations per chunk
+    const unsigned long long it0 = (unsigned long long)k * SFAR_WARPS + warp;
+    const unsigned long long its = (unsigned long long)K * SFAR_WARPS;
+    const size_t slot = a.slot;
+    const uint4 zero = make_uint4(0, 0, 0, 0);
+    uint8_t *rs = a.region, *ag = a.region2;
+
+    // 1. reduce-scatter send
+    if (!c.drop) {
+        for (int i = 0; i < R - 1; ++i) {
+            const int j = peer_of(r, i);
+            uint8_t *dst = rs + ((size_t)(j * 2 + c.par) * R + r) * slot;
+            for (unsigned long long it = it0; it < nitc; it += its) {
+                const uint4 x = lane < 31 ? load_vec<ES>(a.in[r], j * cvec + it * 31ull + lane, nbytes) : zero;
+                ll128_store_data(dst + (it * 4ull + g) * 128ull, m, ll128_pack(x, lane));
+            }
+        }
+        __syncwarp();
+        fence_acq_rel_gpu();
+        for (int i = 0; i < R - 1; ++i) {
+            const int j = peer_of(r, i);
+            uint8_t *dst = rs + ((size_t)(j * 2 + c.par) * R + r) * slot;
+            for (unsigned long long it = it0; it < nitc; it += its)
+                if (m == 0)
+                    st_relaxed_u32((uint32_t *)(dst + (it * 4ull + g) * 128ull), e);
+        }
+    }
+
+    sfar_mid_delay<TEST>(c);
+
+    // 2. owner: receive, reduce, all-gather send
+    const uint8_t *rs_mine = rs + (size_t)(r * 2 + c.par) * R * slot;
+    bool ok = true;
+    for (unsigned long long it = it0; it < nitc; it += its) {
+        const size_t loff = (it * 4ull + g) * 128ull;
+        int lok = 1;
+        for (int i = m; i < R - 1 && lok; i += 8) {
+            const int q = peer_of(r, i);
+            const uint32_t *f = (const uint32_t *)(rs_mine + (size_t)q * slot + loff);
+            SfarWaiter w;
+            while (ld_relaxed_u32(f) != e) {
+                if (w.tick(a.ctl)) {
+                    sfar_record_fault(a.ctl, r, k, q, e, SFAR_WAIT_RS);
+                    lok = 0;
+                    break;
+                }
+            }
+        }
+        ok = __all_sync(SFAR_FULL, lok) != 0;
+        if (!ok)
+            break;
+        fence_acq_rel_gpu();
+        const unsigned long long vb = r * cvec + it * 31ull + lane;
+        const uint4 x = lane < 31 ? load_vec<ES>(a.in[r], vb, nbytes) : zero;
+        const uint4 own = ll128_pack(x, lane);
+        uint4 y[RB];
+#pragma unroll
+        for (int q = 0; q < RB; ++q)
+            if (q < R && q != r)
+                y[q] = ld_relaxed_v4(rs_mine + (size_t)q * slot + loff + 16 * m);
+        SfarAcc<DT> acc;
+        acc.set(r == 0 ? own : y[0]);
+#pragma unroll
+        for (int q = 1; q < RB; ++q)
+            if (q < R)
+                acc.add(q == r ? own : y[q]);
+        const uint4 res = acc.get();
+        if (!c.drop) {
+#pragma unroll
+            for (int i = 0; i < RB - 1; ++i)
+                if (i < R - 1) {
+                    const int p = peer_of(r, i);
+                    ll128_store_data(ag + ((size_t)(p * 2 + c.par) * R + r) * slot + loff, m, res);
+                }
+        }
+        const uint4 o = ll128_unpack(res, lane);
+        if (lane < 31)
+            store_vec<ES>(a.out[r], vb, nbytes, o);
+    }
+    if (ok && !c.drop) {
+        __syncwarp();
+        fence_acq_rel_gpu();
+        for (unsigned long long it = it0; it < nitc; it += its)
+            for (int i = m; i < R - 1; i += 8) {
+                const int p = peer_of(r, i);
+                st_relaxed_u32((uint32_t *)(ag + ((size_t)(p * 2 + c.par) * R + r) * slot + (it * 4ull + g) * 128ull),
+                               e);
+            }
+    }
+
+    // 3. all-gather receive
+    const uint8_t *ag_mine = ag + (size_t)(r * 2 + c.par) * R * slot;
+    for (int i = 0; i < R - 1 && ok; ++i) {
+        const int j = peer_of(r, i);
+        for (unsigned long long it = it0; it < nitc; it += its) {
+            const uint8_t *line = ag_mine + (size_t)j * slot + (it * 4ull + g) * 128ull;
+            int lok = 1;
+            if (m == 0) {
+                SfarWaiter w;
+                while (ld_relaxed_u32((const uint32_t *)line) != e) {
+                    if (w.tick(a.ctl)) {
+                        sfar_record_fault(a.ctl, r, k, j, e, SFAR_WAIT_AG);
+                        lok = 0;
+                        break;
+                    }
+                }
+            }
+            ok = __all_sync(SFAR_FULL, lok) != 0;
+            if (!ok)
+                break;
+            fence_acq_rel_gpu();
+            const uint4 o = ll128_unpack(ld_relaxed_v4(line + 16 * m), lane);
+            if (lane < 31)
+                store_vec<ES>(a.out[r], j * cvec + it * 31ull + lane, nbytes, o);
+        }
+    }
+    sfar_epilogue(a, r, k, e);
+}
+
+const void *sfar_kernel_twoshot(int dt, int wide, int test)
+{
+#define SFAR_PICK(D, W, T)                                        \
+    if (dt == D && wide == W && test == T)                       \
+        return (const void *)k_twoshot<D, (W ? 16 : 8), (T != 0)>;
+    SFAR_PICK(0, 0, 0) SFAR_PICK(0, 0, 1) SFAR_PICK(0, 1, 0) SFAR_PICK(0, 1, 1)
+    SFAR_PICK(1, 0, 0) SFAR_PICK(1, 0, 1) SFAR_PICK(1, 1, 0) SFAR_PICK(1, 1, 1)
+#undef SFAR_PICK
+    return nullptr;
+}

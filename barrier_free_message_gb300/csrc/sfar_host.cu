@@ -1,0 +1,598 @@
+// sfar_host.cu -- the C ABI of libsfar: handle, buffers, launch, status.
+//
+// The handle is the analogue of the pages' LLBuffer object ("Every
+// Microsecond Counts" (page 1), section "Unified primitives and API design":
+// a buffer object that hides the slot layout, the synchronisation mode, the
+// epoch and the reset).  One device allocation holds, for R simulated ranks,
+// the receive regions of every protocol, the flags, the per-(rank, CTA)
+// epoch counters and the status block ("symmetric memory" of the pages
+// becomes regions at fixed offsets of one allocation).  A call validates its
+// arguments on the host and enqueues exactly one kernel; nothing is
+// allocated or synchronised per call, so calls can be captured in a CUDA
+// graph and replayed with no host involvement (the epochs live on the device).
+#include <cuda_runtime.h>
+#include <stdlib.h>
+#include <string.h>
+
+#include <new>
+
+#include "sfar.h"
+#include "sfar_internal.h"
+#include "sfar_test.h"
+
+namespace {
+
+thread_local sfar_status g_last_error = SFAR_OK;
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+size_t ceil_div(size_t x, size_t a) { return (x + a - 1) / a; }
+
+const size_t kTmaMinBytesPerCta = 32u << 10;
+
+}  // namespace
+
+struct sfar {
+    int R = 0;
+    size_t max_bytes = 0;
+    int dt = 0, es = 2;
+    int dev = 0, sms = 0;
+    size_t rb = 0;                      // per-rank limit of the receive-buffer protocols
+    uint8_t *ws = nullptr;
+    size_t ws_bytes = 0;
+    size_t ctl_bytes = 0;               // the status block sits at the start of ws
+    uint32_t *epoch = nullptr, *done = nullptr;
+    uint32_t *fa = nullptr, *fb = nullptr, *fc = nullptr, *fd = nullptr;
+    SfarCtl *ctl = nullptr;
+    uint8_t *r_raw = nullptr, *r_ll = nullptr, *r_ll128 = nullptr, *r_sent = nullptr;
+    uint8_t *r_rs = nullptr, *r_ag = nullptr;
+    size_t s_raw = 0, s_ll = 0, s_ll128 = 0, s_2s = 0, sent_bytes = 0;
+    int mode = SFAR_LAUNCH_SERIAL;
+    int ctas_override = 0;
+    bool k_strag = false, k_drop = false, k_single = false;
+    bool poisoned = false;
+    cudaStream_t priv = nullptr;
+    SfarCtl *host_ctl = nullptr;
+    int kmax[SFAR_NUM_PROTOS] = {};
+    int tma_tb = 0, tma_ns = 0;
+    size_t tma_smem = 0;
+};
+
+static const void *kernel_for(const sfar *h, int p, int test)
+{
+    const int wide = h->R > 8;
+    switch (p) {
+    case SFAR_BASELINE: return sfar_kernel_db(h->dt, wide, test, 1);
+    case SFAR_DB: return sfar_kernel_db(h->dt, wide, test, 0);
+    case SFAR_LL: return sfar_kernel_ll(h->dt, wide, test);
+    case SFAR_LL128: return sfar_kernel_ll128(h->dt, wide, test);
+    case SFAR_SENTINEL: return sfar_kernel_sentinel(h->dt, wide, test);
+    case SFAR_TWOSHOT: return sfar_kernel_twoshot(h->dt, wide, test);
+    case SFAR_TWOSHOT_TMA: return sfar_kernel_tma(h->dt, test);
+    default: return nullptr;
+    }
+}
+
+static int threads_for(int p) { return p == SFAR_TWOSHOT_TMA ? SFAR_TMA_THREADS : SFAR_THREADS; }
+static size_t smem_for(const sfar *h, int p) { return p == SFAR_TWOSHOT_TMA ? h->tma_smem : 0; }
+
+// Launch geometry: CTAs per rank (K) and, for the chunked paths, chunk and
+// per-CTA range in elements.
+static int geometry(const sfar *h, int p, size_t n, size_t *chunk, size_t *sub)
+{
+    const size_t bytes = n * (size_t)h->es;
+    const size_t nvec = ceil_div(bytes, 16);
+    size_t K = 1;
+    *chunk = 0;
+    *sub = 0;
+    switch (p) {
+    case SFAR_BASELINE:
+    case SFAR_DB:
+    case SFAR_LL:
+    case SFAR_SENTINEL:
+        K = ceil_div(nvec, SFAR_THREADS);                     // one 16-byte vector per thread
+        break;
+    case SFAR_LL128:
+        K = ceil_div(ceil_div(nvec, 31), SFAR_WARPS);         // one 4-line group per warp
+        break;
+    case SFAR_TWOSHOT: {
+        const size_t epi = SFAR_ITER_BYTES / (size_t)h->es;   // elements per 4-line group
+        const size_t c = align_up(ceil_div(n, (size_t)h->R), epi);
+        *chunk = c;
+        K = ceil_div(c / epi, SFAR_WARPS);
+        break;
+    }
+    case SFAR_TWOSHOT_TMA: {
+        const size_t g = 16 / (size_t)h->es;
+        const size_t c = align_up(ceil_div(n, (size_t)h->R), g);
+        *chunk = c;
+        K = ceil_div(c * (size_t)h->es, kTmaMinBytesPerCta);
+        break;
+    }
+    default:
+        break;
+    }
+    if (h->ctas_override > 0)
+        K = (size_t)h->ctas_override;
+    if (K < 1)
+        K = 1;
+    if (K > (size_t)h->kmax[p])
+        K = (size_t)h->kmax[p];
+    if (p == SFAR_TWOSHOT_TMA) {
+        const size_t g = 16 / (size_t)h->es;
+        *sub = align_up(ceil_div(*chunk, K), g);
+    }
+    return (int)K;
+}
+
+static sfar_status launch_knob(sfar *h, int which, unsigned long long value, const uint32_t *ptr, uint32_t len,
+                               int rank, cudaStream_t s, int phase = 0)
+{
+    SfarKnobArgs k;
+    memset(&k, 0, sizeof k);
+    k.ctl = h->ctl;
+    k.which = which;
+    k.value = value;
+    k.ptr = ptr;
+    k.len = len;
+    k.rank = rank;
+    k.phase = phase;
+    k.epoch_row0 = h->epoch;
+    void *args[] = {&k};
+    int cur = -1;
+    cudaGetDevice(&cur);
+    if (cur != h->dev)
+        cudaSetDevice(h->dev);
+    cudaError_t err = cudaLaunchKernel(sfar_kernel_set_knob(), dim3(1), dim3(1), args, 0, s);
+    if (cur != h->dev && cur >= 0)
+        cudaSetDevice(cur);
+    if (err != cudaSuccess) {
+        cudaGetLastError();
+        return SFAR_ERR_CUDA;
+    }
+    return SFAR_OK;
+}
+
+extern "C" {
+
+sfar_status sfar_last_error(void) { return g_last_error; }
+
+const char *sfar_strerror(sfar_status st)
+{
+    switch (st) {
+    case SFAR_OK: return "ok";
+    case SFAR_ERR_INVALID: return "invalid argument";
+    case SFAR_ERR_CUDA: return "CUDA runtime error";
+    case SFAR_ERR_OOM: return "out of memory";
+    case SFAR_ERR_TIMEOUT: return "a bounded device wait gave up (lost message or stalled rank)";
+    case SFAR_ERR_UNSUPPORTED: return "unsupported device or launch geometry";
+    case SFAR_ERR_POISONED: return "handle poisoned by an earlier device failure; call sfar_reset";
+    default: return "unknown status";
+    }
+}
+
+sfar_t *sfar_create(int R, size_t max_bytes, sfar_dtype dt)
+{
+    if (R < 2 || R > SFAR_MAX_R || max_bytes == 0 || (dt != SFAR_BF16 && dt != SFAR_FP32)) {
+        g_last_error = SFAR_ERR_INVALID;
+        return nullptr;
+    }
+    int dev = 0, major = 0, minor = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+        cudaGetLastError();
+        g_last_error = SFAR_ERR_CUDA;
+        return nullptr;
+    }
+    if (major != 10 || minor != 3) {
+        g_last_error = SFAR_ERR_UNSUPPORTED;
+        return nullptr;
+    }
+    sfar *h = new (std::nothrow) sfar();
+    if (!h) {
+        g_last_error = SFAR_ERR_OOM;
+        return nullptr;
+    }
+    h->R = R;
+    h->max_bytes = max_bytes;
+    h->dt = (int)dt;
+    h->es = dt == SFAR_BF16 ? 2 : 4;
+    h->dev = dev;
+    h->sms = sms;
+    h->rb = align_up(max_bytes < SFAR_RECV_MAX_BYTES ? max_bytes : SFAR_RECV_MAX_BYTES, 16);
+
+    // slot sizes (bytes per receiver, parity, sender)
+    const size_t nvec = h->rb / 16;
+    h->s_raw = align_up(h->rb, 256);
+    h->s_ll = align_up(2 * h->rb, 256);
+    h->s_ll128 = align_up(ceil_div(nvec, 31) * 512, 256);
+    {
+        const size_t nmax = h->rb / (size_t)h->es;
+        const size_t epi = SFAR_ITER_BYTES / (size_t)h->es;
+        const size_t c = align_up(ceil_div(nmax, (size_t)R), epi);
+        h->s_2s = align_up(c / epi * 512, 256);
+    }
+    const size_t RR2 = (size_t)R * 2 * R;
+    size_t off = 0;
+    auto carve = [&](size_t bytes) {
+        size_t o = off;
+        off = align_up(off + bytes, 256);
+        return o;
+    };
+    const size_t o_ctl = carve(sizeof(SfarCtl));
+    h->ctl_bytes = off;
+    const size_t o_epoch = carve((size_t)R * SFAR_KMAX * 4);
+    const size_t o_done = carve((size_t)R * SFAR_KMAX * 4);
+    const size_t o_fa = carve((size_t)R * R * SFAR_KMAX * 4);
+    const size_t o_fb = carve((size_t)R * R * SFAR_KMAX * 4);
+    const size_t o_fc = carve((size_t)R * SFAR_KMAX * 4);
+    const size_t o_fd = carve((size_t)R * R * SFAR_KMAX * 4);
+    const size_t o_raw = carve(RR2 * h->s_raw);
+    const size_t o_ll = carve(RR2 * h->s_ll);
+    const size_t o_ll128 = carve(RR2 * h->s_ll128);
+    const size_t o_rs = carve(RR2 * h->s_2s);
+    const size_t o_ag = carve(RR2 * h->s_2s);
+    const size_t o_sent = carve(RR2 * h->s_raw);
+    h->sent_bytes = RR2 * h->s_raw;
+    h->ws_bytes = off;
+
+    if (cudaMalloc(&h->ws, h->ws_bytes) != cudaSuccess) {
+        cudaGetLastError();
+        delete h;
+        g_last_error = SFAR_ERR_OOM;
+        return nullptr;
+    }
+    h->ctl = reinterpret_cast<SfarCtl *>(h->ws + o_ctl);
+    h->epoch = reinterpret_cast<uint32_t *>(h->ws + o_epoch);
+    h->done = reinterpret_cast<uint32_t *>(h->ws + o_done);
+    h->fa = reinterpret_cast<uint32_t *>(h->ws + o_fa);
+    h->fb = reinterpret_cast<uint32_t *>(h->ws + o_fb);
+    h->fc = reinterpret_cast<uint32_t *>(h->ws + o_fc);
+    h->fd = reinterpret_cast<uint32_t *>(h->ws + o_fd);
+    h->r_raw = h->ws + o_raw;
+    h->r_ll = h->ws + o_ll;
+    h->r_ll128 = h->ws + o_ll128;
+    h->r_rs = h->ws + o_rs;
+    h->r_ag = h->ws + o_ag;
+    h->r_sent = h->ws + o_sent;
+
+    // TMA path: stage = R tiles of tile_bytes; 4 stages + 2 output buffers
+    {
+        size_t tb = 32768 / (size_t)R;
+        if (tb < 2048) tb = 2048;
+        if (tb > 16384) tb = 16384;
+        tb &= ~(size_t)15;
+        h->tma_tb = (int)tb;
+        h->tma_ns = 4;
+        h->tma_smem = (size_t)h->tma_ns * R * tb + 2 * tb + (size_t)h->tma_ns * 8;
+    }
+
+    SfarCtl init;
+    memset(&init, 0, sizeof init);
+    unsigned long long timeout_ns = 1000000000ull;
+    if (const char *env = getenv("SFAR_TIMEOUT_US")) {
+        const unsigned long long us = strtoull(env, nullptr, 10);
+        if (us > 0)
+            timeout_ns = us * 1000ull;
+    }
+    init.timeout_ns = timeout_ns;
+    init.strag_rank = -1;
+    init.drop_rank = -1;
+    init.f_rank = init.f_cta = init.f_peer = -1;
+
+    sfar_status st = SFAR_OK;
+    if (cudaMemset(h->ws, 0, h->ws_bytes) != cudaSuccess || cudaMemset(h->r_sent, 0xff, h->sent_bytes) != cudaSuccess ||
+        cudaMemcpy(h->ctl, &init, sizeof init, cudaMemcpyHostToDevice) != cudaSuccess ||
+        cudaStreamCreateWithFlags(&h->priv, cudaStreamNonBlocking) != cudaSuccess ||
+        cudaMallocHost(&h->host_ctl, sizeof(SfarCtl)) != cudaSuccess)
+        st = SFAR_ERR_CUDA;
+    for (int test = 0; test < 2 && st == SFAR_OK; ++test) {
+        const void *f = kernel_for(h, SFAR_TWOSHOT_TMA, test);
+        if (cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)h->tma_smem) != cudaSuccess)
+            st = SFAR_ERR_UNSUPPORTED;
+    }
+    for (int p = 0; p < SFAR_NUM_PROTOS && st == SFAR_OK; ++p) {
+        int km = SFAR_KMAX;
+        for (int test = 0; test < 2; ++test) {
+            int nb = 0;
+            if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, kernel_for(h, p, test), threads_for(p),
+                                                              smem_for(h, p)) != cudaSuccess) {
+                st = SFAR_ERR_CUDA;
+                break;
+            }
+            const int k = nb * sms / R;
+            if (k < km)
+                km = k;
+        }
+        if (km < 1)
+            st = SFAR_ERR_UNSUPPORTED;
+        h->kmax[p] = km;
+    }
+    if (st == SFAR_OK && cudaDeviceSynchronize() != cudaSuccess)
+        st = SFAR_ERR_CUDA;
+    if (st != SFAR_OK) {
+        cudaGetLastError();
+        sfar_destroy(h);
+        g_last_error = st;
+        return nullptr;
+    }
+    g_last_error = SFAR_OK;
+    return h;
+}
+
+void sfar_destroy(sfar_t *h)
+{
+    if (!h)
+        return;
+    if (h->ws)
+        cudaFree(h->ws);
+    if (h->host_ctl)
+        cudaFreeHost(h->host_ctl);
+    if (h->priv)
+        cudaStreamDestroy(h->priv);
+    delete h;
+}
+
+size_t sfar_max_bytes(const sfar_t *h, sfar_proto p)
+{
+    if (!h || (int)p < 0 || (int)p >= SFAR_NUM_PROTOS)
+        return 0;
+    return p == SFAR_TWOSHOT_TMA ? h->max_bytes : h->rb;
+}
+
+sfar_status sfar_query_launch(const sfar_t *h, size_t n, sfar_proto p, int *ctas_per_rank, int *threads_per_cta)
+{
+    if (!h || (int)p < 0 || (int)p >= SFAR_NUM_PROTOS)
+        return SFAR_ERR_INVALID;
+    size_t chunk, sub;
+    const int K = geometry(h, p, n, &chunk, &sub);
+    if (ctas_per_rank)
+        *ctas_per_rank = K;
+    if (threads_per_cta)
+        *threads_per_cta = threads_for(p);
+    return SFAR_OK;
+}
+
+sfar_status sfar_allreduce(sfar_t *h, const void *const in[], void *const out[], size_t n, sfar_proto p,
+                           sfar_stream_t s)
+{
+    if (!h || (int)p < 0 || (int)p >= SFAR_NUM_PROTOS)
+        return SFAR_ERR_INVALID;
+    if (h->poisoned)
+        return SFAR_ERR_POISONED;
+    if (n == 0)
+        return SFAR_OK;
+    if (!in || !out || n > ((size_t)-1) / 16)
+        return SFAR_ERR_INVALID;
+    const int R = h->R;
+    const size_t bytes = n * (size_t)h->es;
+    if (bytes > sfar_max_bytes(h, p))
+        return SFAR_ERR_INVALID;
+    for (int r = 0; r < R; ++r) {
+        if (!in[r] || !out[r] || ((uintptr_t)in[r] & 15u) || ((uintptr_t)out[r] & 15u))
+            return SFAR_ERR_INVALID;
+    }
+    // no output may overlap an input or another output
+    for (int i = 0; i < R; ++i) {
+        const uintptr_t o0 = (uintptr_t)out[i], o1 = o0 + bytes;
+        for (int j = 0; j < R; ++j) {
+            const uintptr_t a0 = (uintptr_t)in[j], a1 = a0 + bytes;
+            if (o0 < a1 && a0 < o1)
+                return SFAR_ERR_INVALID;
+            if (j != i) {
+                const uintptr_t b0 = (uintptr_t)out[j], b1 = b0 + bytes;
+                if (o0 < b1 && b0 < o1)
+                    return SFAR_ERR_INVALID;
+            }
+        }
+    }
+
+    SfarArgs a;
+    memset(&a, 0, sizeof a);
+    for (int r = 0; r < R; ++r) {
+        a.in[r] = in[r];
+        a.out[r] = out[r];
+    }
+    size_t chunk = 0, sub = 0;
+    const int K = geometry(h, p, n, &chunk, &sub);
+    a.n = n;
+    a.chunk = chunk;
+    a.sub = sub;
+    a.epoch = h->epoch;
+    a.done = h->done;
+    a.ctl = h->ctl;
+    a.R = R;
+    a.K = K;
+    a.overlap = h->mode == SFAR_LAUNCH_OVERLAP;
+    switch (p) {
+    case SFAR_BASELINE:
+    case SFAR_DB:
+        a.region = h->r_raw;
+        a.slot = h->s_raw;
+        a.fa = h->fa;
+        a.fb = h->fb;
+        break;
+    case SFAR_LL:
+        a.region = h->r_ll;
+        a.slot = h->s_ll;
+        break;
+    case SFAR_LL128:
+        a.region = h->r_ll128;
+        a.slot = h->s_ll128;
+        break;
+    case SFAR_SENTINEL:
+        a.region = h->r_sent;
+        a.slot = h->s_raw;
+        break;
+    case SFAR_TWOSHOT:
+        a.region = h->r_rs;
+        a.region2 = h->r_ag;
+        a.slot = h->s_2s;
+        break;
+    case SFAR_TWOSHOT_TMA:
+        a.fa = h->fc;
+        a.fb = h->fd;
+        a.tile_bytes = h->tma_tb;
+        a.stages = h->tma_ns;
+        break;
+    }
+    const int test = (h->k_strag || h->k_drop || h->k_single) ? 1 : 0;
+
+    cudaLaunchConfig_t cfg;
+    memset(&cfg, 0, sizeof cfg);
+    cfg.gridDim = dim3((unsigned)(R * K));
+    cfg.blockDim = dim3((unsigned)threads_for(p));
+    cfg.dynamicSmemBytes = smem_for(h, p);
+    cfg.stream = (cudaStream_t)s;
+    cudaLaunchAttribute attr[1];
+    if (h->mode == SFAR_LAUNCH_OVERLAP) {
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+    }
+    void *args[] = {&a};
+    int cur = -1;
+    cudaGetDevice(&cur);
+    if (cur != h->dev)
+        cudaSetDevice(h->dev);
+    cudaError_t err = cudaLaunchKernelExC(&cfg, kernel_for(h, p, test), args);
+    if (cur != h->dev && cur >= 0)
+        cudaSetDevice(cur);
+    if (err != cudaSuccess) {
+        cudaGetLastError();
+        return SFAR_ERR_CUDA;
+    }
+    return SFAR_OK;
+}
+
+sfar_status sfar_status_get(sfar_t *h, sfar_fault *info)
+{
+    if (!h)
+        return SFAR_ERR_INVALID;
+    if (cudaMemcpyAsync(h->host_ctl, h->ctl, 32, cudaMemcpyDeviceToHost, h->priv) != cudaSuccess ||
+        cudaStreamSynchronize(h->priv) != cudaSuccess) {
+        cudaGetLastError();
+        return SFAR_ERR_CUDA;
+    }
+    const SfarCtl *c = h->host_ctl;
+    const sfar_status code = c->status;
+    if (info) {
+        info->code = code;
+        info->rank = code ? c->f_rank : -1;
+        info->cta = code ? c->f_cta : -1;
+        info->peer = code ? c->f_peer : -1;
+        info->epoch = code ? c->f_epoch : 0;
+        info->where = code ? c->f_where : 0;
+    }
+    if (code != SFAR_OK)
+        h->poisoned = true;
+    return code;
+}
+
+sfar_status sfar_reset(sfar_t *h, sfar_stream_t s)
+{
+    if (!h)
+        return SFAR_ERR_INVALID;
+    cudaStream_t st = (cudaStream_t)s;
+    if (cudaMemsetAsync(h->ws + h->ctl_bytes, 0, h->ws_bytes - h->ctl_bytes, st) != cudaSuccess ||
+        cudaMemsetAsync(h->r_sent, 0xff, h->sent_bytes, st) != cudaSuccess) {
+        cudaGetLastError();
+        return SFAR_ERR_CUDA;
+    }
+    sfar_status r = launch_knob(h, KNOB_CLEAR_STATUS, 0, nullptr, 0, -1, st);
+    if (r == SFAR_OK)
+        r = launch_knob(h, KNOB_STRAG, 0, nullptr, 0, -1, st);
+    if (r == SFAR_OK)
+        r = launch_knob(h, KNOB_DROP, 0, nullptr, 0, -1, st);
+    if (r != SFAR_OK)
+        return r;
+    h->k_strag = false;
+    h->k_drop = false;
+    h->poisoned = false;
+    return SFAR_OK;
+}
+
+// ------------------------------------------------------------------ test hooks
+sfar_status sfar_test_set_straggler(sfar_t *h, const uint32_t *delays_ns, uint32_t len, int rank, int phase,
+                                    sfar_stream_t s)
+{
+    if (!h || (len > 0 && !delays_ns) || rank >= h->R || (phase != 0 && phase != 1))
+        return SFAR_ERR_INVALID;
+    sfar_status r = launch_knob(h, KNOB_STRAG, 0, delays_ns, len, rank < 0 ? -1 : rank, (cudaStream_t)s, phase);
+    if (r == SFAR_OK)
+        h->k_strag = len > 0;
+    return r;
+}
+
+sfar_status sfar_test_drop_rank(sfar_t *h, int rank, sfar_stream_t s)
+{
+    if (!h || rank >= h->R)
+        return SFAR_ERR_INVALID;
+    sfar_status r = launch_knob(h, KNOB_DROP, 0, nullptr, 0, rank < 0 ? -1 : rank, (cudaStream_t)s);
+    if (r == SFAR_OK)
+        h->k_drop = rank >= 0;
+    return r;
+}
+
+sfar_status sfar_test_set_timeout(sfar_t *h, uint64_t ns, sfar_stream_t s)
+{
+    if (!h || ns == 0)
+        return SFAR_ERR_INVALID;
+    return launch_knob(h, KNOB_TIMEOUT, ns, nullptr, 0, -1, (cudaStream_t)s);
+}
+
+sfar_status sfar_test_force_single_buffer(sfar_t *h, int on, sfar_stream_t s)
+{
+    if (!h)
+        return SFAR_ERR_INVALID;
+    sfar_status r = launch_knob(h, KNOB_SINGLE, on ? 1 : 0, nullptr, 0, -1, (cudaStream_t)s);
+    if (r == SFAR_OK)
+        h->k_single = on != 0;
+    return r;
+}
+
+sfar_status sfar_set_launch_mode(sfar_t *h, int mode)
+{
+    if (!h || (mode != SFAR_LAUNCH_SERIAL && mode != SFAR_LAUNCH_OVERLAP))
+        return SFAR_ERR_INVALID;
+    h->mode = mode;
+    return SFAR_OK;
+}
+
+sfar_status sfar_test_set_ctas(sfar_t *h, int ctas_per_rank)
+{
+    if (!h || ctas_per_rank < 0)
+        return SFAR_ERR_INVALID;
+    h->ctas_override = ctas_per_rank;
+    return SFAR_OK;
+}
+
+sfar_status sfar_probe_empty(sfar_stream_t s)
+{
+    if (cudaLaunchKernel(sfar_kernel_empty(), dim3(1), dim3(32), nullptr, 0, (cudaStream_t)s) != cudaSuccess) {
+        cudaGetLastError();
+        return SFAR_ERR_CUDA;
+    }
+    return SFAR_OK;
+}
+
+sfar_status sfar_probe_pingpong(uint32_t *flags, int trips, uint64_t *ns_out, sfar_stream_t s)
+{
+    if (!flags || !ns_out || trips < 1)
+        return SFAR_ERR_INVALID;
+    // > half of an SM's shared memory each, so the two CTAs sit on different SMs
+    const int smem = 120 * 1024;
+    unsigned long long *ns = reinterpret_cast<unsigned long long *>(ns_out);
+    void *args[] = {&flags, &trips, &ns};
+    if (cudaFuncSetAttribute(sfar_kernel_pingpong(), cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess ||
+        cudaMemsetAsync(flags, 0, 64 * sizeof(uint32_t), (cudaStream_t)s) != cudaSuccess ||
+        cudaLaunchKernel(sfar_kernel_pingpong(), dim3(2), dim3(32), args, smem, (cudaStream_t)s) != cudaSuccess) {
+        cudaGetLastError();
+        return SFAR_ERR_CUDA;
+    }
+    return SFAR_OK;
+}
+
+}  // extern "C"

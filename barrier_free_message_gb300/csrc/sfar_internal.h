@@ -1,0 +1,75 @@
+// sfar_internal.h -- layout shared by the host code and the kernels of libsfar.
+#pragma once
+#include <stddef.h>
+#include <stdint.h>
+
+#define SFAR_MAX_R 16
+#define SFAR_KMAX 128                       // CTAs per rank, upper bound (flag array stride)
+#define SFAR_THREADS 256                    // threads per CTA of the receive-buffer kernels
+#define SFAR_WARPS (SFAR_THREADS / 32)
+#define SFAR_RECV_MAX_BYTES (2ull << 20)    // per-rank limit of the receive-buffer protocols
+#define SFAR_LL128_PAYLOAD 124              // bytes of payload per 128-byte LL128 line
+#define SFAR_ITER_BYTES (4 * SFAR_LL128_PAYLOAD)   // payload of the 4 lines one warp moves at once
+#define SFAR_TMA_THREADS 256
+
+// Device status block of one handle.  The first 32 bytes are the sticky
+// status and the fault record; the knobs follow.
+struct SfarCtl {
+    int status;               // 0 = OK, else SFAR_ERR_TIMEOUT (sticky until reset)
+    int f_rank, f_cta, f_peer;
+    uint32_t f_epoch;
+    int f_where;
+    int pad0[2];
+    unsigned long long timeout_ns;
+    // knobs, read only by the test variants of the kernels
+    const uint32_t *strag_delays;
+    uint32_t strag_len;
+    int strag_rank;           // < 0: rotating (call mod R)
+    int strag_phase;          // 0: before the sends, 1: between sends and receives
+    int drop_rank;            // < 0: none
+    int single_buffer;
+    uint32_t strag_base[SFAR_KMAX];   // epoch of (rank 0, CTA k) when the straggler was armed
+};
+
+// Kernel parameters, passed by value (fits the parameter space).
+struct SfarArgs {
+    const void *in[SFAR_MAX_R];
+    void *out[SFAR_MAX_R];
+    unsigned long long n;         // elements per rank
+    unsigned long long slot;      // bytes per (receiver, parity, sender) slot of `region`
+    unsigned long long chunk;     // two-shot: elements per owner chunk
+    unsigned long long sub;       // TMA path: elements per CTA range within a chunk
+    uint8_t *region;              // receive region of the protocol
+    uint8_t *region2;             // two-shot: all-gather region
+    uint32_t *epoch;              // [R][SFAR_KMAX] call counters
+    uint32_t *done;               // [R][SFAR_KMAX] last finished epoch (overlap mode)
+    uint32_t *fa;                 // flags [R][R][SFAR_KMAX]: ready / top barrier / arrival
+    uint32_t *fb;                 // flags [R][R][SFAR_KMAX]: bottom barrier / completion
+    SfarCtl *ctl;
+    int R, K, overlap, tile_bytes, stages;
+};
+
+// Kernel lookup, one function per translation unit.  dt: 0 bf16, 1 fp32.
+// wide: R > 8.  test: the variant that reads the knobs.
+const void *sfar_kernel_ll(int dt, int wide, int test);
+const void *sfar_kernel_ll128(int dt, int wide, int test);
+const void *sfar_kernel_sentinel(int dt, int wide, int test);
+const void *sfar_kernel_db(int dt, int wide, int test, int baseline);
+const void *sfar_kernel_twoshot(int dt, int wide, int test);
+const void *sfar_kernel_tma(int dt, int test);
+const void *sfar_kernel_set_knob();
+const void *sfar_kernel_empty();
+const void *sfar_kernel_pingpong();
+
+// Knob writes (one-thread kernel): which field and value.
+enum SfarKnob { KNOB_TIMEOUT = 1, KNOB_STRAG = 2, KNOB_DROP = 3, KNOB_SINGLE = 4, KNOB_CLEAR_STATUS = 5 };
+struct SfarKnobArgs {
+    SfarCtl *ctl;
+    int which;
+    unsigned long long value;
+    const uint32_t *ptr;
+    uint32_t len;
+    int rank;
+    int phase;
+    const uint32_t *epoch_row0;   // epoch[0][*] for the straggler base
+};

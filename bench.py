@@ -1,0 +1,474 @@
+#!/usr/bin/env python3
+"""Benchmark of the barrier-free small-message AllReduce on one GB300.
+
+Workload (tensor-parallel decode): R = 8 simulated ranks, 8192 bf16 elements
+per rank (16 KB, hidden 8192, batch 1), values normal(0, 1) with seed 1, 160
+AllReduce calls per simulated token (80 layers x 2), 64 tokens.  Each token's
+160 calls are one CUDA graph; the 64 token graphs use distinct input and
+output buffers (1.34 GB of inputs, larger than L2), and a step is one token.
+
+Printed: ONE JSON line with the headline (microseconds per call of the
+chosen protocol), the per-protocol latencies, the measured floor (empty
+graph-launched kernel + one L2 flag round trip), the end-to-end number
+through the public API with host buffers, the HBM roofline of the
+large-message path, and the CPU oracle timed on the host.
+
+  python bench.py [--steps K] [--warmup W] [--proto ll] [--mode serial]
+  python bench.py --impl reference      # the CPU oracle as the reference arm
+  torchrun ... bench.py --gpus N        # N independent replicas, max over ranks
+"""
+import argparse
+import glob
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from barrier_free_message_gb300 import _build, inputs, sfar  # noqa: E402
+
+METRIC = "AllReduce µs/call at R=8, 16 KB/rank bf16 (graph-chained); GB/s vs HBM peak"
+WORKLOAD = "tp-decode-r8-16k"
+CALLS_PER_STEP = 160
+TOKENS = 64
+PROTOS = ["ll", "ll128", "sentinel", "db", "baseline"]
+
+
+# --------------------------------------------------------------- distributed
+def dist_setup(n_gpus):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(0)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(value: float, world: int) -> float:
+    """Largest value over all ranks (every rank gets it)."""
+    if world <= 1:
+        return value
+    import torch.distributed as dist
+    dev = torch.device("cuda", torch.cuda.current_device()) if dist.get_backend() == "nccl" else torch.device("cpu")
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ["clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.active",
+              "clocks_event_reasons.hw_slowdown", "clocks_event_reasons.hw_thermal_slowdown",
+              "clocks_event_reasons.sw_thermal_slowdown", "clocks_event_reasons.sw_power_cap"]
+    REASONS = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+
+    def __init__(self):
+        self.lines = []
+        self.proc = None
+        self.thread = None
+        try:
+            uuid = str(torch.cuda.get_device_properties(torch.cuda.current_device()).uuid)
+            self.gpu = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+        except Exception:
+            self.gpu = str(torch.cuda.current_device())
+
+    def start(self):
+        cmd = ["nvidia-smi", f"--id={self.gpu}", "--query-gpu=" + ",".join(self.FIELDS),
+               "--format=csv,noheader,nounits", "-lms", "50"]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+        time.sleep(0.15)
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if not self.proc:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.1)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.thread.join(timeout=5)
+        sm, smax, reasons = [], [], set()
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) != len(self.FIELDS):
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+            except ValueError:
+                continue
+            for name, val in zip(self.REASONS, parts[4:]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ----------------------------------------------------------------- helpers
+def measured_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return json.load(f), "measured"
+    except Exception:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}, "fallback"
+
+
+def kernel_sources_hash():
+    h = hashlib.sha256()
+    for p in sorted(glob.glob(os.path.join(ROOT, "barrier_free_message_gb300", "csrc", "*"))):
+        with open(p, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(kernel: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on
+    the current kernel sources; otherwise None."""
+    try:
+        with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+            t = json.load(f)
+        e = t.get(kernel)
+        if e and e.get("sources") == kernel_sources_hash():
+            return e.get("dram_bytes_per_launch")
+    except Exception:
+        pass
+    return None
+
+
+def gen_calls(w, calls):
+    x = torch.empty((calls, w.R, w.n), dtype=torch.bfloat16 if w.dtype == "bf16" else torch.float32)
+    for c in range(calls):
+        x[c] = inputs.draw_workload_call(w, c)
+    return x
+
+
+def capture_token_graphs(h, x_dev, out_dev, proto, tokens):
+    calls, R, n = x_dev.shape
+    graphs = []
+    for t in range(tokens):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for c in range(t * CALLS_PER_STEP, (t + 1) * CALLS_PER_STEP):
+                code = sfar.sfar_allreduce(h.h, [x_dev[c, r].data_ptr() for r in range(R)],
+                                           [out_dev[c, r].data_ptr() for r in range(R)], n, proto)
+                if code != sfar.SFAR_OK:
+                    raise sfar.SfarError(code, "sfar_allreduce during capture")
+        graphs.append(g)
+    return graphs
+
+
+def time_graphs(graphs, steps, warmup, world, sampler=None):
+    stream = torch.cuda.current_stream()
+    for i in range(warmup):
+        graphs[i % len(graphs)].replay()
+    torch.cuda.synchronize()
+    barrier(world)
+    torch.cuda.synchronize()
+    if sampler:
+        sampler.start()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for i in range(steps):
+        graphs[(warmup + i) % len(graphs)].replay()
+    end.record(stream)
+    torch.cuda.synchronize()
+    clocks = sampler.stop() if sampler else None
+    barrier(world)
+    ms = start.elapsed_time(end)
+    return max_over_ranks(ms, world), clocks
+
+
+def check_status(h, what):
+    code, f = sfar.sfar_status_get(h.h)
+    if code != sfar.SFAR_OK:
+        raise RuntimeError(f"{what}: device status {sfar.strerror(code)} (rank {f.rank} cta {f.cta} peer {f.peer} "
+                           f"where {sfar.WAIT_NAMES.get(f.where, f.where)})")
+
+
+def floor_probe():
+    """Empty graph-launched kernel + one L2 flag round trip, in microseconds."""
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for _ in range(CALLS_PER_STEP):
+            assert sfar.sfar_probe_empty() == sfar.SFAR_OK
+    for _ in range(5):
+        g.replay()
+    torch.cuda.synchronize()
+    reps = 50
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s.record()
+    for _ in range(reps):
+        g.replay()
+    e.record()
+    torch.cuda.synchronize()
+    empty_us = s.elapsed_time(e) * 1000.0 / (reps * CALLS_PER_STEP)
+    flags = torch.zeros(64, dtype=torch.int32, device="cuda")
+    ns = torch.zeros(1, dtype=torch.int64, device="cuda")
+    trips = 100000
+    rtts = []
+    for _ in range(3):
+        assert sfar.sfar_probe_pingpong(flags.data_ptr(), trips, ns.data_ptr()) == sfar.SFAR_OK
+        torch.cuda.synchronize()
+        v = int(ns.item())
+        if v < 0 or v == 2**64 - 1:
+            raise RuntimeError("ping-pong probe timed out")
+        rtts.append(v / trips / 1000.0)
+    rtt_us = min(rtts)
+    return {"empty_kernel_us": empty_us, "flag_rtt_us": rtt_us, "floor_us": empty_us + rtt_us}
+
+
+def spot_check(out_dev, x_host, calls):
+    """Bit-exact comparison of a few calls with the CPU oracle."""
+    import oracle
+    for c in calls:
+        want = oracle.allreduce(inputs.to_bits(x_host[c]))
+        got = inputs.to_bits(out_dev[c].cpu())
+        if not np.array_equal(got, want):
+            return False
+    return True
+
+
+def large_message_roofline(peak_gbs, R=8, mb=64, dtype="bf16", iters=10):
+    """HBM roofline of the two-shot TMA path: 2*R*S bytes per call."""
+    n = (mb << 20) // 2
+    h = sfar.Sfar(R, mb << 20, dtype)
+    sets = []
+    for s in range(2):
+        g = torch.Generator(device="cuda").manual_seed(4 * 1000 + s)
+        ins = [torch.randn(n, generator=g, device="cuda").to(torch.bfloat16) for _ in range(R)]
+        outs = [torch.empty_like(t) for t in ins]
+        sets.append((ins, outs))
+    for i in range(3):
+        h.allreduce(*sets[i % 2], "twoshot_tma")
+    torch.cuda.synchronize()
+    s_ev, e_ev = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s_ev.record()
+    for i in range(iters):
+        h.allreduce(*sets[i % 2], "twoshot_tma")
+    e_ev.record()
+    torch.cuda.synchronize()
+    check_status(h, "twoshot_tma")
+    ms = s_ev.elapsed_time(e_ev) / iters
+    ok = all(torch.equal(sets[(iters - 1) % 2][1][r], sets[(iters - 1) % 2][1][0]) for r in range(R))
+    k, _ = h.launch(n, "twoshot_tma")
+    h.close()
+    byts = 2 * R * (mb << 20)
+    gbs = byts / (ms * 1e-3) / 1e9
+    return {"bound": "hbm", "kernel": "k_tma", "workload": f"R={R}, {mb} MB/rank {dtype}, two-shot TMA",
+            "achieved": round(gbs, 1), "peak": peak_gbs, "unit": "GB/s", "frac": round(gbs / peak_gbs, 4),
+            "us_per_call": round(ms * 1000, 2), "algorithmic_bytes": byts, "ctas_per_rank": k,
+            "traffic": profiled_traffic("k_tma"), "ranks_identical": ok}
+
+
+def oracle_cpu_time(x_host, budget_s=10.0, calls_per_step=None):
+    """The oracle as it stands, single-threaded, on a bounded sample of calls."""
+    import oracle
+    xs = [inputs.to_bits(x_host[c]) for c in range(min(len(x_host), 2048))]
+    oracle.allreduce(xs[0])
+    done, t0 = 0, time.perf_counter()
+    while True:
+        oracle.allreduce(xs[done % len(xs)])
+        done += 1
+        if calls_per_step is not None:
+            if done >= calls_per_step:
+                break
+        elif time.perf_counter() - t0 >= budget_s:
+            break
+    dt = time.perf_counter() - t0
+    return dt / done * 1e6, done, dt
+
+
+# ----------------------------------------------------------------- arms
+def run_reference(args, world, rank):
+    if rank != 0:
+        return
+    import oracle  # noqa: F401
+    from oracle.build import build_oracle
+    build_oracle()
+    w = inputs.WORKLOADS[WORKLOAD]
+    x = gen_calls(w, 512)
+    for _ in range(args.warmup):
+        oracle_cpu_time(x, calls_per_step=CALLS_PER_STEP)
+    t0 = time.perf_counter()
+    total_calls = 0
+    for _ in range(args.steps):
+        _, n_calls, _ = oracle_cpu_time(x, calls_per_step=CALLS_PER_STEP)
+        total_calls += n_calls
+    dt = time.perf_counter() - t0
+    us = dt / total_calls * 1e6
+    line = {"impl": "reference", "metric": METRIC, "value": round(us, 3), "unit": "us/call", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt * 1e3 / args.steps, 3),
+            "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic",
+            "config": {"workload": WORKLOAD, "R": w.R, "n": w.n, "bytes_per_rank": w.bytes_per_rank,
+                       "io_dtype": w.dtype, "calls_per_step": CALLS_PER_STEP},
+            "cpu_baseline": {"value": round(us, 3), "unit": "us/call", "cores": 1, "kind": "oracle",
+                             "sample": f"{args.steps} steps x {CALLS_PER_STEP} calls of R=8 x 8192 bf16, "
+                                       f"cycling over 512 generated calls"},
+            "e2e": {"value": round(us, 3), "unit": "us/call", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args, world, rank):
+    _build.build()
+    sfar.lib()
+    w = inputs.WORKLOADS[WORKLOAD]
+    calls = TOKENS * CALLS_PER_STEP
+    peaks, peak_kind = measured_peaks()
+    hbm_peak = float(peaks.get("hbm_gbs", 6800.0))
+
+    x_host = gen_calls(w, calls).pin_memory()
+    x_dev = x_host.cuda()
+    out_dev = torch.empty_like(x_dev)
+    out_host = torch.empty_like(x_host).pin_memory()
+
+    h = sfar.Sfar(w.R, w.bytes_per_rank, w.dtype)
+    h.set_mode(args.mode)
+    protos = [args.proto] + [p for p in PROTOS if p != args.proto]
+    per_proto = {}
+    headline = None
+    for proto in protos:
+        warm_in = [x_dev[0, r] for r in range(w.R)]
+        warm_out = [out_dev[0, r] for r in range(w.R)]
+        h.allreduce(warm_in, warm_out, proto)
+        torch.cuda.synchronize()
+        graphs = capture_token_graphs(h, x_dev, out_dev, proto, TOKENS)
+        sampler = ClockSampler() if proto == args.proto else None
+        ms, clocks = time_graphs(graphs, args.steps, args.warmup, world, sampler)
+        check_status(h, proto)
+        us = ms * 1000.0 / (args.steps * CALLS_PER_STEP)
+        parity = spot_check(out_dev, x_host, [0, 1, calls // 2, calls - 1])
+        per_proto[proto] = {"us_per_call": round(us, 3), "bit_exact_sample": parity}
+        if proto == args.proto:
+            headline = (ms, us, clocks, graphs)
+        else:
+            del graphs
+    ms, us, clocks, graphs = headline
+
+    # end to end: host buffers in, result back, through the public API
+    stream = torch.cuda.current_stream()
+    e2e_steps = min(args.steps, 4 * TOKENS)
+    for i in range(min(args.warmup, 3)):
+        t = i % TOKENS
+        sl = slice(t * CALLS_PER_STEP, (t + 1) * CALLS_PER_STEP)
+        x_dev[sl].copy_(x_host[sl], non_blocking=True)
+        graphs[t].replay()
+        out_host[sl].copy_(out_dev[sl], non_blocking=True)
+    torch.cuda.synchronize()
+    barrier(world)
+    s_ev, e_ev = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s_ev.record(stream)
+    for i in range(e2e_steps):
+        t = i % TOKENS
+        sl = slice(t * CALLS_PER_STEP, (t + 1) * CALLS_PER_STEP)
+        x_dev[sl].copy_(x_host[sl], non_blocking=True)
+        graphs[t].replay()
+        out_host[sl].copy_(out_dev[sl], non_blocking=True)
+    e_ev.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(s_ev.elapsed_time(e_ev), world)
+    e2e_us = e2e_ms * 1000.0 / (e2e_steps * CALLS_PER_STEP)
+    step_bytes = CALLS_PER_STEP * w.R * w.bytes_per_rank
+    e2e_ok = bool(np.array_equal(inputs.to_bits(out_host[0]), inputs.to_bits(out_dev[0].cpu())))
+    del graphs
+    k, threads = h.launch(w.n, args.proto)
+    h.close()
+
+    floor = floor_probe()
+    large = large_message_roofline(hbm_peak) if not args.no_large else None
+
+    cpu = None
+    if rank == 0 and not args.no_cpu:
+        from oracle.build import build_oracle
+        build_oracle()
+        cpu_us, cpu_calls, cpu_s = oracle_cpu_time(x_host, budget_s=args.cpu_seconds)
+        cpu = {"value": round(cpu_us, 3), "unit": "us/call", "cores": 1, "kind": "oracle",
+               "sample": f"{cpu_calls} calls of R=8 x 8192 bf16 (tp-decode), {cpu_s:.1f} s, single thread"}
+
+    if rank != 0:
+        return
+    algo_bytes = 2 * w.R * w.bytes_per_rank
+    hbm_gbs = algo_bytes / (us * 1e-6) / 1e9
+    roofline = {"bound": "latency", "kernel": f"k_{args.proto}", "achieved": round(us, 3),
+                "peak": round(floor["floor_us"], 3), "unit": "us/call",
+                "frac": round(floor["floor_us"] / us, 4),
+                "traffic": profiled_traffic(f"k_{args.proto}"),
+                "algorithmic_bytes": algo_bytes, "hbm_achieved_gbs": round(hbm_gbs, 1),
+                "hbm_frac": round(hbm_gbs / hbm_peak, 5), "peak_kind": "measured floor (" + peak_kind + " HBM)"}
+    line = {"metric": METRIC, "value": round(us, 3), "unit": "us/call", "n_gpus": args.gpus, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(ms / args.steps, 4), "higher_is_better": False,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "R": w.R, "n": w.n, "bytes_per_rank": w.bytes_per_rank,
+                       "io_dtype": w.dtype, "proto": args.proto, "mode": args.mode,
+                       "calls_per_step": CALLS_PER_STEP, "tokens": TOKENS,
+                       "graph": "one CUDA graph per token (160 calls)", "ctas_per_rank": k,
+                       "threads_per_cta": threads,
+                       "l2": "inputs larger than L2: 64 token buffers, 1.34 GB, cycled",
+                       "parallelism": f"replicas x{args.gpus}"},
+            "protocols": per_proto, "floor": {k2: round(v, 3) for k2, v in floor.items()},
+            "vs_floor": round(us / floor["floor_us"], 3),
+            "roofline": roofline, "roofline_large": large,
+            "e2e": {"value": round(e2e_us, 3), "unit": "us/call", "h2d_bytes_per_step": step_bytes,
+                    "d2h_bytes_per_step": step_bytes, "steps": e2e_steps, "result_copied_back": e2e_ok},
+            "gpu_launches": args.steps * CALLS_PER_STEP,
+            "clocks": clocks, "cpu_baseline": cpu}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=640)
+    ap.add_argument("--warmup", type=int, default=8)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--proto", choices=PROTOS, default="ll")
+    ap.add_argument("--mode", choices=["serial", "overlap"], default="serial")
+    ap.add_argument("--no-large", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)
+    world, rank, _ = dist_setup(args.gpus)
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+    else:
+        run_ours(args, world, rank)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,172 @@
+/*
+ * sfar.h -- libsfar: barrier-free small-message AllReduce for R simulated
+ * ranks on one GB300 (sm_103a).
+ *
+ * The operation (all calls below): every rank r holds a vector in[r] of n
+ * elements; afterwards every out[r] holds the element-wise sum over the R
+ * ranks.  "Every Microsecond Counts" (page 1), section "Tensor parallelism
+ * and AllReduce", defines the collective (partial results of all GPUs summed
+ * and handed back to all); section "Unified primitives and API design"
+ * defines recvReduce (receive every peer's value and reduce it in registers).
+ * The sum is a left fold in rank order 0..R-1 with binary32 accumulation
+ * (round to nearest even after every add) and one rounding to the output
+ * type, so the result is unique bit for bit and identical on every rank,
+ * whatever the protocol.
+ *
+ * Simulated ranks: rank r is a group of CTAs of one kernel with its own
+ * receive buffers in HBM; ranks exchange data only by stores into each
+ * other's buffers and synchronise only through flags in global memory.
+ *
+ * Threading: a handle may be used from one host thread at a time.  All
+ * device work is asynchronous on the caller's stream and can be captured in
+ * a CUDA graph (no allocation, no synchronisation inside sfar_allreduce).
+ */
+#ifndef SFAR_H
+#define SFAR_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t; NULL is the legacy default stream. */
+typedef struct CUstream_st *sfar_stream_t;
+
+typedef struct sfar sfar_t;
+
+typedef enum {
+    SFAR_BF16 = 0, /* 2-byte elements, bfloat16 */
+    SFAR_FP32 = 1  /* 4-byte elements, IEEE binary32 */
+} sfar_dtype;
+
+/*
+ * Protocols.  Sources: "Every Microsecond Counts" (page 1), sections
+ * "Global memory barriers" (the two barriers), "Four barrier-free mechanisms"
+ * (LL, sentinel, double buffering, LL128) and "Unified primitives and API
+ * design" (one-shot and two-shot variants, table of variants); "SiFAR"
+ * (page 3), sections "Limits of existing algorithms" (one-shot with top and
+ * bottom barrier, two-shot) and "Technique 1" (double buffering removes the
+ * bottom barrier).
+ */
+typedef enum {
+    SFAR_BASELINE = 0,    /* one-shot, one receive buffer, top AND bottom barrier      */
+    SFAR_DB = 1,          /* one-shot, double-buffered by epoch parity, ready flags
+                             (top barrier) only: the bottom barrier is gone           */
+    SFAR_LL = 2,          /* one-shot, LL packets: 8-byte words {4 B data, 4 B flag}  */
+    SFAR_LL128 = 3,       /* one-shot, 128-byte lines: 4 B flag + 124 B payload       */
+    SFAR_SENTINEL = 4,    /* one-shot, receive buffers prefilled with a NaN pattern   */
+    SFAR_TWOSHOT = 5,     /* reduce-scatter + all-gather over LL128 lines, double
+                             buffered (medium messages)                               */
+    SFAR_TWOSHOT_TMA = 6  /* reduce-scatter + all-gather straight from the inputs to
+                             the outputs with TMA bulk copies (large messages)        */
+} sfar_proto;
+
+#define SFAR_NUM_PROTOS 7
+
+typedef int sfar_status;
+#define SFAR_OK 0
+#define SFAR_ERR_INVALID 1     /* bad argument (rank count, size, pointer, alignment, overlap) */
+#define SFAR_ERR_CUDA 2        /* a CUDA runtime call failed (launch, copy, query)            */
+#define SFAR_ERR_OOM 3         /* device or pinned allocation failed in sfar_create           */
+#define SFAR_ERR_TIMEOUT 4     /* a bounded wait on the device gave up (see sfar_fault)       */
+#define SFAR_ERR_UNSUPPORTED 5 /* this device cannot run the kernels (not sm_103, or the grid
+                                  cannot be co-resident)                                       */
+#define SFAR_ERR_POISONED 6    /* an earlier device-side failure; call sfar_reset             */
+
+/* Where a bounded device wait gave up (sfar_fault.where). */
+#define SFAR_WAIT_DONE 1      /* overlap mode: previous call of the same rank/CTA      */
+#define SFAR_WAIT_LL 2        /* LL packet flag                                        */
+#define SFAR_WAIT_SENTINEL 3  /* sentinel-prefilled slot still holds the sentinel      */
+#define SFAR_WAIT_READY 4     /* ready flag / top barrier                              */
+#define SFAR_WAIT_BOTTOM 5    /* bottom barrier                                        */
+#define SFAR_WAIT_LL128 6     /* LL128 line flag (one-shot)                            */
+#define SFAR_WAIT_RS 7        /* two-shot reduce-scatter line flag                     */
+#define SFAR_WAIT_AG 8        /* two-shot all-gather line flag                         */
+#define SFAR_WAIT_ARRIVE 9    /* TMA path: peer arrival (top barrier)                  */
+#define SFAR_WAIT_COMPLETE 10 /* TMA path: owner completion flags                      */
+#define SFAR_WAIT_COPY 11     /* TMA path: bulk copy completion                        */
+
+typedef struct {
+    sfar_status code; /* SFAR_OK or SFAR_ERR_TIMEOUT                          */
+    int rank;         /* simulated rank whose wait gave up                    */
+    int cta;          /* CTA index within that rank                           */
+    int peer;         /* rank it was waiting for (-1 if not one rank)         */
+    uint32_t epoch;   /* call epoch (starts at 1, +1 per call per CTA)        */
+    int where;        /* SFAR_WAIT_*                                          */
+} sfar_fault;
+
+/*
+ * sfar_create: a handle for R simulated ranks (2 <= R <= 16) on the current
+ * CUDA device, for messages of up to max_bytes per rank (> 0) of type dt.
+ * Allocates, on the current device, the receive regions of every protocol
+ * (double-buffered: [rank][parity][sender][wire bytes]; the sentinel region
+ * prefilled with all-ones), the flag arrays, per-(rank, CTA) epoch counters
+ * and a status block, and zero-initialises them.  The receive-buffer
+ * protocols (every protocol but SFAR_TWOSHOT_TMA) handle up to
+ * min(max_bytes, 2 MiB) per rank; SFAR_TWOSHOT_TMA handles up to max_bytes.
+ * The library owns everything it allocates.  Returns NULL on error and sets
+ * the calling thread's sfar_last_error(): SFAR_ERR_INVALID (bad R, max_bytes
+ * or dt: checked before any CUDA call), SFAR_ERR_UNSUPPORTED (device is not
+ * sm_103), SFAR_ERR_OOM, SFAR_ERR_CUDA.
+ */
+sfar_t *sfar_create(int R, size_t max_bytes, sfar_dtype dt);
+
+/* The error of the calling thread's last failed sfar_create (thread-local). */
+sfar_status sfar_last_error(void);
+
+/*
+ * sfar_allreduce: in and out are HOST arrays of R DEVICE pointers (owned by
+ * the caller); in[r] and out[r] each hold n elements of the handle's dtype,
+ * 16-byte aligned.  No output may overlap an input or another output.
+ * n * element size must not exceed the protocol's limit (see sfar_create).
+ * n == 0 is a no-op.  Enqueues ONE kernel on stream s and returns at once;
+ * capturable in a CUDA graph.  Returns, without enqueuing anything,
+ * SFAR_ERR_INVALID for a bad argument, SFAR_ERR_POISONED after a device-side
+ * failure that sfar_status_get has reported, SFAR_ERR_UNSUPPORTED if the
+ * grid the call needs cannot be co-resident, and SFAR_ERR_CUDA if the launch
+ * fails.  A device-side failure (a bounded wait giving up) does not show
+ * here: it is recorded in the handle's status block (sticky) and every later
+ * kernel of the handle exits at once; read it with sfar_status_get.
+ */
+sfar_status sfar_allreduce(sfar_t *h, const void *const in[], void *const out[], size_t n,
+                           sfar_proto p, sfar_stream_t s);
+
+/*
+ * sfar_status_get: reads the handle's device status block through a private
+ * stream and returns its code (SFAR_OK or SFAR_ERR_TIMEOUT); fills *info if
+ * info is not NULL.  It does not wait for the caller's streams: synchronise
+ * them first to see the outcome of the work enqueued so far.  A non-OK code
+ * poisons the handle on the host too, until sfar_reset.
+ */
+sfar_status sfar_status_get(sfar_t *h, sfar_fault *info);
+
+/*
+ * sfar_reset: enqueues on s the re-initialisation of every flag, epoch and
+ * receive region (sentinel region re-seeded) and clears the status block and
+ * the host-side poison.  The caller must ensure no kernel of this handle is
+ * still running on another stream.
+ */
+sfar_status sfar_reset(sfar_t *h, sfar_stream_t s);
+
+/* sfar_destroy: frees everything the handle owns; NULL is allowed.  The
+ * caller must have synchronised all work enqueued with the handle. */
+void sfar_destroy(sfar_t *h);
+
+/* A static, human-readable string for a status code. */
+const char *sfar_strerror(sfar_status st);
+
+/* Launch geometry of a call (for reports): CTAs per rank and threads per
+ * CTA the kernel would use for n elements under protocol p. */
+sfar_status sfar_query_launch(const sfar_t *h, size_t n, sfar_proto p, int *ctas_per_rank,
+                              int *threads_per_cta);
+
+/* Largest n * element size per rank that protocol p accepts on this handle. */
+size_t sfar_max_bytes(const sfar_t *h, sfar_proto p);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SFAR_H */

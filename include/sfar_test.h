@@ -1,0 +1,84 @@
+/*
+ * sfar_test.h -- test and measurement hooks of libsfar.
+ *
+ * Nothing here is needed to use the AllReduce.  The hooks let tests and the
+ * benchmark delay a simulated rank, drop a rank's sends, shorten the device
+ * wait limit, switch the launch mode and time the latency floor.  Each knob
+ * is a field of the handle's device status block, written by a one-thread
+ * kernel on the given stream, so it takes effect for calls enqueued after it
+ * on that stream.  Calls made while a knob is armed run a kernel variant that
+ * reads the knobs; otherwise the kernels never read them.
+ */
+#ifndef SFAR_TEST_H
+#define SFAR_TEST_H
+
+#include "sfar.h"
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/*
+ * Straggler injection.  The straggler of a workload is the last-arriving
+ * rank, and it sets the latency ("SiFAR" (page 3), sections "Technique 3"
+ * and "Limitations"; the tail-latency discussion of the small-message page).
+ * From the next call on, call i (counted per CTA from the arming point)
+ * delays every CTA of rank (rank < 0 ? i mod R : rank) by delays_ns[i mod len]
+ * nanoseconds (a spin on %globaltimer).  phase 0: the delay comes before the
+ * rank sends anything (a late arrival).  phase 1: it comes after the rank's
+ * sends and before it reads what it received (a slow reader, the case in
+ * which a peer that has moved on could overwrite data not yet read).
+ * delays_ns is a DEVICE array of len uint32 owned by the caller; it must stay
+ * valid while calls that use it run.  len == 0 disarms.
+ */
+sfar_status sfar_test_set_straggler(sfar_t *h, const uint32_t *delays_ns, uint32_t len, int rank, int phase,
+                                    sfar_stream_t s);
+
+/* Rank `rank` (or none if rank < 0) skips every send from the next call on,
+ * so its peers' waits run out: the negative test of the bounded waits. */
+sfar_status sfar_test_drop_rank(sfar_t *h, int rank, sfar_stream_t s);
+
+/* Wait limit of every device poll, in nanoseconds (default 1 s, or the
+ * environment variable SFAR_TIMEOUT_US read by sfar_create). */
+sfar_status sfar_test_set_timeout(sfar_t *h, uint64_t ns, sfar_stream_t s);
+
+/* Use parity 0 for every call of the double-buffered protocols (DB, LL,
+ * LL128, SENTINEL, TWOSHOT): the negative test of double buffering. */
+sfar_status sfar_test_force_single_buffer(sfar_t *h, int on, sfar_stream_t s);
+
+/*
+ * Launch mode.  SFAR_LAUNCH_SERIAL (default): plain stream order, so the end
+ * of each kernel is a full barrier between calls.  SFAR_LAUNCH_OVERLAP:
+ * programmatic dependent launch; each CTA lets the next call's kernel start
+ * as soon as it has taken its epoch, and the next call's CTA (r, k) waits only
+ * for CTA (r, k) of this call (a wait inside one rank, not across ranks).
+ * Calls may then overtake one another across ranks, which is what double
+ * buffering has to survive.  Use OVERLAP only for chains of calls whose
+ * inputs do not depend on the previous call's outputs.
+ */
+#define SFAR_LAUNCH_SERIAL 0
+#define SFAR_LAUNCH_OVERLAP 1
+sfar_status sfar_set_launch_mode(sfar_t *h, int mode);
+
+/* CTAs per rank for every later call (0 = automatic). Clamped to what can
+ * be co-resident. */
+sfar_status sfar_test_set_ctas(sfar_t *h, int ctas_per_rank);
+
+/*
+ * Latency floor probes.
+ * sfar_probe_empty: enqueue one empty kernel (1 CTA, 32 threads) on s.
+ * sfar_probe_pingpong: enqueue one kernel of two CTAs on different SMs that
+ *   pass a token `trips` times through two flags in global memory
+ *   (st.release / ld.acquire at GPU scope); ns_out (device, 1 uint64) gets
+ *   the elapsed %globaltimer nanoseconds.  flags is a device array of 64
+ *   uint32 that the probe zeroes first.  Waits are bounded (1 s); on
+ *   timeout ns_out gets UINT64_MAX.
+ */
+sfar_status sfar_probe_empty(sfar_stream_t s);
+sfar_status sfar_probe_pingpong(uint32_t *flags, int trips, uint64_t *ns_out, sfar_stream_t s);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SFAR_TEST_H */
