@@ -38,7 +38,7 @@ __device__ __forceinline__ bool flag_exchange(const SfarArgs &a, uint32_t *flags
     int ok = 1;
     for (int i = lane; i < R - 1 && ok; i += 32) {
         const int q = peer_of(r, i);
-        if (!poll_flag_ge(flags + ((size_t)r * R + q) * SFAR_KMAX + k, e, a.ctl)) {
+        if (!poll_flag_ge(flags + ((size_t)r * R + q) * SFAR_KMAX + k, e, a.ctl, where == SFAR_WAIT_BOTTOM)) {
             sfar_record_fault(a.ctl, r, k, q, e, where);
             ok = 0;
         }
@@ -52,24 +52,26 @@ template <int DT, int RB, bool TEST, bool BASE>
 __global__ void __launch_bounds__(SFAR_THREADS) k_db(const __grid_constant__ SfarArgs a)
 {
     constexpr int ES = DT == 0 ? 2 : 4;
+    sfar_entry(a);
     const int R = a.R, K = a.K;
     const int r = blockIdx.x / K, k = blockIdx.x - r * K;
+    const unsigned long long nbytes = a.n * ES;
+    const unsigned long long nvec = (nbytes + 15ull) >> 4;
+    const unsigned long long stride = (unsigned long long)K * blockDim.x;
+    const unsigned long long v0 = (unsigned long long)k * blockDim.x + threadIdx.x;
+    const uint4 x0 = load_vec<ES>(a.in[r], v0, nbytes);     // before the prologue's barrier
     SfarCall c;
     if (!sfar_prologue<TEST>(a, r, k, c))
         return;
     const uint32_t e = c.e;
     const int par = BASE ? 0 : c.par;
-    const unsigned long long nbytes = a.n * ES;
-    const unsigned long long nvec = (nbytes + 15ull) >> 4;
-    const unsigned long long stride = (unsigned long long)K * SFAR_THREADS;
-    const unsigned long long v0 = (unsigned long long)k * SFAR_THREADS + threadIdx.x;
     const size_t slot = a.slot;
     __shared__ int s_ok;
 
     // send raw vectors
     if (!c.drop) {
         for (unsigned long long v = v0; v < nvec; v += stride) {
-            const uint4 x = load_vec<ES>(a.in[r], v, nbytes);
+            const uint4 x = v == v0 ? x0 : load_vec<ES>(a.in[r], v, nbytes);
 #pragma unroll
             for (int i = 0; i < RB - 1; ++i) {
                 if (i < R - 1) {
@@ -87,13 +89,14 @@ __global__ void __launch_bounds__(SFAR_THREADS) k_db(const __grid_constant__ Sfa
             s_ok = ok;
     }
     __syncthreads();
+    sfar_stamp<TEST>(c, TP_SENT);      // here: after the top barrier
     // a slow reader (test knob): the data is there, its reads come late
     sfar_mid_delay<TEST>(c);
 
     if (s_ok) {
         const uint8_t *mine = a.region + (size_t)(r * 2 + par) * R * slot;
         for (unsigned long long v = v0; v < nvec; v += stride) {
-            const uint4 own = load_vec<ES>(a.in[r], v, nbytes);
+            const uint4 own = v == v0 ? x0 : load_vec<ES>(a.in[r], v, nbytes);
             uint4 x[RB];
 #pragma unroll
             for (int q = 0; q < RB; ++q)
@@ -114,7 +117,9 @@ __global__ void __launch_bounds__(SFAR_THREADS) k_db(const __grid_constant__ Sfa
                 flag_exchange(a, a.fb, r, k, e, true, SFAR_WAIT_BOTTOM);
         }
     }
+    sfar_stamp<TEST>(c, TP_RECEIVED);
     sfar_epilogue(a, r, k, e);
+    sfar_stamp<TEST>(c, TP_EXIT);
 }
 
 const void *sfar_kernel_db(int dt, int wide, int test, int baseline)

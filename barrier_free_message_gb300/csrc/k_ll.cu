@@ -12,35 +12,59 @@
 // vector v (16 bytes) of sender q lands at bytes [32v, 32v + 32) of slot q as
 // two LL lines {w0,e,w1,e} {w2,e,w3,e}, written as 8-byte words (each word is
 // single-copy atomic, so flag == e proves its data word arrived).
-// Grid: R * K CTAs of 256 threads; CTA (r, k) = blockIdx r * K + k handles
-// vectors k*256 + t + j*K*256 of rank r.  Parity e & 1 double-buffers the
+// Grid: R * K CTAs of T threads; CTA (r, k) = blockIdx r * K + k handles
+// vectors k*T + t + j*K*T of rank r.  Parity e & 1 double-buffers the
 // region: a sender can reach parity e & 1 again only at epoch e + 2, and its
 // CTA (r, k) of epoch e + 1 first received epoch e + 1 data from every peer's
 // CTA k, which each peer sends only after finishing epoch e (section part 3:
 // a received message is the licence to overwrite the previous buffer).
+//
+// Latency: the first input vector is loaded before the prologue's barrier,
+// so its DRAM latency overlaps the epoch ticket; every poll round re-reads
+// all peers that are not ready yet at once, so one round trip covers them all.
 #include "sfar_prims.cuh"
+
+template <int RB>
+struct LLSlots {
+    unsigned long long w0[RB], w1[RB], w2[RB], w3[RB];
+    __device__ __forceinline__ void load(int q, const uint8_t *src)
+    {
+        ld_relaxed_v2u64(src, w0[q], w1[q]);
+        ld_relaxed_v2u64(src + 16, w2[q], w3[q]);
+    }
+    __device__ __forceinline__ bool ready(int q, uint32_t e) const
+    {
+        return ll_ready(w0[q], w1[q], w2[q], w3[q], e);
+    }
+    __device__ __forceinline__ uint4 data(int q) const
+    {
+        return make_uint4((uint32_t)w0[q], (uint32_t)w1[q], (uint32_t)w2[q], (uint32_t)w3[q]);
+    }
+};
 
 template <int DT, int RB, bool TEST>
 __global__ void __launch_bounds__(SFAR_THREADS) k_ll(const __grid_constant__ SfarArgs a)
 {
     constexpr int ES = DT == 0 ? 2 : 4;
+    sfar_entry(a);
     const int R = a.R, K = a.K;
     const int r = blockIdx.x / K, k = blockIdx.x - r * K;
+    const unsigned long long nbytes = a.n * ES;
+    const unsigned long long nvec = (nbytes + 15ull) >> 4;
+    const unsigned long long stride = (unsigned long long)K * blockDim.x;
+    const unsigned long long v0 = (unsigned long long)k * blockDim.x + threadIdx.x;
+    const uint4 x0 = load_vec<ES>(a.in[r], v0, nbytes);     // zero past the end
     SfarCall c;
     if (!sfar_prologue<TEST>(a, r, k, c))
         return;
     const uint32_t e = c.e;
-    const unsigned long long nbytes = a.n * ES;
-    const unsigned long long nvec = (nbytes + 15ull) >> 4;
-    const unsigned long long stride = (unsigned long long)K * SFAR_THREADS;
-    const unsigned long long v0 = (unsigned long long)k * SFAR_THREADS + threadIdx.x;
     const unsigned long long eh = (unsigned long long)e << 32;
     const size_t slot = a.slot;
 
     // send: pack each input vector once, store it into every peer's slot r
     if (!c.drop) {
         for (unsigned long long v = v0; v < nvec; v += stride) {
-            const uint4 x = load_vec<ES>(a.in[r], v, nbytes);
+            const uint4 x = v == v0 ? x0 : load_vec<ES>(a.in[r], v, nbytes);
             const unsigned long long p0 = x.x | eh, p1 = x.y | eh, p2 = x.z | eh, p3 = x.w | eh;
 #pragma unroll
             for (int i = 0; i < RB - 1; ++i) {
@@ -53,54 +77,96 @@ __global__ void __launch_bounds__(SFAR_THREADS) k_ll(const __grid_constant__ Sfa
             }
         }
     }
-
+    sfar_stamp<TEST>(c, TP_SENT);
     sfar_mid_delay<TEST>(c);
+    sfar_poll_delay<TEST>(c);
 
     // receive and reduce: poll every peer's packets, fold in rank order
     const uint8_t *mine = a.region + (size_t)(r * 2 + c.par) * R * slot;
     bool ok = true;
+    // Two rounds of polls are kept in flight, the second issued `stagger`
+    // cycles after the first (set B; R <= 8 only), so a packet that lands
+    // just after one round passed is seen half a round trip later, not a
+    // whole one.  Each round re-reads only the peers not seen yet.
+    constexpr bool TWO_SETS = RB <= 8;
+    const bool stag = TWO_SETS && a.stagger > 0;
     for (unsigned long long v = v0; v < nvec && ok; v += stride) {
-        const uint4 own = load_vec<ES>(a.in[r], v, nbytes);
-        unsigned long long w0[RB], w1[RB], w2[RB], w3[RB];
+        const uint4 own = v == v0 ? x0 : load_vec<ES>(a.in[r], v, nbytes);
+        LLSlots<RB> A;
+        LLSlots<TWO_SETS ? RB : 1> B;
+        bool rdy[RB], fromB[RB];
 #pragma unroll
         for (int q = 0; q < RB; ++q) {
-            if (q < R && q != r) {
-                const uint8_t *src = mine + (size_t)q * slot + v * 32ull;
-                ld_relaxed_v2u64(src, w0[q], w1[q]);
-                ld_relaxed_v2u64(src + 16, w2[q], w3[q]);
-            }
+            rdy[q] = q >= R || q == r;
+            fromB[q] = false;
+            if (!rdy[q])
+                A.load(q, mine + (size_t)q * slot + v * 32ull);
         }
+        if (TWO_SETS && stag) {
+            const long long t0 = clock64();
+            while (clock64() - t0 < a.stagger) {
+            }
 #pragma unroll
-        for (int q = 0; q < RB; ++q) {
-            if (q < R && q != r && ok) {
-                SfarWaiter w;
-                const uint8_t *src = mine + (size_t)q * slot + v * 32ull;
-                while (!ll_ready(w0[q], w1[q], w2[q], w3[q], e)) {
-                    if (w.tick(a.ctl)) {
-                        sfar_record_fault(a.ctl, r, k, q, e, SFAR_WAIT_LL);
-                        ok = false;
-                        break;
+            for (int q = 0; q < (TWO_SETS ? RB : 1); ++q)
+                if (!rdy[q])
+                    B.load(q, mine + (size_t)q * slot + v * 32ull);
+        }
+        SfarWaiter w;
+        while (true) {
+            bool all = true;
+#pragma unroll
+            for (int q = 0; q < RB; ++q) {
+                if (!rdy[q])
+                    rdy[q] = A.ready(q, e);
+                all = all && rdy[q];
+            }
+            if (all)
+                break;
+#pragma unroll
+            for (int q = 0; q < RB; ++q)
+                if (!rdy[q])
+                    A.load(q, mine + (size_t)q * slot + v * 32ull);
+            if (TWO_SETS && stag) {
+                all = true;
+#pragma unroll
+                for (int q = 0; q < (TWO_SETS ? RB : 1); ++q) {
+                    if (!rdy[q] && B.ready(q, e)) {
+                        rdy[q] = true;
+                        fromB[q] = true;
                     }
-                    ld_relaxed_v2u64(src, w0[q], w1[q]);
-                    ld_relaxed_v2u64(src + 16, w2[q], w3[q]);
+                    all = all && rdy[q];
                 }
+                if (all)
+                    break;
+#pragma unroll
+                for (int q = 0; q < (TWO_SETS ? RB : 1); ++q)
+                    if (!rdy[q])
+                        B.load(q, mine + (size_t)q * slot + v * 32ull);
+            }
+            if (w.tick(a.ctl)) {
+                int late = -1;
+#pragma unroll
+                for (int q = RB - 1; q >= 0; --q)
+                    if (!rdy[q])
+                        late = q;
+                sfar_record_fault(a.ctl, r, k, late, e, SFAR_WAIT_LL);
+                ok = false;
+                break;
             }
         }
         if (!ok)
             break;
         SfarAcc<DT> acc;
-        acc.set(r == 0 ? own
-                       : make_uint4((uint32_t)w0[0], (uint32_t)w1[0], (uint32_t)w2[0], (uint32_t)w3[0]));
+        acc.set(r == 0 ? own : (TWO_SETS && fromB[0] ? B.data(0) : A.data(0)));
 #pragma unroll
-        for (int q = 1; q < RB; ++q) {
+        for (int q = 1; q < RB; ++q)
             if (q < R)
-                acc.add(q == r ? own
-                               : make_uint4((uint32_t)w0[q], (uint32_t)w1[q], (uint32_t)w2[q],
-                                            (uint32_t)w3[q]));
-        }
+                acc.add(q == r ? own : (TWO_SETS && fromB[q] ? B.data(q & (TWO_SETS ? RB - 1 : 0)) : A.data(q)));
         store_vec<ES>(a.out[r], v, nbytes, acc.get());
     }
+    sfar_stamp<TEST>(c, TP_RECEIVED);
     sfar_epilogue(a, r, k, e);
+    sfar_stamp<TEST>(c, TP_EXIT);
 }
 
 const void *sfar_kernel_ll(int dt, int wide, int test)

@@ -24,25 +24,28 @@ template <int DT, int RB, bool TEST>
 __global__ void __launch_bounds__(SFAR_THREADS) k_ll128(const __grid_constant__ SfarArgs a)
 {
     constexpr int ES = DT == 0 ? 2 : 4;
+    sfar_entry(a);
     const int R = a.R, K = a.K;
     const int r = blockIdx.x / K, k = blockIdx.x - r * K;
-    SfarCall c;
-    if (!sfar_prologue<TEST>(a, r, k, c))
-        return;
-    const uint32_t e = c.e;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, g = lane >> 3, m = lane & 7;
     const unsigned long long nbytes = a.n * ES;
     const unsigned long long nvec = (nbytes + 15ull) >> 4;
     const unsigned long long nit = (nvec + 30ull) / 31ull;
-    const unsigned long long it0 = (unsigned long long)k * SFAR_WARPS + warp;
-    const unsigned long long its = (unsigned long long)K * SFAR_WARPS;
-    const size_t slot = a.slot;
+    const unsigned long long it0 = (unsigned long long)k * (blockDim.x >> 5) + warp;
+    const unsigned long long its = (unsigned long long)K * (blockDim.x >> 5);
     const uint4 zero = make_uint4(0, 0, 0, 0);
+    // first group's input, loaded before the prologue's barrier
+    const uint4 x0 = lane < 31 ? load_vec<ES>(a.in[r], it0 * 31ull + lane, nbytes) : zero;
+    SfarCall c;
+    if (!sfar_prologue<TEST>(a, r, k, c))
+        return;
+    const uint32_t e = c.e;
+    const size_t slot = a.slot;
 
     // send: payload of every line to every peer, then one fence, then the flags
     if (!c.drop) {
         for (unsigned long long it = it0; it < nit; it += its) {
-            const uint4 x = lane < 31 ? load_vec<ES>(a.in[r], it * 31ull + lane, nbytes) : zero;
+            const uint4 x = it == it0 ? x0 : (lane < 31 ? load_vec<ES>(a.in[r], it * 31ull + lane, nbytes) : zero);
             const uint4 y = ll128_pack(x, lane);
 #pragma unroll
             for (int i = 0; i < RB - 1; ++i) {
@@ -64,6 +67,7 @@ __global__ void __launch_bounds__(SFAR_THREADS) k_ll128(const __grid_constant__ 
             }
     }
 
+    sfar_stamp<TEST>(c, TP_SENT);
     sfar_mid_delay<TEST>(c);
 
     // receive: poll the line flags, read the payload, fold in rank order
@@ -88,7 +92,7 @@ __global__ void __launch_bounds__(SFAR_THREADS) k_ll128(const __grid_constant__ 
         if (!ok)
             break;
         fence_acq_rel_gpu();
-        const uint4 x = lane < 31 ? load_vec<ES>(a.in[r], it * 31ull + lane, nbytes) : zero;
+        const uint4 x = it == it0 ? x0 : (lane < 31 ? load_vec<ES>(a.in[r], it * 31ull + lane, nbytes) : zero);
         const uint4 own = ll128_pack(x, lane);
         uint4 y[RB];
 #pragma unroll
@@ -105,7 +109,9 @@ __global__ void __launch_bounds__(SFAR_THREADS) k_ll128(const __grid_constant__ 
         if (lane < 31)
             store_vec<ES>(a.out[r], it * 31ull + lane, nbytes, res);
     }
+    sfar_stamp<TEST>(c, TP_RECEIVED);
     sfar_epilogue(a, r, k, e);
+    sfar_stamp<TEST>(c, TP_EXIT);
 }
 
 const void *sfar_kernel_ll128(int dt, int wide, int test)

@@ -28,6 +28,15 @@ __global__ void k_set_knob(const SfarKnobArgs k)
     case KNOB_SINGLE:
         c->single_buffer = (int)k.value;
         break;
+    case KNOB_TRACE:
+        c->trace = reinterpret_cast<unsigned long long *>(const_cast<uint32_t *>(k.ptr));
+        c->trace_calls = k.len;
+        for (int i = 0; i < SFAR_KMAX; ++i)
+            c->trace_base[i] = k.epoch_row0[i];
+        break;
+    case KNOB_POLL_DELAY:
+        c->poll_delay_ns = (uint32_t)k.value;
+        break;
     case KNOB_CLEAR_STATUS:
         c->status = 0;
         c->f_rank = c->f_cta = c->f_peer = -1;
@@ -42,8 +51,22 @@ __global__ void k_set_knob(const SfarKnobArgs k)
 __global__ void k_empty() {}
 
 // Two CTAs (forced onto different SMs by their shared-memory size) pass a
-// token back and forth through two flags 128 bytes apart.
-__global__ void k_pingpong(uint32_t *flags, int trips, unsigned long long *ns_out)
+// token back and forth through two flags 128 bytes apart.  relaxed = 0:
+// st.release / ld.acquire at GPU scope (a flag that publishes data); 1:
+// relaxed stores and loads (the cost of the hand-off alone, as in LL).
+__device__ __forceinline__ void pp_store(uint32_t *p, uint32_t v, int relaxed)
+{
+    if (relaxed)
+        st_relaxed_u32(p, v);
+    else
+        st_release_u32(p, v);
+}
+__device__ __forceinline__ uint32_t pp_load(const uint32_t *p, int relaxed)
+{
+    return relaxed ? ld_relaxed_u32(p) : ld_acquire_u32(p);
+}
+
+__global__ void k_pingpong(uint32_t *flags, int trips, int relaxed, unsigned long long *ns_out)
 {
     extern __shared__ uint8_t pad[];
     if (threadIdx.x != 0)
@@ -55,9 +78,9 @@ __global__ void k_pingpong(uint32_t *flags, int trips, unsigned long long *ns_ou
     bool ok = true;
     if (blockIdx.x == 0) {
         for (int i = 1; i <= trips && ok; ++i) {
-            st_release_u32(ping, (uint32_t)i);
+            pp_store(ping, (uint32_t)i, relaxed);
             uint32_t it = 0;
-            while (ld_acquire_u32(pong) != (uint32_t)i)
+            while (pp_load(pong, relaxed) != (uint32_t)i)
                 if ((++it & 255u) == 0 && globaltimer() - start > limit) {
                     ok = false;
                     break;
@@ -69,14 +92,14 @@ __global__ void k_pingpong(uint32_t *flags, int trips, unsigned long long *ns_ou
     } else {
         for (int i = 1; i <= trips && ok; ++i) {
             uint32_t it = 0, v;
-            while ((v = ld_acquire_u32(ping)) != (uint32_t)i) {
+            while ((v = pp_load(ping, relaxed)) != (uint32_t)i) {
                 if (v == 0xffffffffu || ((++it & 255u) == 0 && globaltimer() - start > limit)) {
                     ok = false;
                     break;
                 }
             }
             if (ok)
-                st_release_u32(pong, (uint32_t)i);
+                pp_store(pong, (uint32_t)i, relaxed);
         }
     }
 }

@@ -39,21 +39,23 @@ template <int DT, int RB, bool TEST>
 __global__ void __launch_bounds__(SFAR_THREADS) k_sentinel(const __grid_constant__ SfarArgs a)
 {
     constexpr int ES = DT == 0 ? 2 : 4;
+    sfar_entry(a);
     const int R = a.R, K = a.K;
     const int r = blockIdx.x / K, k = blockIdx.x - r * K;
+    const unsigned long long nbytes = a.n * ES;
+    const unsigned long long nvec = (nbytes + 15ull) >> 4;
+    const unsigned long long stride = (unsigned long long)K * blockDim.x;
+    const unsigned long long v0 = (unsigned long long)k * blockDim.x + threadIdx.x;
+    const uint4 x0 = load_vec<ES>(a.in[r], v0, nbytes);     // before the prologue's barrier
     SfarCall c;
     if (!sfar_prologue<TEST>(a, r, k, c))
         return;
     const uint32_t e = c.e;
-    const unsigned long long nbytes = a.n * ES;
-    const unsigned long long nvec = (nbytes + 15ull) >> 4;
-    const unsigned long long stride = (unsigned long long)K * SFAR_THREADS;
-    const unsigned long long v0 = (unsigned long long)k * SFAR_THREADS + threadIdx.x;
     const size_t slot = a.slot;
 
     if (!c.drop) {
         for (unsigned long long v = v0; v < nvec; v += stride) {
-            const uint4 x = load_vec<ES>(a.in[r], v, nbytes);
+            const uint4 x = v == v0 ? x0 : load_vec<ES>(a.in[r], v, nbytes);
 #pragma unroll
             for (int i = 0; i < RB - 1; ++i) {
                 if (i < R - 1) {
@@ -64,29 +66,76 @@ __global__ void __launch_bounds__(SFAR_THREADS) k_sentinel(const __grid_constant
         }
     }
 
+    sfar_stamp<TEST>(c, TP_SENT);
     sfar_mid_delay<TEST>(c);
+    sfar_poll_delay<TEST>(c);
     uint8_t *mine = a.region + (size_t)(r * 2 + c.par) * R * slot;
     const uint4 sent = make_uint4(0xffffffffu, 0xffffffffu, 0xffffffffu, 0xffffffffu);
+    constexpr bool TWO_SETS = RB <= 8;
+    const bool stag = TWO_SETS && a.stagger > 0;
     bool ok = true;
     for (unsigned long long v = v0; v < nvec && ok; v += stride) {
-        const uint4 own = load_vec<ES>(a.in[r], v, nbytes);
-        uint4 x[RB];
-#pragma unroll
-        for (int q = 0; q < RB; ++q)
-            if (q < R && q != r)
-                x[q] = ld_relaxed_v4(mine + (size_t)q * slot + v * 16ull);
+        const uint4 own = v == v0 ? x0 : load_vec<ES>(a.in[r], v, nbytes);
+        // every round re-reads all peers still holding the sentinel at once;
+        // with R <= 8 a second round (y) runs `stagger` cycles behind the first
+        uint4 x[RB], y[TWO_SETS ? RB : 1];
+        bool rdy[RB];
 #pragma unroll
         for (int q = 0; q < RB; ++q) {
-            if (q < R && q != r && ok) {
-                SfarWaiter w;
-                while (has_sentinel<DT>(x[q])) {
-                    if (w.tick(a.ctl)) {
-                        sfar_record_fault(a.ctl, r, k, q, e, SFAR_WAIT_SENTINEL);
-                        ok = false;
-                        break;
-                    }
+            rdy[q] = q >= R || q == r;
+            if (!rdy[q])
+                x[q] = ld_relaxed_v4(mine + (size_t)q * slot + v * 16ull);
+        }
+        if (TWO_SETS && stag) {
+            const long long t0 = clock64();
+            while (clock64() - t0 < a.stagger) {
+            }
+#pragma unroll
+            for (int q = 0; q < (TWO_SETS ? RB : 1); ++q)
+                if (!rdy[q])
+                    y[q] = ld_relaxed_v4(mine + (size_t)q * slot + v * 16ull);
+        }
+        SfarWaiter w;
+        while (true) {
+            bool all = true;
+#pragma unroll
+            for (int q = 0; q < RB; ++q) {
+                if (!rdy[q])
+                    rdy[q] = !has_sentinel<DT>(x[q]);
+                all = all && rdy[q];
+            }
+            if (all)
+                break;
+#pragma unroll
+            for (int q = 0; q < RB; ++q)
+                if (!rdy[q])
                     x[q] = ld_relaxed_v4(mine + (size_t)q * slot + v * 16ull);
+            if (TWO_SETS && stag) {
+                all = true;
+#pragma unroll
+                for (int q = 0; q < (TWO_SETS ? RB : 1); ++q) {
+                    if (!rdy[q] && !has_sentinel<DT>(y[q])) {
+                        rdy[q] = true;
+                        x[q] = y[q];
+                    }
+                    all = all && rdy[q];
                 }
+                if (all)
+                    break;
+#pragma unroll
+                for (int q = 0; q < (TWO_SETS ? RB : 1); ++q)
+                    if (!rdy[q])
+                        y[q] = ld_relaxed_v4(mine + (size_t)q * slot + v * 16ull);
+            }
+            if (w.tick(a.ctl)) {
+                int late = -1;
+#pragma unroll
+                for (int q = RB - 1; q >= 0; --q)
+                    if (!rdy[q])
+                        late = q;
+                sfar_record_fault(a.ctl, r, k, late, e, SFAR_WAIT_SENTINEL);
+                ok = false;
+                break;
             }
         }
         if (!ok)
@@ -104,7 +153,9 @@ __global__ void __launch_bounds__(SFAR_THREADS) k_sentinel(const __grid_constant
             if (q < R && q != r)
                 st_relaxed_v4(mine + (size_t)q * slot + v * 16ull, sent);
     }
+    sfar_stamp<TEST>(c, TP_RECEIVED);
     sfar_epilogue(a, r, k, e);
+    sfar_stamp<TEST>(c, TP_EXIT);
 }
 
 const void *sfar_kernel_sentinel(int dt, int wide, int test)

@@ -9,12 +9,15 @@
 // reduced chunk once into every rank's output, with no staging buffers.
 //
 // Owner CTA (j, k) takes a contiguous range of chunk j and streams it in
-// tiles: one thread issues, per tile, R 1-D bulk copies
-// (cp.async.bulk global -> shared, completion on an mbarrier) into a ring of
-// stages; all threads fold the R tiles from shared memory in rank order,
-// round once, write the tile to a shared output buffer; one thread then
-// issues R bulk copies shared -> global, one per rank's output.  No
-// multicast and no bulk reduction (its order of additions is not fixed).
+// tiles through a ring of shared-memory stages.  Per tile, the lanes of warp
+// 0 issue one 1-D bulk copy each (lane q: rank q's input, global -> shared,
+// completion counted in bytes on the stage's mbarrier); all threads fold the
+// R tiles from shared memory in rank order, round once and write the tile
+// into one of three shared output buffers; then lane p of warp 0 issues the
+// bulk copy shared -> global into rank p's output.  A buffer is reused only
+// after the copies that read it have finished reading (wait_group.read).
+// No multicast and no bulk reduction (its order of additions is not fixed).
+// Streaming copies carry an L2 evict-first hint: every byte is touched once.
 //
 // Synchronisation between simulated ranks (the pages' counters reaching N,
 // page 1 section "Four barrier-free mechanisms", part 4, kept as flags):
@@ -26,6 +29,8 @@
 //     all owners before it reports its call finished.
 // No receive buffers, so nothing to double-buffer and no bottom barrier.
 #include "sfar_prims.cuh"
+
+#define TMA_OUT_BUFS 3
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p)
 {
@@ -51,19 +56,27 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t phase)
         : "memory");
     return ok != 0;
 }
-__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar)
+__device__ __forceinline__ uint64_t policy_evict_first()
 {
-    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
-                 "l"(src), "r"(bytes), "r"(bar)
-                 : "memory");
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
 }
-__device__ __forceinline__ void bulk_s2g(void *dst, uint32_t src, uint32_t bytes)
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar, uint64_t pol)
 {
-    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst), "r"(src), "r"(bytes)
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(dst),
+        "l"(src), "r"(bytes), "r"(bar), "l"(pol)
+        : "memory");
+}
+__device__ __forceinline__ void bulk_s2g(void *dst, uint32_t src, uint32_t bytes, uint64_t pol)
+{
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group.L2::cache_hint [%0], [%1], %2, %3;" ::"l"(dst), "r"(src),
+                 "r"(bytes), "l"(pol)
                  : "memory");
 }
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
-__device__ __forceinline__ void bulk_wait_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read1() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
 __device__ __forceinline__ void bulk_wait0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 __device__ __forceinline__ void fence_proxy_async_smem()
 {
@@ -78,6 +91,7 @@ template <int DT, bool TEST>
 __global__ void __launch_bounds__(SFAR_TMA_THREADS, 1) k_tma(const __grid_constant__ SfarArgs a)
 {
     constexpr int ES = DT == 0 ? 2 : 4;
+    sfar_entry(a);
     const int R = a.R, K = a.K;
     const int r = blockIdx.x / K, k = blockIdx.x - r * K;
     const int tid = threadIdx.x, lane = tid & 31;
@@ -126,10 +140,11 @@ __global__ void __launch_bounds__(SFAR_TMA_THREADS, 1) k_tma(const __grid_consta
 
     extern __shared__ __align__(128) uint8_t smem[];
     uint8_t *stage0 = smem;                                           // [NS][R][TB]
-    uint8_t *obuf = smem + (size_t)NS * R * TB;                       // [2][TB]
-    uint64_t *bars = reinterpret_cast<uint64_t *>(obuf + 2 * (size_t)TB);
+    uint8_t *obuf = smem + (size_t)NS * R * TB;                       // [TMA_OUT_BUFS][TB]
+    uint64_t *bars = reinterpret_cast<uint64_t *>(obuf + (size_t)TMA_OUT_BUFS * TB);
 
     if (ok && ntiles > 0) {
+        const uint64_t pol = policy_evict_first();
         if (tid == 0) {
             for (int s = 0; s < NS; ++s)
                 mbar_init(smem_u32(bars + s), 1);
@@ -137,16 +152,20 @@ __global__ void __launch_bounds__(SFAR_TMA_THREADS, 1) k_tma(const __grid_consta
             fence_proxy_async_smem();
         }
         __syncthreads();
+        // warp 0 only: lane 0 arms the stage's byte count, lane q copies rank q's tile
         auto issue = [&](unsigned long long t) {
             const int s = (int)(t % NS);
             const unsigned long long off = t * TB;
             const uint32_t tb = (uint32_t)((len16 - off) < TB ? (len16 - off) : TB);
             const uint32_t bar = smem_u32(bars + s);
-            mbar_expect_tx(bar, tb * (uint32_t)R);
-            for (int q = 0; q < R; ++q)
-                bulk_g2s(smem_u32(stage0 + ((size_t)s * R + q) * TB), (const uint8_t *)a.in[q] + b0 + off, tb, bar);
+            if (lane == 0)
+                mbar_expect_tx(bar, tb * (uint32_t)R);
+            __syncwarp();
+            for (int q = lane; q < R; q += 32)
+                bulk_g2s(smem_u32(stage0 + ((size_t)s * R + q) * TB), (const uint8_t *)a.in[q] + b0 + off, tb, bar,
+                         pol);
         };
-        if (tid == 0)
+        if (tid < 32)
             for (unsigned long long t = 0; t < ntiles && t < (unsigned long long)NS; ++t)
                 issue(t);
 
@@ -168,7 +187,7 @@ __global__ void __launch_bounds__(SFAR_TMA_THREADS, 1) k_tma(const __grid_consta
                 }
             }
             const uint8_t *st = stage0 + (size_t)s * R * TB;
-            uint8_t *ob = obuf + (size_t)(t & 1ull) * TB;
+            uint8_t *ob = obuf + (size_t)(t % TMA_OUT_BUFS) * TB;
             if (tok) {
                 for (uint32_t u = tid * 16u; u < tb; u += SFAR_TMA_THREADS * 16u) {
                     SfarAcc<DT> acc;
@@ -179,21 +198,23 @@ __global__ void __launch_bounds__(SFAR_TMA_THREADS, 1) k_tma(const __grid_consta
                 }
                 fence_proxy_async_smem();
             }
-            if (tid == 0)
-                bulk_wait_read0();    // the previous tile's stores have read their buffer
+            // the stores of tile t - 1 may still be reading; those of t - 2
+            // (whose buffer tile t + 1 reuses) must be done
+            if (tid < 32)
+                bulk_wait_read1();
             if (!__syncthreads_and(tok)) {
                 ok = false;
                 break;
             }
-            if (tid == 0) {
-                for (int p = 0; p < R; ++p)
-                    bulk_s2g((uint8_t *)a.out[p] + b0 + off, smem_u32(ob), tb);
+            if (tid < 32) {
+                for (int p = lane; p < R; p += 32)
+                    bulk_s2g((uint8_t *)a.out[p] + b0 + off, smem_u32(ob), tb, pol);
                 bulk_commit();
                 if (t + NS < ntiles)
                     issue(t + NS);      // every thread has finished reading stage s
             }
         }
-        if (tid == 0) {
+        if (tid < 32) {
             bulk_wait0();               // stores complete before completion is signalled
             fence_proxy_async_global();
         }
@@ -231,7 +252,7 @@ __global__ void __launch_bounds__(SFAR_TMA_THREADS, 1) k_tma(const __grid_consta
         int wok = ok ? 1 : 0;
         for (int i = lane; i < R - 1 && wok; i += 32) {
             const int q = peer_of(r, i);
-            if (!poll_flag_ge(cmpl + ((size_t)r * R + q) * SFAR_KMAX + k, e, a.ctl)) {
+            if (!poll_flag_ge(cmpl + ((size_t)r * R + q) * SFAR_KMAX + k, e, a.ctl, true)) {
                 sfar_record_fault(a.ctl, r, k, q, e, SFAR_WAIT_COMPLETE);
                 wok = 0;
             }
@@ -239,7 +260,9 @@ __global__ void __launch_bounds__(SFAR_TMA_THREADS, 1) k_tma(const __grid_consta
         __syncwarp();
         fence_acq_rel_gpu();
     }
+    sfar_stamp<TEST>(c, TP_RECEIVED);
     sfar_epilogue(a, r, k, e);
+    sfar_stamp<TEST>(c, TP_EXIT);
 }
 
 const void *sfar_kernel_tma(int dt, int test)

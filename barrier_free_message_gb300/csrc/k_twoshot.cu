@@ -30,6 +30,7 @@ template <int DT, int RB, bool TEST>
 __global__ void __launch_bounds__(SFAR_THREADS) k_twoshot(const __grid_constant__ SfarArgs a)
 {
     constexpr int ES = DT == 0 ? 2 : 4;
+    sfar_entry(a);
     const int R = a.R, K = a.K;
     const int r = blockIdx.x / K, k = blockIdx.x - r * K;
     SfarCall c;
@@ -40,8 +41,8 @@ __global__ void __launch_bounds__(SFAR_THREADS) k_twoshot(const __grid_constant_
     const unsigned long long nbytes = a.n * ES;
     const unsigned long long cvec = a.chunk * ES / 16ull;       // vectors per chunk (multiple of 31)
     const unsigned long long nitc = cvec / 31ull;              // iterations per chunk
-    const unsigned long long it0 = (unsigned long long)k * SFAR_WARPS + warp;
-    const unsigned long long its = (unsigned long long)K * SFAR_WARPS;
+    const unsigned long long it0 = (unsigned long long)k * (blockDim.x >> 5) + warp;
+    const unsigned long long its = (unsigned long long)K * (blockDim.x >> 5);
     const size_t slot = a.slot;
     const uint4 zero = make_uint4(0, 0, 0, 0);
     uint8_t *rs = a.region, *ag = a.region2;
@@ -67,6 +68,7 @@ __global__ void __launch_bounds__(SFAR_THREADS) k_twoshot(const __grid_constant_
         }
     }
 
+    sfar_stamp<TEST>(c, TP_SENT);
     sfar_mid_delay<TEST>(c);
 
     // 2. owner: receive, reduce, all-gather send
@@ -137,7 +139,7 @@ __global__ void __launch_bounds__(SFAR_THREADS) k_twoshot(const __grid_constant_
             const uint8_t *line = ag_mine + (size_t)j * slot + (it * 4ull + g) * 128ull;
             int lok = 1;
             if (m == 0) {
-                SfarWaiter w;
+                SfarWaiter w(true);
                 while (ld_relaxed_u32((const uint32_t *)line) != e) {
                     if (w.tick(a.ctl)) {
                         sfar_record_fault(a.ctl, r, k, j, e, SFAR_WAIT_AG);
@@ -155,7 +157,9 @@ __global__ void __launch_bounds__(SFAR_THREADS) k_twoshot(const __grid_constant_
                 store_vec<ES>(a.out[r], j * cvec + it * 31ull + lane, nbytes, o);
         }
     }
+    sfar_stamp<TEST>(c, TP_RECEIVED);
     sfar_epilogue(a, r, k, e);
+    sfar_stamp<TEST>(c, TP_EXIT);
 }
 
 const void *sfar_kernel_twoshot(int dt, int wide, int test)

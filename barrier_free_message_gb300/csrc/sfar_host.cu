@@ -47,12 +47,13 @@ struct sfar {
     uint8_t *r_rs = nullptr, *r_ag = nullptr;
     size_t s_raw = 0, s_ll = 0, s_ll128 = 0, s_2s = 0, sent_bytes = 0;
     int mode = SFAR_LAUNCH_SERIAL;
-    int ctas_override = 0;
-    bool k_strag = false, k_drop = false, k_single = false;
+    int ctas_override = 0, threads_override = 0;
+    int stagger = 0;                    // cycles between the two poll rounds (LL, sentinel)
+    bool k_strag = false, k_drop = false, k_single = false, k_trace = false, k_poll = false;
     bool poisoned = false;
     cudaStream_t priv = nullptr;
     SfarCtl *host_ctl = nullptr;
-    int kmax[SFAR_NUM_PROTOS] = {};
+    int kmax[SFAR_NUM_PROTOS][SFAR_NTHREAD_OPTS] = {};   // co-resident CTAs per rank
     int tma_tb = 0, tma_ns = 0;
     size_t tma_smem = 0;
 };
@@ -72,55 +73,81 @@ static const void *kernel_for(const sfar *h, int p, int test)
     }
 }
 
-static int threads_for(int p) { return p == SFAR_TWOSHOT_TMA ? SFAR_TMA_THREADS : SFAR_THREADS; }
 static size_t smem_for(const sfar *h, int p) { return p == SFAR_TWOSHOT_TMA ? h->tma_smem : 0; }
 
-// Launch geometry: CTAs per rank (K) and, for the chunked paths, chunk and
-// per-CTA range in elements.
-static int geometry(const sfar *h, int p, size_t n, size_t *chunk, size_t *sub)
+// Thread counts a receive-buffer kernel may be launched with (index ti).
+static const int kThreadOpts[SFAR_NTHREAD_OPTS] = {64, 128, 256};
+
+static int thread_index(int threads)
 {
-    const size_t bytes = n * (size_t)h->es;
-    const size_t nvec = ceil_div(bytes, 16);
-    size_t K = 1;
+    for (int i = 0; i < SFAR_NTHREAD_OPTS; ++i)
+        if (kThreadOpts[i] == threads)
+            return i;
+    return -1;
+}
+
+// Work units of a call: 16-byte vectors (one-shot vector protocols), 4-line
+// groups per warp (LL128, two-shot), or bytes of a chunk (TMA path).
+static size_t work_units(const sfar *h, int p, size_t n, size_t *chunk)
+{
+    const size_t nvec = ceil_div(n * (size_t)h->es, 16);
     *chunk = 0;
-    *sub = 0;
     switch (p) {
-    case SFAR_BASELINE:
-    case SFAR_DB:
-    case SFAR_LL:
-    case SFAR_SENTINEL:
-        K = ceil_div(nvec, SFAR_THREADS);                     // one 16-byte vector per thread
-        break;
     case SFAR_LL128:
-        K = ceil_div(ceil_div(nvec, 31), SFAR_WARPS);         // one 4-line group per warp
-        break;
+        return ceil_div(nvec, 31);
     case SFAR_TWOSHOT: {
         const size_t epi = SFAR_ITER_BYTES / (size_t)h->es;   // elements per 4-line group
-        const size_t c = align_up(ceil_div(n, (size_t)h->R), epi);
-        *chunk = c;
-        K = ceil_div(c / epi, SFAR_WARPS);
-        break;
+        *chunk = align_up(ceil_div(n, (size_t)h->R), epi);
+        return *chunk / epi;
     }
-    case SFAR_TWOSHOT_TMA: {
-        const size_t g = 16 / (size_t)h->es;
-        const size_t c = align_up(ceil_div(n, (size_t)h->R), g);
-        *chunk = c;
-        K = ceil_div(c * (size_t)h->es, kTmaMinBytesPerCta);
-        break;
-    }
+    case SFAR_TWOSHOT_TMA:
+        *chunk = align_up(ceil_div(n, (size_t)h->R), 16 / (size_t)h->es);
+        return *chunk * (size_t)h->es;
     default:
-        break;
+        return nvec;
+    }
+}
+
+// Launch geometry: CTAs per rank (K), threads per CTA and, for the chunked
+// paths, chunk and per-CTA range in elements.  Without an override, the
+// receive-buffer kernels take the smallest CTA that keeps one work unit per
+// thread (or per warp) while the whole grid fits on the SMs once, so the
+// R * K CTAs spread over as many SMs as the message can use.
+static int geometry(const sfar *h, int p, size_t n, size_t *chunk, size_t *sub, int *threads)
+{
+    const size_t units = work_units(h, p, n, chunk);
+    *sub = 0;
+    const bool warp_units = p == SFAR_LL128 || p == SFAR_TWOSHOT;
+    int ti = SFAR_NTHREAD_OPTS - 1;
+    size_t K = 1;
+    if (p == SFAR_TWOSHOT_TMA) {
+        *threads = SFAR_TMA_THREADS;
+        ti = 0;
+        K = ceil_div(units, kTmaMinBytesPerCta);
+    } else {
+        if (h->threads_override > 0 && thread_index(h->threads_override) >= 0) {
+            ti = thread_index(h->threads_override);
+        } else {
+            for (int i = 0; i < SFAR_NTHREAD_OPTS; ++i) {
+                const size_t per = warp_units ? (size_t)kThreadOpts[i] / 32 : (size_t)kThreadOpts[i];
+                if ((size_t)h->R * ceil_div(units, per) <= (size_t)h->sms) {
+                    ti = i;
+                    break;
+                }
+            }
+        }
+        *threads = kThreadOpts[ti];
+        const size_t per = warp_units ? (size_t)*threads / 32 : (size_t)*threads;
+        K = ceil_div(units, per);
     }
     if (h->ctas_override > 0)
         K = (size_t)h->ctas_override;
     if (K < 1)
         K = 1;
-    if (K > (size_t)h->kmax[p])
-        K = (size_t)h->kmax[p];
-    if (p == SFAR_TWOSHOT_TMA) {
-        const size_t g = 16 / (size_t)h->es;
-        *sub = align_up(ceil_div(*chunk, K), g);
-    }
+    if (K > (size_t)h->kmax[p][ti])
+        K = (size_t)h->kmax[p][ti];
+    if (p == SFAR_TWOSHOT_TMA)
+        *sub = align_up(ceil_div(*chunk, K), 16 / (size_t)h->es);
     return (int)K;
 }
 
@@ -257,15 +284,20 @@ sfar_t *sfar_create(int R, size_t max_bytes, sfar_dtype dt)
     h->r_ag = h->ws + o_ag;
     h->r_sent = h->ws + o_sent;
 
-    // TMA path: stage = R tiles of tile_bytes; 4 stages + 2 output buffers
+    // TMA path: a stage holds R tiles (about 48 KB in all); as many stages as
+    // fit in 220 KB of shared memory next to 3 output buffers, 2 to 8
     {
-        size_t tb = 32768 / (size_t)R;
+        size_t tb = 49152 / (size_t)R;
         if (tb < 2048) tb = 2048;
         if (tb > 16384) tb = 16384;
         tb &= ~(size_t)15;
+        const size_t budget = 220u << 10, outb = 3 * tb;
+        size_t ns = (budget - outb) / ((size_t)R * tb);
+        if (ns < 2) ns = 2;
+        if (ns > 8) ns = 8;
         h->tma_tb = (int)tb;
-        h->tma_ns = 4;
-        h->tma_smem = (size_t)h->tma_ns * R * tb + 2 * tb + (size_t)h->tma_ns * 8;
+        h->tma_ns = (int)ns;
+        h->tma_smem = ns * R * tb + outb + ns * 8;
     }
 
     SfarCtl init;
@@ -292,22 +324,28 @@ sfar_t *sfar_create(int R, size_t max_bytes, sfar_dtype dt)
         if (cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)h->tma_smem) != cudaSuccess)
             st = SFAR_ERR_UNSUPPORTED;
     }
+    // co-residency: every CTA of a call must be resident at once (ranks wait
+    // on each other), so K is capped by the occupancy of each variant
     for (int p = 0; p < SFAR_NUM_PROTOS && st == SFAR_OK; ++p) {
-        int km = SFAR_KMAX;
-        for (int test = 0; test < 2; ++test) {
-            int nb = 0;
-            if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, kernel_for(h, p, test), threads_for(p),
-                                                              smem_for(h, p)) != cudaSuccess) {
-                st = SFAR_ERR_CUDA;
-                break;
+        const int nopts = p == SFAR_TWOSHOT_TMA ? 1 : SFAR_NTHREAD_OPTS;
+        for (int ti = 0; ti < nopts && st == SFAR_OK; ++ti) {
+            const int threads = p == SFAR_TWOSHOT_TMA ? SFAR_TMA_THREADS : kThreadOpts[ti];
+            int km = SFAR_KMAX;
+            for (int test = 0; test < 2; ++test) {
+                int nb = 0;
+                if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, kernel_for(h, p, test), threads,
+                                                                  smem_for(h, p)) != cudaSuccess) {
+                    st = SFAR_ERR_CUDA;
+                    break;
+                }
+                const int k = nb * sms / R;
+                if (k < km)
+                    km = k;
             }
-            const int k = nb * sms / R;
-            if (k < km)
-                km = k;
+            if (km < 1)
+                st = SFAR_ERR_UNSUPPORTED;
+            h->kmax[p][ti] = km;
         }
-        if (km < 1)
-            st = SFAR_ERR_UNSUPPORTED;
-        h->kmax[p] = km;
     }
     if (st == SFAR_OK && cudaDeviceSynchronize() != cudaSuccess)
         st = SFAR_ERR_CUDA;
@@ -346,11 +384,12 @@ sfar_status sfar_query_launch(const sfar_t *h, size_t n, sfar_proto p, int *ctas
     if (!h || (int)p < 0 || (int)p >= SFAR_NUM_PROTOS)
         return SFAR_ERR_INVALID;
     size_t chunk, sub;
-    const int K = geometry(h, p, n, &chunk, &sub);
+    int threads = 0;
+    const int K = geometry(h, p, n, &chunk, &sub, &threads);
     if (ctas_per_rank)
         *ctas_per_rank = K;
     if (threads_per_cta)
-        *threads_per_cta = threads_for(p);
+        *threads_per_cta = threads;
     return SFAR_OK;
 }
 
@@ -395,7 +434,8 @@ sfar_status sfar_allreduce(sfar_t *h, const void *const in[], void *const out[],
         a.out[r] = out[r];
     }
     size_t chunk = 0, sub = 0;
-    const int K = geometry(h, p, n, &chunk, &sub);
+    int threads = 0;
+    const int K = geometry(h, p, n, &chunk, &sub, &threads);
     a.n = n;
     a.chunk = chunk;
     a.sub = sub;
@@ -405,6 +445,7 @@ sfar_status sfar_allreduce(sfar_t *h, const void *const in[], void *const out[],
     a.R = R;
     a.K = K;
     a.overlap = h->mode == SFAR_LAUNCH_OVERLAP;
+    a.stagger = h->stagger;
     switch (p) {
     case SFAR_BASELINE:
     case SFAR_DB:
@@ -437,16 +478,16 @@ sfar_status sfar_allreduce(sfar_t *h, const void *const in[], void *const out[],
         a.stages = h->tma_ns;
         break;
     }
-    const int test = (h->k_strag || h->k_drop || h->k_single) ? 1 : 0;
+    const int test = (h->k_strag || h->k_drop || h->k_single || h->k_trace || h->k_poll) ? 1 : 0;
 
     cudaLaunchConfig_t cfg;
     memset(&cfg, 0, sizeof cfg);
     cfg.gridDim = dim3((unsigned)(R * K));
-    cfg.blockDim = dim3((unsigned)threads_for(p));
+    cfg.blockDim = dim3((unsigned)threads);
     cfg.dynamicSmemBytes = smem_for(h, p);
     cfg.stream = (cudaStream_t)s;
     cudaLaunchAttribute attr[1];
-    if (h->mode == SFAR_LAUNCH_OVERLAP) {
+    if (h->mode != SFAR_LAUNCH_PLAIN) {
         attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
         attr[0].val.programmaticStreamSerializationAllowed = 1;
         cfg.attrs = attr;
@@ -506,10 +547,16 @@ sfar_status sfar_reset(sfar_t *h, sfar_stream_t s)
         r = launch_knob(h, KNOB_STRAG, 0, nullptr, 0, -1, st);
     if (r == SFAR_OK)
         r = launch_knob(h, KNOB_DROP, 0, nullptr, 0, -1, st);
+    if (r == SFAR_OK)
+        r = launch_knob(h, KNOB_TRACE, 0, nullptr, 0, -1, st);
+    if (r == SFAR_OK)
+        r = launch_knob(h, KNOB_POLL_DELAY, 0, nullptr, 0, -1, st);
     if (r != SFAR_OK)
         return r;
     h->k_strag = false;
     h->k_drop = false;
+    h->k_trace = false;
+    h->k_poll = false;
     h->poisoned = false;
     return SFAR_OK;
 }
@@ -555,17 +602,49 @@ sfar_status sfar_test_force_single_buffer(sfar_t *h, int on, sfar_stream_t s)
 
 sfar_status sfar_set_launch_mode(sfar_t *h, int mode)
 {
-    if (!h || (mode != SFAR_LAUNCH_SERIAL && mode != SFAR_LAUNCH_OVERLAP))
+    if (!h || (mode != SFAR_LAUNCH_SERIAL && mode != SFAR_LAUNCH_OVERLAP && mode != SFAR_LAUNCH_PLAIN))
         return SFAR_ERR_INVALID;
     h->mode = mode;
     return SFAR_OK;
 }
 
-sfar_status sfar_test_set_ctas(sfar_t *h, int ctas_per_rank)
+sfar_status sfar_test_set_trace(sfar_t *h, uint64_t *trace, uint32_t calls, sfar_stream_t s)
 {
-    if (!h || ctas_per_rank < 0)
+    if (!h)
+        return SFAR_ERR_INVALID;
+    if (!trace)
+        calls = 0;
+    sfar_status r = launch_knob(h, KNOB_TRACE, 0, reinterpret_cast<const uint32_t *>(trace), calls, -1,
+                                (cudaStream_t)s);
+    if (r == SFAR_OK)
+        h->k_trace = calls > 0;
+    return r;
+}
+
+sfar_status sfar_test_set_poll_delay(sfar_t *h, uint32_t ns, sfar_stream_t s)
+{
+    if (!h)
+        return SFAR_ERR_INVALID;
+    sfar_status r = launch_knob(h, KNOB_POLL_DELAY, ns, nullptr, 0, -1, (cudaStream_t)s);
+    if (r == SFAR_OK)
+        h->k_poll = ns > 0;
+    return r;
+}
+
+sfar_status sfar_test_set_stagger(sfar_t *h, int cycles)
+{
+    if (!h || cycles < 0 || cycles > 100000)
+        return SFAR_ERR_INVALID;
+    h->stagger = cycles;
+    return SFAR_OK;
+}
+
+sfar_status sfar_test_set_geometry(sfar_t *h, int ctas_per_rank, int threads_per_cta)
+{
+    if (!h || ctas_per_rank < 0 || (threads_per_cta != 0 && thread_index(threads_per_cta) < 0))
         return SFAR_ERR_INVALID;
     h->ctas_override = ctas_per_rank;
+    h->threads_override = threads_per_cta;
     return SFAR_OK;
 }
 
@@ -578,14 +657,14 @@ sfar_status sfar_probe_empty(sfar_stream_t s)
     return SFAR_OK;
 }
 
-sfar_status sfar_probe_pingpong(uint32_t *flags, int trips, uint64_t *ns_out, sfar_stream_t s)
+sfar_status sfar_probe_pingpong(uint32_t *flags, int trips, int relaxed, uint64_t *ns_out, sfar_stream_t s)
 {
     if (!flags || !ns_out || trips < 1)
         return SFAR_ERR_INVALID;
     // > half of an SM's shared memory each, so the two CTAs sit on different SMs
     const int smem = 120 * 1024;
     unsigned long long *ns = reinterpret_cast<unsigned long long *>(ns_out);
-    void *args[] = {&flags, &trips, &ns};
+    void *args[] = {&flags, &trips, &relaxed, &ns};
     if (cudaFuncSetAttribute(sfar_kernel_pingpong(), cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess ||
         cudaMemsetAsync(flags, 0, 64 * sizeof(uint32_t), (cudaStream_t)s) != cudaSuccess ||
         cudaLaunchKernel(sfar_kernel_pingpong(), dim3(2), dim3(32), args, smem, (cudaStream_t)s) != cudaSuccess) {

@@ -11,6 +11,7 @@
 #define SFAR_LL128_PAYLOAD 124              // bytes of payload per 128-byte LL128 line
 #define SFAR_ITER_BYTES (4 * SFAR_LL128_PAYLOAD)   // payload of the 4 lines one warp moves at once
 #define SFAR_TMA_THREADS 256
+#define SFAR_NTHREAD_OPTS 3                 // receive-buffer kernels: 64, 128 or 256 threads
 
 // Device status block of one handle.  The first 32 bytes are the sticky
 // status and the fault record; the knobs follow.
@@ -29,7 +30,13 @@ struct SfarCtl {
     int drop_rank;            // < 0: none
     int single_buffer;
     uint32_t strag_base[SFAR_KMAX];   // epoch of (rank 0, CTA k) when the straggler was armed
+    // tracing: SFAR_TRACE_POINTS %globaltimer stamps per (call, CTA)
+    unsigned long long *trace;
+    uint32_t trace_calls;
+    uint32_t poll_delay_ns;           // spin before the first poll of a receive
+    uint32_t trace_base[SFAR_KMAX];
 };
+#define SFAR_TRACE_POINTS 8
 
 // Kernel parameters, passed by value (fits the parameter space).
 struct SfarArgs {
@@ -47,6 +54,7 @@ struct SfarArgs {
     uint32_t *fb;                 // flags [R][R][SFAR_KMAX]: bottom barrier / completion
     SfarCtl *ctl;
     int R, K, overlap, tile_bytes, stages;
+    int stagger;                  // LL / sentinel: SM cycles between the two poll rounds (0: one round)
 };
 
 // Kernel lookup, one function per translation unit.  dt: 0 bf16, 1 fp32.
@@ -62,7 +70,15 @@ const void *sfar_kernel_empty();
 const void *sfar_kernel_pingpong();
 
 // Knob writes (one-thread kernel): which field and value.
-enum SfarKnob { KNOB_TIMEOUT = 1, KNOB_STRAG = 2, KNOB_DROP = 3, KNOB_SINGLE = 4, KNOB_CLEAR_STATUS = 5 };
+enum SfarKnob {
+    KNOB_TIMEOUT = 1,
+    KNOB_STRAG = 2,
+    KNOB_DROP = 3,
+    KNOB_SINGLE = 4,
+    KNOB_CLEAR_STATUS = 5,
+    KNOB_TRACE = 6,
+    KNOB_POLL_DELAY = 7
+};
 struct SfarKnobArgs {
     SfarCtl *ctl;
     int which;

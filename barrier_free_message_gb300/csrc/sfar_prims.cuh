@@ -122,6 +122,27 @@ __device__ __forceinline__ void pdl_launch_dependents()
 {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
+// Waits until every prerequisite grid has completed and its memory is visible
+// (a no-op when the kernel was launched without a programmatic dependency).
+__device__ __forceinline__ void pdl_wait()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// First statement of every AllReduce kernel.  In serial mode the kernel is
+// launched as a programmatic dependent of the previous kernel on the stream:
+// it lets its own successor be scheduled at once, then waits for its
+// predecessor to complete, so it sees exactly what plain stream order would
+// show it, but the launch of each kernel overlaps the end of the previous one.
+// In overlap mode the kernel does not wait (the prologue hands off inside one
+// rank instead).
+__device__ __forceinline__ void sfar_entry(const SfarArgs &a)
+{
+    if (!a.overlap) {
+        pdl_launch_dependents();
+        pdl_wait();
+    }
+}
 
 // ------------------------------------------------------------ bounded waits
 __device__ __forceinline__ void sfar_record_fault(SfarCtl *ctl, int rank, int cta, int peer, uint32_t e,
@@ -140,10 +161,14 @@ __device__ __forceinline__ void sfar_record_fault(SfarCtl *ctl, int rank, int ct
 // One waiter per poll loop.  tick() is cheap on the fast path (a counter);
 // every 128 iterations it reads %globaltimer, gives up after the limit, and
 // also gives up at once if another CTA has already recorded a failure.
+// Waits that can only fail because an earlier wait failed (completion,
+// all-gather, bottom barrier, the overlap hand-off) are "downstream" and get
+// twice the limit, so the first failure recorded is the root cause.
 struct SfarWaiter {
     unsigned long long t0;
     uint32_t it;
-    __device__ __forceinline__ SfarWaiter() : t0(0), it(0) {}
+    int shift;
+    __device__ __forceinline__ SfarWaiter(bool downstream = false) : t0(0), it(0), shift(downstream ? 1 : 0) {}
     __device__ __forceinline__ bool tick(const SfarCtl *ctl)
     {
         if ((++it & 127u) != 0)
@@ -155,7 +180,7 @@ struct SfarWaiter {
         }
         if (ld_relaxed_s32(&ctl->status) != 0)
             return true;
-        return now - t0 > ld_relaxed_u64(&ctl->timeout_ns);
+        return now - t0 > (ld_relaxed_u64(&ctl->timeout_ns) << shift);
     }
 };
 
@@ -163,9 +188,10 @@ struct SfarWaiter {
 __device__ __forceinline__ bool epoch_ge(uint32_t a, uint32_t b) { return (int32_t)(a - b) >= 0; }
 
 // Poll a u32 flag until it reaches epoch e (relaxed loads; the caller fences).
-__device__ __forceinline__ bool poll_flag_ge(const uint32_t *f, uint32_t e, const SfarCtl *ctl)
+__device__ __forceinline__ bool poll_flag_ge(const uint32_t *f, uint32_t e, const SfarCtl *ctl,
+                                             bool downstream = false)
 {
-    SfarWaiter w;
+    SfarWaiter w(downstream);
     while (!epoch_ge(ld_relaxed_u32(f), e))
         if (w.tick(ctl))
             return false;
@@ -178,7 +204,19 @@ struct SfarCall {
     int par;        // receive-buffer parity
     bool drop;      // test knob: this rank sends nothing
     uint32_t mid_delay_ns;   // test knob: straggler delay between sends and receives
+    uint32_t poll_delay_ns;  // test knob: spin before the first poll
+    unsigned long long *trace;   // test knob: this CTA's stamps for this call (thread 0 only)
 };
+
+// Trace points (test variants with tracing armed; thread 0's view).
+enum { TP_ENTRY = 0, TP_TICKET = 1, TP_SENT = 2, TP_RECEIVED = 3, TP_EXIT = 4 };
+
+template <bool TEST>
+__device__ __forceinline__ void sfar_stamp(const SfarCall &c, int point)
+{
+    if (TEST && c.trace)
+        c.trace[point] = globaltimer();
+}
 
 __device__ __forceinline__ void spin_ns(unsigned long long d)
 {
@@ -194,9 +232,13 @@ __device__ __forceinline__ bool sfar_prologue(const SfarArgs &a, int r, int k, S
 {
     __shared__ uint32_t s_e;
     __shared__ int s_flags;
+    unsigned long long t_entry = 0;
+    c.trace = nullptr;
     if (threadIdx.x == 0) {
+        if (TEST)
+            t_entry = globaltimer();
         // Ticket: the epoch of this (rank, CTA).  Its latency overlaps the
-        // input loads the caller issues right after.
+        // input loads the caller has issued just before.
         const uint32_t e = atomicAdd(a.epoch + r * SFAR_KMAX + k, 1u) + 1u;
         int flags = ld_relaxed_s32(&a.ctl->status) != 0 ? 1 : 0;
         if (TEST) {
@@ -219,14 +261,26 @@ __device__ __forceinline__ bool sfar_prologue(const SfarArgs &a, int r, int k, S
     c.drop = (flags & 2) != 0;
     c.par = (flags & 4) ? 0 : (int)(c.e & 1u);
     c.mid_delay_ns = 0;
+    c.poll_delay_ns = 0;
     if (a.overlap || TEST) {
         __shared__ int s_ok;
-        __shared__ uint32_t s_mid;
+        __shared__ uint32_t s_mid, s_pd;
         if (threadIdx.x == 0) {
             int ok = 1;
+            if (TEST) {
+                const volatile SfarCtl *ctl = a.ctl;
+                unsigned long long *tr = ctl->trace;
+                const uint32_t ti = c.e - ctl->trace_base[k] - 1u;
+                if (tr && ti < ctl->trace_calls) {
+                    c.trace = tr + ((size_t)ti * gridDim.x + blockIdx.x) * SFAR_TRACE_POINTS;
+                    c.trace[TP_ENTRY] = t_entry;
+                    c.trace[TP_TICKET] = globaltimer();
+                }
+                s_pd = ctl->poll_delay_ns;
+            }
             if (a.overlap) {
                 // wait for CTA (r, k) of the previous call: a wait inside one rank
-                SfarWaiter w;
+                SfarWaiter w(true);
                 const uint32_t *d = a.done + r * SFAR_KMAX + k;
                 while (!epoch_ge(ld_acquire_u32(d), c.e - 1u)) {
                     if (w.tick(a.ctl)) {
@@ -259,6 +313,8 @@ __device__ __forceinline__ bool sfar_prologue(const SfarArgs &a, int r, int k, S
         if (!s_ok)
             return false;
         c.mid_delay_ns = s_mid;
+        if (TEST)
+            c.poll_delay_ns = s_pd;
     }
     return true;
 }
@@ -273,6 +329,14 @@ __device__ __forceinline__ void sfar_mid_delay(const SfarCall &c)
             spin_ns(c.mid_delay_ns);
         __syncthreads();
     }
+}
+
+// Test variants: every thread waits this long before its first poll.
+template <bool TEST>
+__device__ __forceinline__ void sfar_poll_delay(const SfarCall &c)
+{
+    if (TEST && c.poll_delay_ns)
+        spin_ns(c.poll_delay_ns);
 }
 
 // Marks (rank, CTA) done with epoch e.  In overlap mode the next call's CTA

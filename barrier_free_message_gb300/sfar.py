@@ -19,7 +19,8 @@ PROTOS = {"baseline": SFAR_BASELINE, "db": SFAR_DB, "ll": SFAR_LL, "ll128": SFAR
 DTYPES = {"bf16": SFAR_BF16, "fp32": SFAR_FP32}
 SFAR_OK, SFAR_ERR_INVALID, SFAR_ERR_CUDA, SFAR_ERR_OOM, SFAR_ERR_TIMEOUT, SFAR_ERR_UNSUPPORTED, \
     SFAR_ERR_POISONED = range(7)
-SFAR_LAUNCH_SERIAL, SFAR_LAUNCH_OVERLAP = 0, 1
+SFAR_LAUNCH_SERIAL, SFAR_LAUNCH_OVERLAP, SFAR_LAUNCH_PLAIN = 0, 1, 2
+MODES = {"serial": SFAR_LAUNCH_SERIAL, "overlap": SFAR_LAUNCH_OVERLAP, "plain": SFAR_LAUNCH_PLAIN}
 WAIT_NAMES = {1: "done", 2: "ll", 3: "sentinel", 4: "ready", 5: "bottom", 6: "ll128", 7: "rs", 8: "ag",
               9: "arrive", 10: "complete", 11: "copy"}
 
@@ -56,9 +57,13 @@ _SIGS = [
     ("sfar_test_set_timeout", ctypes.c_int, [ctypes.c_void_p, ctypes.c_uint64, ctypes.c_void_p]),
     ("sfar_test_force_single_buffer", ctypes.c_int, [ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p]),
     ("sfar_set_launch_mode", ctypes.c_int, [ctypes.c_void_p, ctypes.c_int]),
-    ("sfar_test_set_ctas", ctypes.c_int, [ctypes.c_void_p, ctypes.c_int]),
+    ("sfar_test_set_geometry", ctypes.c_int, [ctypes.c_void_p, ctypes.c_int, ctypes.c_int]),
+    ("sfar_test_set_trace", ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_uint32, ctypes.c_void_p]),
+    ("sfar_test_set_poll_delay", ctypes.c_int, [ctypes.c_void_p, ctypes.c_uint32, ctypes.c_void_p]),
+    ("sfar_test_set_stagger", ctypes.c_int, [ctypes.c_void_p, ctypes.c_int]),
     ("sfar_probe_empty", ctypes.c_int, [ctypes.c_void_p]),
-    ("sfar_probe_pingpong", ctypes.c_int, [ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p]),
+    ("sfar_probe_pingpong", ctypes.c_int, [ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_void_p,
+                                           ctypes.c_void_p]),
 ]
 
 
@@ -162,20 +167,32 @@ def sfar_test_force_single_buffer(h, on: bool, stream=None) -> int:
 
 
 def sfar_set_launch_mode(h, mode) -> int:
-    m = {"serial": SFAR_LAUNCH_SERIAL, "overlap": SFAR_LAUNCH_OVERLAP}.get(mode, mode)
+    m = MODES.get(mode, mode)
     return lib().sfar_set_launch_mode(h, int(m))
 
 
-def sfar_test_set_ctas(h, k: int) -> int:
-    return lib().sfar_test_set_ctas(h, k)
+def sfar_test_set_geometry(h, ctas_per_rank: int = 0, threads_per_cta: int = 0) -> int:
+    return lib().sfar_test_set_geometry(h, ctas_per_rank, threads_per_cta)
+
+
+def sfar_test_set_trace(h, trace_ptr: int, calls: int, stream=None) -> int:
+    return lib().sfar_test_set_trace(h, trace_ptr, calls, _stream(stream))
+
+
+def sfar_test_set_poll_delay(h, ns: int, stream=None) -> int:
+    return lib().sfar_test_set_poll_delay(h, ns, _stream(stream))
+
+
+def sfar_test_set_stagger(h, cycles: int) -> int:
+    return lib().sfar_test_set_stagger(h, cycles)
 
 
 def sfar_probe_empty(stream=None) -> int:
     return lib().sfar_probe_empty(_stream(stream))
 
 
-def sfar_probe_pingpong(flags_ptr: int, trips: int, ns_ptr: int, stream=None) -> int:
-    return lib().sfar_probe_pingpong(flags_ptr, trips, ns_ptr, _stream(stream))
+def sfar_probe_pingpong(flags_ptr: int, trips: int, ns_ptr: int, relaxed: bool = False, stream=None) -> int:
+    return lib().sfar_probe_pingpong(flags_ptr, trips, 1 if relaxed else 0, ns_ptr, _stream(stream))
 
 
 # --------------------------------------------------------- convenience class

@@ -47,35 +47,63 @@ sfar_status sfar_test_set_timeout(sfar_t *h, uint64_t ns, sfar_stream_t s);
 sfar_status sfar_test_force_single_buffer(sfar_t *h, int on, sfar_stream_t s);
 
 /*
- * Launch mode.  SFAR_LAUNCH_SERIAL (default): plain stream order, so the end
- * of each kernel is a full barrier between calls.  SFAR_LAUNCH_OVERLAP:
- * programmatic dependent launch; each CTA lets the next call's kernel start
- * as soon as it has taken its epoch, and the next call's CTA (r, k) waits only
- * for CTA (r, k) of this call (a wait inside one rank, not across ranks).
- * Calls may then overtake one another across ranks, which is what double
- * buffering has to survive.  Use OVERLAP only for chains of calls whose
- * inputs do not depend on the previous call's outputs.
+ * Launch mode.  SFAR_LAUNCH_SERIAL (default): stream order.  The kernel is
+ * launched as a programmatic dependent of the previous kernel on the stream
+ * and waits (griddepcontrol.wait) for it to complete before touching memory,
+ * so the end of each kernel is still a full barrier between calls; only the
+ * launch overlaps.  SFAR_LAUNCH_PLAIN: stream order with no programmatic
+ * launch at all (for comparison).  SFAR_LAUNCH_OVERLAP: each CTA lets the
+ * next call's kernel start as soon as it has taken its epoch, and the next
+ * call's CTA (r, k) waits only for CTA (r, k) of this call (a wait inside one
+ * rank, not across ranks).  Calls may then overtake one another across
+ * ranks, which is what double buffering has to survive.  Use OVERLAP only
+ * for chains of calls whose inputs do not depend on the previous call's
+ * outputs.
  */
 #define SFAR_LAUNCH_SERIAL 0
 #define SFAR_LAUNCH_OVERLAP 1
+#define SFAR_LAUNCH_PLAIN 2
 sfar_status sfar_set_launch_mode(sfar_t *h, int mode);
 
-/* CTAs per rank for every later call (0 = automatic). Clamped to what can
- * be co-resident. */
-sfar_status sfar_test_set_ctas(sfar_t *h, int ctas_per_rank);
+/*
+ * Tracing.  From the next call on, for `calls` calls, thread 0 of every CTA
+ * writes %globaltimer nanoseconds at 8 slots per (call, CTA):
+ * trace[(call * grid + blockIdx) * 8 + point], points 0 = kernel entry,
+ * 1 = epoch ticket received, 2 = sends issued (DB/baseline: top barrier
+ * passed), 3 = receive and reduction done, 4 = exit; 5..7 unused.  grid is
+ * R * CTAs per rank of that call.  trace is a DEVICE array of uint64 owned by
+ * the caller, sized for calls * grid * 8; NULL or calls == 0 disarms.
+ */
+sfar_status sfar_test_set_trace(sfar_t *h, uint64_t *trace, uint32_t calls, sfar_stream_t s);
+
+/* Every receiving thread spins this many nanoseconds before its first poll
+ * (one-shot LL and sentinel); 0 disarms. */
+sfar_status sfar_test_set_poll_delay(sfar_t *h, uint32_t ns, sfar_stream_t s);
+
+/* One-shot LL and sentinel with R <= 8: keep a second round of polls in
+ * flight, issued `cycles` SM cycles after the first (0 = one round only; at
+ * most 100000).  Takes effect for calls made after it. */
+sfar_status sfar_test_set_stagger(sfar_t *h, int cycles);
+
+/* Launch geometry of every later call of the receive-buffer protocols:
+ * CTAs per rank (0 = automatic; clamped to what can be co-resident) and
+ * threads per CTA (0 = automatic, else 64, 128 or 256; the TMA path always
+ * uses 256).  SFAR_ERR_INVALID for another thread count. */
+sfar_status sfar_test_set_geometry(sfar_t *h, int ctas_per_rank, int threads_per_cta);
 
 /*
  * Latency floor probes.
  * sfar_probe_empty: enqueue one empty kernel (1 CTA, 32 threads) on s.
  * sfar_probe_pingpong: enqueue one kernel of two CTAs on different SMs that
  *   pass a token `trips` times through two flags in global memory
- *   (st.release / ld.acquire at GPU scope); ns_out (device, 1 uint64) gets
- *   the elapsed %globaltimer nanoseconds.  flags is a device array of 64
- *   uint32 that the probe zeroes first.  Waits are bounded (1 s); on
- *   timeout ns_out gets UINT64_MAX.
+ *   (relaxed == 0: st.release / ld.acquire at GPU scope; relaxed != 0:
+ *   relaxed GPU-scope stores and loads); ns_out (device, 1 uint64) gets the
+ *   elapsed %globaltimer nanoseconds.  flags is a device array of 64 uint32
+ *   that the probe zeroes first.  Waits are bounded (1 s); on timeout ns_out
+ *   gets UINT64_MAX.
  */
 sfar_status sfar_probe_empty(sfar_stream_t s);
-sfar_status sfar_probe_pingpong(uint32_t *flags, int trips, uint64_t *ns_out, sfar_stream_t s);
+sfar_status sfar_probe_pingpong(uint32_t *flags, int trips, int relaxed, uint64_t *ns_out, sfar_stream_t s);
 
 #ifdef __cplusplus
 }
