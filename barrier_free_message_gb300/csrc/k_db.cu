@@ -52,21 +52,24 @@ template <int DT, int RB, bool TEST, bool BASE>
 __global__ void __launch_bounds__(SFAR_THREADS) k_db(const __grid_constant__ SfarArgs a)
 {
     constexpr int ES = DT == 0 ? 2 : 4;
-    sfar_entry(a);
     const int R = a.R, K = a.K;
     const int r = blockIdx.x / K, k = blockIdx.x - r * K;
     const unsigned long long nbytes = a.n * ES;
     const unsigned long long nvec = (nbytes + 15ull) >> 4;
     const unsigned long long stride = (unsigned long long)K * blockDim.x;
     const unsigned long long v0 = (unsigned long long)k * blockDim.x + threadIdx.x;
+    if (v0 * 16ull < nbytes)
+        prefetch_l2((const char *)a.in[r] + v0 * 16ull);
+    const SfarEntry ent = sfar_entry(a);
     const uint4 x0 = load_vec<ES>(a.in[r], v0, nbytes);     // before the prologue's barrier
     SfarCall c;
-    if (!sfar_prologue<TEST>(a, r, k, c))
+    if (!sfar_prologue<TEST>(a, r, k, c, ent))
         return;
     const uint32_t e = c.e;
     const int par = BASE ? 0 : c.par;
     const size_t slot = a.slot;
     __shared__ int s_ok;
+    sfar_stamp_after(c, TP_INPUT, x0.x);
 
     // send raw vectors
     if (!c.drop) {
@@ -89,7 +92,7 @@ __global__ void __launch_bounds__(SFAR_THREADS) k_db(const __grid_constant__ Sfa
             s_ok = ok;
     }
     __syncthreads();
-    sfar_stamp<TEST>(c, TP_SENT);      // here: after the top barrier
+    sfar_stamp(c, TP_SENT);      // here: after the top barrier
     // a slow reader (test knob): the data is there, its reads come late
     sfar_mid_delay<TEST>(c);
 
@@ -117,9 +120,9 @@ __global__ void __launch_bounds__(SFAR_THREADS) k_db(const __grid_constant__ Sfa
                 flag_exchange(a, a.fb, r, k, e, true, SFAR_WAIT_BOTTOM);
         }
     }
-    sfar_stamp<TEST>(c, TP_RECEIVED);
+    sfar_stamp(c, TP_RECEIVED);
     sfar_epilogue(a, r, k, e);
-    sfar_stamp<TEST>(c, TP_EXIT);
+    sfar_stamp(c, TP_EXIT);
 }
 
 const void *sfar_kernel_db(int dt, int wide, int test, int baseline)

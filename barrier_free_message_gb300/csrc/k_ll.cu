@@ -46,20 +46,23 @@ template <int DT, int RB, bool TEST>
 __global__ void __launch_bounds__(SFAR_THREADS) k_ll(const __grid_constant__ SfarArgs a)
 {
     constexpr int ES = DT == 0 ? 2 : 4;
-    sfar_entry(a);
     const int R = a.R, K = a.K;
     const int r = blockIdx.x / K, k = blockIdx.x - r * K;
     const unsigned long long nbytes = a.n * ES;
     const unsigned long long nvec = (nbytes + 15ull) >> 4;
     const unsigned long long stride = (unsigned long long)K * blockDim.x;
     const unsigned long long v0 = (unsigned long long)k * blockDim.x + threadIdx.x;
+    if (v0 * 16ull < nbytes)
+        prefetch_l2((const char *)a.in[r] + v0 * 16ull);
+    const SfarEntry ent = sfar_entry(a);
     const uint4 x0 = load_vec<ES>(a.in[r], v0, nbytes);     // zero past the end
     SfarCall c;
-    if (!sfar_prologue<TEST>(a, r, k, c))
+    if (!sfar_prologue<TEST>(a, r, k, c, ent))
         return;
     const uint32_t e = c.e;
     const unsigned long long eh = (unsigned long long)e << 32;
     const size_t slot = a.slot;
+    sfar_stamp_after(c, TP_INPUT, x0.x);
 
     // send: pack each input vector once, store it into every peer's slot r
     if (!c.drop) {
@@ -77,39 +80,21 @@ __global__ void __launch_bounds__(SFAR_THREADS) k_ll(const __grid_constant__ Sfa
             }
         }
     }
-    sfar_stamp<TEST>(c, TP_SENT);
+    sfar_stamp(c, TP_SENT);
     sfar_mid_delay<TEST>(c);
-    sfar_poll_delay<TEST>(c);
 
     // receive and reduce: poll every peer's packets, fold in rank order
     const uint8_t *mine = a.region + (size_t)(r * 2 + c.par) * R * slot;
     bool ok = true;
-    // Two rounds of polls are kept in flight, the second issued `stagger`
-    // cycles after the first (set B; R <= 8 only), so a packet that lands
-    // just after one round passed is seen half a round trip later, not a
-    // whole one.  Each round re-reads only the peers not seen yet.
-    constexpr bool TWO_SETS = RB <= 8;
-    const bool stag = TWO_SETS && a.stagger > 0;
     for (unsigned long long v = v0; v < nvec && ok; v += stride) {
         const uint4 own = v == v0 ? x0 : load_vec<ES>(a.in[r], v, nbytes);
-        LLSlots<RB> A;
-        LLSlots<TWO_SETS ? RB : 1> B;
-        bool rdy[RB], fromB[RB];
+        LLSlots<RB> s;
+        bool rdy[RB];
 #pragma unroll
         for (int q = 0; q < RB; ++q) {
             rdy[q] = q >= R || q == r;
-            fromB[q] = false;
             if (!rdy[q])
-                A.load(q, mine + (size_t)q * slot + v * 32ull);
-        }
-        if (TWO_SETS && stag) {
-            const long long t0 = clock64();
-            while (clock64() - t0 < a.stagger) {
-            }
-#pragma unroll
-            for (int q = 0; q < (TWO_SETS ? RB : 1); ++q)
-                if (!rdy[q])
-                    B.load(q, mine + (size_t)q * slot + v * 32ull);
+                s.load(q, mine + (size_t)q * slot + v * 32ull);
         }
         SfarWaiter w;
         while (true) {
@@ -117,32 +102,11 @@ __global__ void __launch_bounds__(SFAR_THREADS) k_ll(const __grid_constant__ Sfa
 #pragma unroll
             for (int q = 0; q < RB; ++q) {
                 if (!rdy[q])
-                    rdy[q] = A.ready(q, e);
+                    rdy[q] = s.ready(q, e);
                 all = all && rdy[q];
             }
             if (all)
                 break;
-#pragma unroll
-            for (int q = 0; q < RB; ++q)
-                if (!rdy[q])
-                    A.load(q, mine + (size_t)q * slot + v * 32ull);
-            if (TWO_SETS && stag) {
-                all = true;
-#pragma unroll
-                for (int q = 0; q < (TWO_SETS ? RB : 1); ++q) {
-                    if (!rdy[q] && B.ready(q, e)) {
-                        rdy[q] = true;
-                        fromB[q] = true;
-                    }
-                    all = all && rdy[q];
-                }
-                if (all)
-                    break;
-#pragma unroll
-                for (int q = 0; q < (TWO_SETS ? RB : 1); ++q)
-                    if (!rdy[q])
-                        B.load(q, mine + (size_t)q * slot + v * 32ull);
-            }
             if (w.tick(a.ctl)) {
                 int late = -1;
 #pragma unroll
@@ -153,20 +117,24 @@ __global__ void __launch_bounds__(SFAR_THREADS) k_ll(const __grid_constant__ Sfa
                 ok = false;
                 break;
             }
+#pragma unroll
+            for (int q = 0; q < RB; ++q)
+                if (!rdy[q])
+                    s.load(q, mine + (size_t)q * slot + v * 32ull);
         }
         if (!ok)
             break;
         SfarAcc<DT> acc;
-        acc.set(r == 0 ? own : (TWO_SETS && fromB[0] ? B.data(0) : A.data(0)));
+        acc.set(r == 0 ? own : s.data(0));
 #pragma unroll
         for (int q = 1; q < RB; ++q)
             if (q < R)
-                acc.add(q == r ? own : (TWO_SETS && fromB[q] ? B.data(q & (TWO_SETS ? RB - 1 : 0)) : A.data(q)));
+                acc.add(q == r ? own : s.data(q));
         store_vec<ES>(a.out[r], v, nbytes, acc.get());
     }
-    sfar_stamp<TEST>(c, TP_RECEIVED);
+    sfar_stamp(c, TP_RECEIVED);
     sfar_epilogue(a, r, k, e);
-    sfar_stamp<TEST>(c, TP_EXIT);
+    sfar_stamp(c, TP_EXIT);
 }
 
 const void *sfar_kernel_ll(int dt, int wide, int test)

@@ -24,7 +24,7 @@ template <int DT, int RB, bool TEST>
 __global__ void __launch_bounds__(SFAR_THREADS) k_ll128(const __grid_constant__ SfarArgs a)
 {
     constexpr int ES = DT == 0 ? 2 : 4;
-    sfar_entry(a);
+    const SfarEntry ent = sfar_entry(a);
     const int R = a.R, K = a.K;
     const int r = blockIdx.x / K, k = blockIdx.x - r * K;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, g = lane >> 3, m = lane & 7;
@@ -37,10 +37,11 @@ __global__ void __launch_bounds__(SFAR_THREADS) k_ll128(const __grid_constant__ 
     // first group's input, loaded before the prologue's barrier
     const uint4 x0 = lane < 31 ? load_vec<ES>(a.in[r], it0 * 31ull + lane, nbytes) : zero;
     SfarCall c;
-    if (!sfar_prologue<TEST>(a, r, k, c))
+    if (!sfar_prologue<TEST>(a, r, k, c, ent))
         return;
     const uint32_t e = c.e;
     const size_t slot = a.slot;
+    sfar_stamp_after(c, TP_INPUT, x0.x);
 
     // send: payload of every line to every peer, then one fence, then the flags
     if (!c.drop) {
@@ -67,7 +68,7 @@ __global__ void __launch_bounds__(SFAR_THREADS) k_ll128(const __grid_constant__ 
             }
     }
 
-    sfar_stamp<TEST>(c, TP_SENT);
+    sfar_stamp(c, TP_SENT);
     sfar_mid_delay<TEST>(c);
 
     // receive: poll the line flags, read the payload, fold in rank order
@@ -109,9 +110,9 @@ __global__ void __launch_bounds__(SFAR_THREADS) k_ll128(const __grid_constant__ 
         if (lane < 31)
             store_vec<ES>(a.out[r], it * 31ull + lane, nbytes, res);
     }
-    sfar_stamp<TEST>(c, TP_RECEIVED);
+    sfar_stamp(c, TP_RECEIVED);
     sfar_epilogue(a, r, k, e);
-    sfar_stamp<TEST>(c, TP_EXIT);
+    sfar_stamp(c, TP_EXIT);
 }
 
 const void *sfar_kernel_ll128(int dt, int wide, int test)

@@ -28,15 +28,6 @@ __global__ void k_set_knob(const SfarKnobArgs k)
     case KNOB_SINGLE:
         c->single_buffer = (int)k.value;
         break;
-    case KNOB_TRACE:
-        c->trace = reinterpret_cast<unsigned long long *>(const_cast<uint32_t *>(k.ptr));
-        c->trace_calls = k.len;
-        for (int i = 0; i < SFAR_KMAX; ++i)
-            c->trace_base[i] = k.epoch_row0[i];
-        break;
-    case KNOB_POLL_DELAY:
-        c->poll_delay_ns = (uint32_t)k.value;
-        break;
     case KNOB_CLEAR_STATUS:
         c->status = 0;
         c->f_rank = c->f_cta = c->f_peer = -1;

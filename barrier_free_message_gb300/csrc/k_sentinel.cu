@@ -39,19 +39,22 @@ template <int DT, int RB, bool TEST>
 __global__ void __launch_bounds__(SFAR_THREADS) k_sentinel(const __grid_constant__ SfarArgs a)
 {
     constexpr int ES = DT == 0 ? 2 : 4;
-    sfar_entry(a);
     const int R = a.R, K = a.K;
     const int r = blockIdx.x / K, k = blockIdx.x - r * K;
     const unsigned long long nbytes = a.n * ES;
     const unsigned long long nvec = (nbytes + 15ull) >> 4;
     const unsigned long long stride = (unsigned long long)K * blockDim.x;
     const unsigned long long v0 = (unsigned long long)k * blockDim.x + threadIdx.x;
+    if (v0 * 16ull < nbytes)
+        prefetch_l2((const char *)a.in[r] + v0 * 16ull);
+    const SfarEntry ent = sfar_entry(a);
     const uint4 x0 = load_vec<ES>(a.in[r], v0, nbytes);     // before the prologue's barrier
     SfarCall c;
-    if (!sfar_prologue<TEST>(a, r, k, c))
+    if (!sfar_prologue<TEST>(a, r, k, c, ent))
         return;
     const uint32_t e = c.e;
     const size_t slot = a.slot;
+    sfar_stamp_after(c, TP_INPUT, x0.x);
 
     if (!c.drop) {
         for (unsigned long long v = v0; v < nvec; v += stride) {
@@ -66,34 +69,21 @@ __global__ void __launch_bounds__(SFAR_THREADS) k_sentinel(const __grid_constant
         }
     }
 
-    sfar_stamp<TEST>(c, TP_SENT);
+    sfar_stamp(c, TP_SENT);
     sfar_mid_delay<TEST>(c);
-    sfar_poll_delay<TEST>(c);
     uint8_t *mine = a.region + (size_t)(r * 2 + c.par) * R * slot;
     const uint4 sent = make_uint4(0xffffffffu, 0xffffffffu, 0xffffffffu, 0xffffffffu);
-    constexpr bool TWO_SETS = RB <= 8;
-    const bool stag = TWO_SETS && a.stagger > 0;
     bool ok = true;
     for (unsigned long long v = v0; v < nvec && ok; v += stride) {
         const uint4 own = v == v0 ? x0 : load_vec<ES>(a.in[r], v, nbytes);
-        // every round re-reads all peers still holding the sentinel at once;
-        // with R <= 8 a second round (y) runs `stagger` cycles behind the first
-        uint4 x[RB], y[TWO_SETS ? RB : 1];
+        // every round re-reads all peers still holding the sentinel at once
+        uint4 x[RB];
         bool rdy[RB];
 #pragma unroll
         for (int q = 0; q < RB; ++q) {
             rdy[q] = q >= R || q == r;
             if (!rdy[q])
                 x[q] = ld_relaxed_v4(mine + (size_t)q * slot + v * 16ull);
-        }
-        if (TWO_SETS && stag) {
-            const long long t0 = clock64();
-            while (clock64() - t0 < a.stagger) {
-            }
-#pragma unroll
-            for (int q = 0; q < (TWO_SETS ? RB : 1); ++q)
-                if (!rdy[q])
-                    y[q] = ld_relaxed_v4(mine + (size_t)q * slot + v * 16ull);
         }
         SfarWaiter w;
         while (true) {
@@ -110,23 +100,6 @@ __global__ void __launch_bounds__(SFAR_THREADS) k_sentinel(const __grid_constant
             for (int q = 0; q < RB; ++q)
                 if (!rdy[q])
                     x[q] = ld_relaxed_v4(mine + (size_t)q * slot + v * 16ull);
-            if (TWO_SETS && stag) {
-                all = true;
-#pragma unroll
-                for (int q = 0; q < (TWO_SETS ? RB : 1); ++q) {
-                    if (!rdy[q] && !has_sentinel<DT>(y[q])) {
-                        rdy[q] = true;
-                        x[q] = y[q];
-                    }
-                    all = all && rdy[q];
-                }
-                if (all)
-                    break;
-#pragma unroll
-                for (int q = 0; q < (TWO_SETS ? RB : 1); ++q)
-                    if (!rdy[q])
-                        y[q] = ld_relaxed_v4(mine + (size_t)q * slot + v * 16ull);
-            }
             if (w.tick(a.ctl)) {
                 int late = -1;
 #pragma unroll
@@ -153,9 +126,9 @@ __global__ void __launch_bounds__(SFAR_THREADS) k_sentinel(const __grid_constant
             if (q < R && q != r)
                 st_relaxed_v4(mine + (size_t)q * slot + v * 16ull, sent);
     }
-    sfar_stamp<TEST>(c, TP_RECEIVED);
+    sfar_stamp(c, TP_RECEIVED);
     sfar_epilogue(a, r, k, e);
-    sfar_stamp<TEST>(c, TP_EXIT);
+    sfar_stamp(c, TP_EXIT);
 }
 
 const void *sfar_kernel_sentinel(int dt, int wide, int test)

@@ -91,12 +91,12 @@ template <int DT, bool TEST>
 __global__ void __launch_bounds__(SFAR_TMA_THREADS, 1) k_tma(const __grid_constant__ SfarArgs a)
 {
     constexpr int ES = DT == 0 ? 2 : 4;
-    sfar_entry(a);
+    const SfarEntry ent = sfar_entry(a);
     const int R = a.R, K = a.K;
     const int r = blockIdx.x / K, k = blockIdx.x - r * K;
     const int tid = threadIdx.x, lane = tid & 31;
     SfarCall c;
-    if (!sfar_prologue<TEST>(a, r, k, c))
+    if (!sfar_prologue<TEST>(a, r, k, c, ent))
         return;
     const uint32_t e = c.e;
     uint32_t *arrive = a.fa;      // [R][KMAX]
@@ -260,9 +260,9 @@ __global__ void __launch_bounds__(SFAR_TMA_THREADS, 1) k_tma(const __grid_consta
         __syncwarp();
         fence_acq_rel_gpu();
     }
-    sfar_stamp<TEST>(c, TP_RECEIVED);
+    sfar_stamp(c, TP_RECEIVED);
     sfar_epilogue(a, r, k, e);
-    sfar_stamp<TEST>(c, TP_EXIT);
+    sfar_stamp(c, TP_EXIT);
 }
 
 const void *sfar_kernel_tma(int dt, int test)

@@ -30,11 +30,11 @@ template <int DT, int RB, bool TEST>
 __global__ void __launch_bounds__(SFAR_THREADS) k_twoshot(const __grid_constant__ SfarArgs a)
 {
     constexpr int ES = DT == 0 ? 2 : 4;
-    sfar_entry(a);
+    const SfarEntry ent = sfar_entry(a);
     const int R = a.R, K = a.K;
     const int r = blockIdx.x / K, k = blockIdx.x - r * K;
     SfarCall c;
-    if (!sfar_prologue<TEST>(a, r, k, c))
+    if (!sfar_prologue<TEST>(a, r, k, c, ent))
         return;
     const uint32_t e = c.e;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, g = lane >> 3, m = lane & 7;
@@ -68,7 +68,7 @@ __global__ void __launch_bounds__(SFAR_THREADS) k_twoshot(const __grid_constant_
         }
     }
 
-    sfar_stamp<TEST>(c, TP_SENT);
+    sfar_stamp(c, TP_SENT);
     sfar_mid_delay<TEST>(c);
 
     // 2. owner: receive, reduce, all-gather send
@@ -157,9 +157,9 @@ __global__ void __launch_bounds__(SFAR_THREADS) k_twoshot(const __grid_constant_
                 store_vec<ES>(a.out[r], j * cvec + it * 31ull + lane, nbytes, o);
         }
     }
-    sfar_stamp<TEST>(c, TP_RECEIVED);
+    sfar_stamp(c, TP_RECEIVED);
     sfar_epilogue(a, r, k, e);
-    sfar_stamp<TEST>(c, TP_EXIT);
+    sfar_stamp(c, TP_EXIT);
 }
 
 const void *sfar_kernel_twoshot(int dt, int wide, int test)

@@ -48,8 +48,9 @@ struct sfar {
     size_t s_raw = 0, s_ll = 0, s_ll128 = 0, s_2s = 0, sent_bytes = 0;
     int mode = SFAR_LAUNCH_SERIAL;
     int ctas_override = 0, threads_override = 0;
-    int stagger = 0;                    // cycles between the two poll rounds (LL, sentinel)
-    bool k_strag = false, k_drop = false, k_single = false, k_trace = false, k_poll = false;
+    unsigned long long *trace = nullptr; // test hook: trace ring (device), calls per CTA
+    uint32_t trace_calls = 0;
+    bool k_strag = false, k_drop = false, k_single = false;
     bool poisoned = false;
     cudaStream_t priv = nullptr;
     SfarCtl *host_ctl = nullptr;
@@ -128,7 +129,9 @@ static int geometry(const sfar *h, int p, size_t n, size_t *chunk, size_t *sub, 
         if (h->threads_override > 0 && thread_index(h->threads_override) >= 0) {
             ti = thread_index(h->threads_override);
         } else {
-            for (int i = 0; i < SFAR_NTHREAD_OPTS; ++i) {
+            // the flag protocols pay per CTA for their barrier, so they start at 128 threads
+            const int first = (p == SFAR_DB || p == SFAR_BASELINE) ? 1 : 0;
+            for (int i = first; i < SFAR_NTHREAD_OPTS; ++i) {
                 const size_t per = warp_units ? (size_t)kThreadOpts[i] / 32 : (size_t)kThreadOpts[i];
                 if ((size_t)h->R * ceil_div(units, per) <= (size_t)h->sms) {
                     ti = i;
@@ -445,7 +448,8 @@ sfar_status sfar_allreduce(sfar_t *h, const void *const in[], void *const out[],
     a.R = R;
     a.K = K;
     a.overlap = h->mode == SFAR_LAUNCH_OVERLAP;
-    a.stagger = h->stagger;
+    a.trace = h->trace;
+    a.trace_calls = h->trace_calls;
     switch (p) {
     case SFAR_BASELINE:
     case SFAR_DB:
@@ -478,7 +482,7 @@ sfar_status sfar_allreduce(sfar_t *h, const void *const in[], void *const out[],
         a.stages = h->tma_ns;
         break;
     }
-    const int test = (h->k_strag || h->k_drop || h->k_single || h->k_trace || h->k_poll) ? 1 : 0;
+    const int test = (h->k_strag || h->k_drop || h->k_single) ? 1 : 0;
 
     cudaLaunchConfig_t cfg;
     memset(&cfg, 0, sizeof cfg);
@@ -547,16 +551,10 @@ sfar_status sfar_reset(sfar_t *h, sfar_stream_t s)
         r = launch_knob(h, KNOB_STRAG, 0, nullptr, 0, -1, st);
     if (r == SFAR_OK)
         r = launch_knob(h, KNOB_DROP, 0, nullptr, 0, -1, st);
-    if (r == SFAR_OK)
-        r = launch_knob(h, KNOB_TRACE, 0, nullptr, 0, -1, st);
-    if (r == SFAR_OK)
-        r = launch_knob(h, KNOB_POLL_DELAY, 0, nullptr, 0, -1, st);
     if (r != SFAR_OK)
         return r;
     h->k_strag = false;
     h->k_drop = false;
-    h->k_trace = false;
-    h->k_poll = false;
     h->poisoned = false;
     return SFAR_OK;
 }
@@ -608,34 +606,17 @@ sfar_status sfar_set_launch_mode(sfar_t *h, int mode)
     return SFAR_OK;
 }
 
-sfar_status sfar_test_set_trace(sfar_t *h, uint64_t *trace, uint32_t calls, sfar_stream_t s)
+sfar_status sfar_test_set_trace(sfar_t *h, uint64_t *trace, uint32_t calls)
 {
     if (!h)
         return SFAR_ERR_INVALID;
-    if (!trace)
-        calls = 0;
-    sfar_status r = launch_knob(h, KNOB_TRACE, 0, reinterpret_cast<const uint32_t *>(trace), calls, -1,
-                                (cudaStream_t)s);
-    if (r == SFAR_OK)
-        h->k_trace = calls > 0;
-    return r;
-}
-
-sfar_status sfar_test_set_poll_delay(sfar_t *h, uint32_t ns, sfar_stream_t s)
-{
-    if (!h)
-        return SFAR_ERR_INVALID;
-    sfar_status r = launch_knob(h, KNOB_POLL_DELAY, ns, nullptr, 0, -1, (cudaStream_t)s);
-    if (r == SFAR_OK)
-        h->k_poll = ns > 0;
-    return r;
-}
-
-sfar_status sfar_test_set_stagger(sfar_t *h, int cycles)
-{
-    if (!h || cycles < 0 || cycles > 100000)
-        return SFAR_ERR_INVALID;
-    h->stagger = cycles;
+    if (!trace || calls == 0) {
+        h->trace = nullptr;
+        h->trace_calls = 0;
+    } else {
+        h->trace = reinterpret_cast<unsigned long long *>(trace);
+        h->trace_calls = calls;
+    }
     return SFAR_OK;
 }
 

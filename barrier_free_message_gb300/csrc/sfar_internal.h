@@ -30,11 +30,6 @@ struct SfarCtl {
     int drop_rank;            // < 0: none
     int single_buffer;
     uint32_t strag_base[SFAR_KMAX];   // epoch of (rank 0, CTA k) when the straggler was armed
-    // tracing: SFAR_TRACE_POINTS %globaltimer stamps per (call, CTA)
-    unsigned long long *trace;
-    uint32_t trace_calls;
-    uint32_t poll_delay_ns;           // spin before the first poll of a receive
-    uint32_t trace_base[SFAR_KMAX];
 };
 #define SFAR_TRACE_POINTS 8
 
@@ -54,7 +49,8 @@ struct SfarArgs {
     uint32_t *fb;                 // flags [R][R][SFAR_KMAX]: bottom barrier / completion
     SfarCtl *ctl;
     int R, K, overlap, tile_bytes, stages;
-    int stagger;                  // LL / sentinel: SM cycles between the two poll rounds (0: one round)
+    unsigned long long *trace;    // NULL, or a ring of trace_calls entries per CTA (see sfar_test.h)
+    uint32_t trace_calls;
 };
 
 // Kernel lookup, one function per translation unit.  dt: 0 bf16, 1 fp32.
@@ -75,9 +71,7 @@ enum SfarKnob {
     KNOB_STRAG = 2,
     KNOB_DROP = 3,
     KNOB_SINGLE = 4,
-    KNOB_CLEAR_STATUS = 5,
-    KNOB_TRACE = 6,
-    KNOB_POLL_DELAY = 7
+    KNOB_CLEAR_STATUS = 5
 };
 struct SfarKnobArgs {
     SfarCtl *ctl;

@@ -128,20 +128,40 @@ __device__ __forceinline__ void pdl_wait()
 {
     asm volatile("griddepcontrol.wait;" ::: "memory");
 }
+// Brings a line into L2 (and its translation into the TLBs) without
+// returning data.  Safe before griddepcontrol.wait: L2 is the point of
+// coherence, so a later write by the previous kernel still updates the line.
+__device__ __forceinline__ void prefetch_l2(const void *p)
+{
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+
+// Trace stamps of one CTA (thread 0): kernel entry, and the moment the
+// programmatic-launch wait returned.  Recorded only when tracing is armed.
+struct SfarEntry {
+    unsigned long long t_entry, t_start;
+};
 
 // First statement of every AllReduce kernel.  In serial mode the kernel is
 // launched as a programmatic dependent of the previous kernel on the stream:
-// it lets its own successor be scheduled at once, then waits for its
-// predecessor to complete, so it sees exactly what plain stream order would
-// show it, but the launch of each kernel overlaps the end of the previous one.
-// In overlap mode the kernel does not wait (the prologue hands off inside one
-// rank instead).
-__device__ __forceinline__ void sfar_entry(const SfarArgs &a)
+// it waits for its predecessor to complete, so it sees exactly what plain
+// stream order would show it, and only then lets its own successor be
+// scheduled, so the successor's launch overlaps this kernel's work while at
+// most one launched kernel waits at any time.  In overlap mode the kernel
+// does not wait (the prologue hands off inside one rank instead).
+__device__ __forceinline__ SfarEntry sfar_entry(const SfarArgs &a)
 {
+    SfarEntry t{0, 0};
+    const bool tr = a.trace != nullptr && threadIdx.x == 0;
+    if (tr)
+        t.t_entry = globaltimer();
     if (!a.overlap) {
-        pdl_launch_dependents();
         pdl_wait();
+        pdl_launch_dependents();
     }
+    if (tr)
+        t.t_start = globaltimer();
+    return t;
 }
 
 // ------------------------------------------------------------ bounded waits
@@ -203,19 +223,36 @@ struct SfarCall {
     uint32_t e;     // this call's epoch (1, 2, ...) for (rank, CTA)
     int par;        // receive-buffer parity
     bool drop;      // test knob: this rank sends nothing
-    uint32_t mid_delay_ns;   // test knob: straggler delay between sends and receives
-    uint32_t poll_delay_ns;  // test knob: spin before the first poll
-    unsigned long long *trace;   // test knob: this CTA's stamps for this call (thread 0 only)
+    uint32_t mid_delay_ns;       // test knob: straggler delay between sends and receives
+    unsigned long long *trace;   // this CTA's trace entry for this call (thread 0 only), or NULL
 };
 
-// Trace points (test variants with tracing armed; thread 0's view).
-enum { TP_ENTRY = 0, TP_TICKET = 1, TP_SENT = 2, TP_RECEIVED = 3, TP_EXIT = 4 };
+// Trace points (thread 0's view); slot TP_EPOCH holds the epoch itself.
+enum {
+    TP_ENTRY = 0,      // kernel entry
+    TP_START = 1,      // programmatic-launch wait returned (serial mode)
+    TP_TICKET = 2,     // epoch known (overlap mode: after the hand-off)
+    TP_INPUT = 3,      // first input vector arrived
+    TP_SENT = 4,       // sends issued (DB / baseline: top barrier passed)
+    TP_RECEIVED = 5,   // receive and reduction done
+    TP_EXIT = 6,       // last statement
+    TP_EPOCH = 7
+};
 
-template <bool TEST>
 __device__ __forceinline__ void sfar_stamp(const SfarCall &c, int point)
 {
-    if (TEST && c.trace)
+    if (c.trace)
         c.trace[point] = globaltimer();
+}
+
+// Stamp once the value `dep` has arrived (the asm consumes it first).
+__device__ __forceinline__ void sfar_stamp_after(const SfarCall &c, int point, uint32_t dep)
+{
+    if (c.trace) {
+        uint32_t sink;
+        asm volatile("mov.b32 %0, %1;" : "=r"(sink) : "r"(dep));
+        c.trace[point] = globaltimer() + (sink & 0u);
+    }
 }
 
 __device__ __forceinline__ void spin_ns(unsigned long long d)
@@ -228,15 +265,12 @@ __device__ __forceinline__ void spin_ns(unsigned long long d)
 // Every thread of the CTA calls this.  Returns false if the CTA must exit at
 // once (the handle already holds a failure, or a wait gave up here).
 template <bool TEST>
-__device__ __forceinline__ bool sfar_prologue(const SfarArgs &a, int r, int k, SfarCall &c)
+__device__ __forceinline__ bool sfar_prologue(const SfarArgs &a, int r, int k, SfarCall &c, const SfarEntry &t)
 {
     __shared__ uint32_t s_e;
     __shared__ int s_flags;
-    unsigned long long t_entry = 0;
     c.trace = nullptr;
     if (threadIdx.x == 0) {
-        if (TEST)
-            t_entry = globaltimer();
         // Ticket: the epoch of this (rank, CTA).  Its latency overlaps the
         // input loads the caller has issued just before.
         const uint32_t e = atomicAdd(a.epoch + r * SFAR_KMAX + k, 1u) + 1u;
@@ -250,34 +284,29 @@ __device__ __forceinline__ bool sfar_prologue(const SfarArgs &a, int r, int k, S
         }
         s_e = e;
         s_flags = flags;
+        if (a.trace) {
+            c.trace = a.trace + ((size_t)(e % a.trace_calls) * gridDim.x + blockIdx.x) * SFAR_TRACE_POINTS;
+            c.trace[TP_ENTRY] = t.t_entry;
+            c.trace[TP_START] = t.t_start;
+            c.trace[TP_EPOCH] = e;
+        }
     }
     __syncthreads();
     c.e = s_e;
     const int flags = s_flags;
-    if (a.overlap)
-        pdl_launch_dependents();   // after the ticket: the next call's CTA (r, k) gets e + 1
-    if (flags & 1)
+    if (flags & 1) {
+        if (a.overlap)
+            pdl_launch_dependents();
         return false;
+    }
     c.drop = (flags & 2) != 0;
     c.par = (flags & 4) ? 0 : (int)(c.e & 1u);
     c.mid_delay_ns = 0;
-    c.poll_delay_ns = 0;
     if (a.overlap || TEST) {
         __shared__ int s_ok;
-        __shared__ uint32_t s_mid, s_pd;
+        __shared__ uint32_t s_mid;
         if (threadIdx.x == 0) {
             int ok = 1;
-            if (TEST) {
-                const volatile SfarCtl *ctl = a.ctl;
-                unsigned long long *tr = ctl->trace;
-                const uint32_t ti = c.e - ctl->trace_base[k] - 1u;
-                if (tr && ti < ctl->trace_calls) {
-                    c.trace = tr + ((size_t)ti * gridDim.x + blockIdx.x) * SFAR_TRACE_POINTS;
-                    c.trace[TP_ENTRY] = t_entry;
-                    c.trace[TP_TICKET] = globaltimer();
-                }
-                s_pd = ctl->poll_delay_ns;
-            }
             if (a.overlap) {
                 // wait for CTA (r, k) of the previous call: a wait inside one rank
                 SfarWaiter w(true);
@@ -310,12 +339,16 @@ __device__ __forceinline__ bool sfar_prologue(const SfarArgs &a, int r, int k, S
             s_mid = mid;
         }
         __syncthreads();
+        // Overlap mode: the next call's kernel may start once every CTA of
+        // this one holds its ticket and has seen its predecessor (r, k) done,
+        // which keeps at most two calls ahead of the oldest running one.
+        if (a.overlap)
+            pdl_launch_dependents();
         if (!s_ok)
             return false;
         c.mid_delay_ns = s_mid;
-        if (TEST)
-            c.poll_delay_ns = s_pd;
     }
+    sfar_stamp(c, TP_TICKET);
     return true;
 }
 
@@ -329,14 +362,6 @@ __device__ __forceinline__ void sfar_mid_delay(const SfarCall &c)
             spin_ns(c.mid_delay_ns);
         __syncthreads();
     }
-}
-
-// Test variants: every thread waits this long before its first poll.
-template <bool TEST>
-__device__ __forceinline__ void sfar_poll_delay(const SfarCall &c)
-{
-    if (TEST && c.poll_delay_ns)
-        spin_ns(c.poll_delay_ns);
 }
 
 // Marks (rank, CTA) done with epoch e.  In overlap mode the next call's CTA

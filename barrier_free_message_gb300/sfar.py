@@ -58,9 +58,7 @@ _SIGS = [
     ("sfar_test_force_single_buffer", ctypes.c_int, [ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p]),
     ("sfar_set_launch_mode", ctypes.c_int, [ctypes.c_void_p, ctypes.c_int]),
     ("sfar_test_set_geometry", ctypes.c_int, [ctypes.c_void_p, ctypes.c_int, ctypes.c_int]),
-    ("sfar_test_set_trace", ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_uint32, ctypes.c_void_p]),
-    ("sfar_test_set_poll_delay", ctypes.c_int, [ctypes.c_void_p, ctypes.c_uint32, ctypes.c_void_p]),
-    ("sfar_test_set_stagger", ctypes.c_int, [ctypes.c_void_p, ctypes.c_int]),
+    ("sfar_test_set_trace", ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_uint32]),
     ("sfar_probe_empty", ctypes.c_int, [ctypes.c_void_p]),
     ("sfar_probe_pingpong", ctypes.c_int, [ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_void_p,
                                            ctypes.c_void_p]),
@@ -175,16 +173,8 @@ def sfar_test_set_geometry(h, ctas_per_rank: int = 0, threads_per_cta: int = 0) 
     return lib().sfar_test_set_geometry(h, ctas_per_rank, threads_per_cta)
 
 
-def sfar_test_set_trace(h, trace_ptr: int, calls: int, stream=None) -> int:
-    return lib().sfar_test_set_trace(h, trace_ptr, calls, _stream(stream))
-
-
-def sfar_test_set_poll_delay(h, ns: int, stream=None) -> int:
-    return lib().sfar_test_set_poll_delay(h, ns, _stream(stream))
-
-
-def sfar_test_set_stagger(h, cycles: int) -> int:
-    return lib().sfar_test_set_stagger(h, cycles)
+def sfar_test_set_trace(h, trace_ptr: int, calls: int) -> int:
+    return lib().sfar_test_set_trace(h, trace_ptr, calls)
 
 
 def sfar_probe_empty(stream=None) -> int:

@@ -66,24 +66,18 @@ sfar_status sfar_test_force_single_buffer(sfar_t *h, int on, sfar_stream_t s);
 sfar_status sfar_set_launch_mode(sfar_t *h, int mode);
 
 /*
- * Tracing.  From the next call on, for `calls` calls, thread 0 of every CTA
- * writes %globaltimer nanoseconds at 8 slots per (call, CTA):
- * trace[(call * grid + blockIdx) * 8 + point], points 0 = kernel entry,
- * 1 = epoch ticket received, 2 = sends issued (DB/baseline: top barrier
- * passed), 3 = receive and reduction done, 4 = exit; 5..7 unused.  grid is
- * R * CTAs per rank of that call.  trace is a DEVICE array of uint64 owned by
- * the caller, sized for calls * grid * 8; NULL or calls == 0 disarms.
+ * Tracing.  Calls made after this (it is a kernel argument: a captured graph
+ * keeps the setting it was captured with) have thread 0 of every CTA write
+ * %globaltimer nanoseconds into a ring: entry (e mod calls) of CTA b is
+ * trace[((e mod calls) * grid + b) * 8 + point], e the CTA's epoch and grid
+ * R * CTAs per rank of that call.  Points: 0 kernel entry, 1 programmatic
+ * launch wait returned, 2 epoch known (overlap mode: after the hand-off),
+ * 3 first input vector arrived, 4 sends issued (DB/baseline: top barrier
+ * passed), 5 receive and reduction done, 6 exit; slot 7 holds e itself.
+ * trace is a DEVICE array of calls * grid * 8 uint64 owned by the caller;
+ * NULL or calls == 0 disarms.
  */
-sfar_status sfar_test_set_trace(sfar_t *h, uint64_t *trace, uint32_t calls, sfar_stream_t s);
-
-/* Every receiving thread spins this many nanoseconds before its first poll
- * (one-shot LL and sentinel); 0 disarms. */
-sfar_status sfar_test_set_poll_delay(sfar_t *h, uint32_t ns, sfar_stream_t s);
-
-/* One-shot LL and sentinel with R <= 8: keep a second round of polls in
- * flight, issued `cycles` SM cycles after the first (0 = one round only; at
- * most 100000).  Takes effect for calls made after it. */
-sfar_status sfar_test_set_stagger(sfar_t *h, int cycles);
+sfar_status sfar_test_set_trace(sfar_t *h, uint64_t *trace, uint32_t calls);
 
 /* Launch geometry of every later call of the receive-buffer protocols:
  * CTAs per rank (0 = automatic; clamped to what can be co-resident) and
