@@ -19,8 +19,7 @@ __global__ void k_set_knob(const SfarKnobArgs k)
         c->strag_len = k.len;
         c->strag_rank = k.rank;
         c->strag_phase = k.phase;
-        for (int i = 0; i < SFAR_KMAX; ++i)
-            c->strag_base[i] = k.epoch_row0[i];
+        c->strag_base = (uint32_t)(k.epoch0[0] / SFAR_KMAX);
         break;
     case KNOB_DROP:
         c->drop_rank = k.rank;

@@ -40,7 +40,8 @@ struct sfar {
     uint8_t *ws = nullptr;
     size_t ws_bytes = 0;
     size_t ctl_bytes = 0;               // the status block sits at the start of ws
-    uint32_t *epoch = nullptr, *done = nullptr;
+    unsigned long long *epoch = nullptr;   // [R] per-rank call counters
+    uint32_t *done = nullptr;
     uint32_t *fa = nullptr, *fb = nullptr, *fc = nullptr, *fd = nullptr;
     SfarCtl *ctl = nullptr;
     uint8_t *r_raw = nullptr, *r_ll = nullptr, *r_ll128 = nullptr, *r_sent = nullptr;
@@ -48,6 +49,9 @@ struct sfar {
     size_t s_raw = 0, s_ll = 0, s_ll128 = 0, s_2s = 0, sent_bytes = 0;
     int mode = SFAR_LAUNCH_SERIAL;
     int ctas_override = 0, threads_override = 0;
+    long long last_key = -1;            // overlap mode: geometry of the previous call
+    sfar_stream_t last_stream = nullptr;
+    unsigned long long last_capture = 0;
     unsigned long long *trace = nullptr; // test hook: trace ring (device), calls per CTA
     uint32_t trace_calls = 0;
     bool k_strag = false, k_drop = false, k_single = false;
@@ -166,7 +170,7 @@ static sfar_status launch_knob(sfar *h, int which, unsigned long long value, con
     k.len = len;
     k.rank = rank;
     k.phase = phase;
-    k.epoch_row0 = h->epoch;
+    k.epoch0 = h->epoch;
     void *args[] = {&k};
     int cur = -1;
     cudaGetDevice(&cur);
@@ -252,7 +256,7 @@ sfar_t *sfar_create(int R, size_t max_bytes, sfar_dtype dt)
     };
     const size_t o_ctl = carve(sizeof(SfarCtl));
     h->ctl_bytes = off;
-    const size_t o_epoch = carve((size_t)R * SFAR_KMAX * 4);
+    const size_t o_epoch = carve((size_t)R * sizeof(unsigned long long));
     const size_t o_done = carve((size_t)R * SFAR_KMAX * 4);
     const size_t o_fa = carve((size_t)R * R * SFAR_KMAX * 4);
     const size_t o_fb = carve((size_t)R * R * SFAR_KMAX * 4);
@@ -274,7 +278,7 @@ sfar_t *sfar_create(int R, size_t max_bytes, sfar_dtype dt)
         return nullptr;
     }
     h->ctl = reinterpret_cast<SfarCtl *>(h->ws + o_ctl);
-    h->epoch = reinterpret_cast<uint32_t *>(h->ws + o_epoch);
+    h->epoch = reinterpret_cast<unsigned long long *>(h->ws + o_epoch);
     h->done = reinterpret_cast<uint32_t *>(h->ws + o_done);
     h->fa = reinterpret_cast<uint32_t *>(h->ws + o_fa);
     h->fb = reinterpret_cast<uint32_t *>(h->ws + o_fb);
@@ -447,7 +451,26 @@ sfar_status sfar_allreduce(sfar_t *h, const void *const in[], void *const out[],
     a.ctl = h->ctl;
     a.R = R;
     a.K = K;
-    a.overlap = h->mode == SFAR_LAUNCH_OVERLAP;
+    // Overlap mode lets a call overtake the previous one only when the two
+    // run the same kernel geometry on the same stream (the hand-off is between
+    // CTAs of the same index); the first call of a graph capture, or one after
+    // a change, is launched with serial semantics.
+    a.overlap = 0;
+    if (h->mode == SFAR_LAUNCH_OVERLAP) {
+        cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+        unsigned long long cap = 0;
+        if (cudaStreamGetCaptureInfo((cudaStream_t)s, &cs, &cap) != cudaSuccess) {
+            cudaGetLastError();
+            cs = cudaStreamCaptureStatusNone;
+        }
+        if (cs != cudaStreamCaptureStatusActive)
+            cap = 0;
+        const long long key = ((long long)p << 40) | ((long long)K << 16) | threads;
+        a.overlap = (key == h->last_key && s == h->last_stream && cap == h->last_capture) ? 1 : 0;
+        h->last_key = key;
+        h->last_stream = s;
+        h->last_capture = cap;
+    }
     a.trace = h->trace;
     a.trace_calls = h->trace_calls;
     switch (p) {
@@ -556,6 +579,7 @@ sfar_status sfar_reset(sfar_t *h, sfar_stream_t s)
     h->k_strag = false;
     h->k_drop = false;
     h->poisoned = false;
+    h->last_key = -1;
     return SFAR_OK;
 }
 
@@ -603,6 +627,7 @@ sfar_status sfar_set_launch_mode(sfar_t *h, int mode)
     if (!h || (mode != SFAR_LAUNCH_SERIAL && mode != SFAR_LAUNCH_OVERLAP && mode != SFAR_LAUNCH_PLAIN))
         return SFAR_ERR_INVALID;
     h->mode = mode;
+    h->last_key = -1;
     return SFAR_OK;
 }
 

@@ -29,7 +29,7 @@ struct SfarCtl {
     int strag_phase;          // 0: before the sends, 1: between sends and receives
     int drop_rank;            // < 0: none
     int single_buffer;
-    uint32_t strag_base[SFAR_KMAX];   // epoch of (rank 0, CTA k) when the straggler was armed
+    uint32_t strag_base;              // last epoch when the straggler was armed
 };
 #define SFAR_TRACE_POINTS 8
 
@@ -43,7 +43,7 @@ struct SfarArgs {
     unsigned long long sub;       // TMA path: elements per CTA range within a chunk
     uint8_t *region;              // receive region of the protocol
     uint8_t *region2;             // two-shot: all-gather region
-    uint32_t *epoch;              // [R][SFAR_KMAX] call counters
+    unsigned long long *epoch;    // [R] call counters: + SFAR_KMAX per call (see the prologue)
     uint32_t *done;               // [R][SFAR_KMAX] last finished epoch (overlap mode)
     uint32_t *fa;                 // flags [R][R][SFAR_KMAX]: ready / top barrier / arrival
     uint32_t *fb;                 // flags [R][R][SFAR_KMAX]: bottom barrier / completion
@@ -81,5 +81,5 @@ struct SfarKnobArgs {
     uint32_t len;
     int rank;
     int phase;
-    const uint32_t *epoch_row0;   // epoch[0][*] for the straggler base
+    const unsigned long long *epoch0;   // rank 0's call counter, for the straggler base
 };

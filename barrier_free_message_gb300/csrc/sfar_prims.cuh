@@ -143,22 +143,21 @@ struct SfarEntry {
 };
 
 // First statement of every AllReduce kernel.  In serial mode the kernel is
-// launched as a programmatic dependent of the previous kernel on the stream:
-// it waits for its predecessor to complete, so it sees exactly what plain
-// stream order would show it, and only then lets its own successor be
-// scheduled, so the successor's launch overlaps this kernel's work while at
-// most one launched kernel waits at any time.  In overlap mode the kernel
-// does not wait (the prologue hands off inside one rank instead).
+// launched as a programmatic dependent of the previous kernel on the stream
+// and waits here for its predecessor to complete, so it sees exactly what
+// plain stream order would show it; the prologue then lets its own successor
+// be scheduled once every CTA holds its ticket, so the successor's launch
+// overlaps this kernel's work while at most one launched kernel waits.  In
+// overlap mode the kernel does not wait (the prologue hands off inside one
+// rank instead).
 __device__ __forceinline__ SfarEntry sfar_entry(const SfarArgs &a)
 {
     SfarEntry t{0, 0};
     const bool tr = a.trace != nullptr && threadIdx.x == 0;
     if (tr)
         t.t_entry = globaltimer();
-    if (!a.overlap) {
+    if (!a.overlap)
         pdl_wait();
-        pdl_launch_dependents();
-    }
     if (tr)
         t.t_start = globaltimer();
     return t;
@@ -271,9 +270,17 @@ __device__ __forceinline__ bool sfar_prologue(const SfarArgs &a, int r, int k, S
     __shared__ int s_flags;
     c.trace = nullptr;
     if (threadIdx.x == 0) {
-        // Ticket: the epoch of this (rank, CTA).  Its latency overlaps the
-        // input loads the caller has issued just before.
-        const uint32_t e = atomicAdd(a.epoch + r * SFAR_KMAX + k, 1u) + 1u;
+        // Ticket.  Every CTA of rank r adds to the rank's call counter: CTA 0
+        // adds SFAR_KMAX - K + 1, the others 1, so each call adds exactly
+        // SFAR_KMAX and every CTA of call c (counted from 0) receives a value
+        // in [c * SFAR_KMAX, (c + 1) * SFAR_KMAX) whatever the order of the
+        // atomics: all CTAs agree on the epoch c + 1, and the epoch is the
+        // same for every launch geometry.  Calls never interleave their
+        // tickets (stream order, or in overlap mode the launch of the next
+        // call after every CTA of this one holds its ticket).  The latency
+        // overlaps the input load the caller issued just before.
+        const unsigned long long add = k == 0 ? (unsigned long long)(SFAR_KMAX - a.K + 1) : 1ull;
+        const uint32_t e = (uint32_t)(atomicAdd(a.epoch + r, add) / SFAR_KMAX) + 1u;
         int flags = ld_relaxed_s32(&a.ctl->status) != 0 ? 1 : 0;
         if (TEST) {
             const volatile SfarCtl *ctl = a.ctl;
@@ -294,11 +301,12 @@ __device__ __forceinline__ bool sfar_prologue(const SfarArgs &a, int r, int k, S
     __syncthreads();
     c.e = s_e;
     const int flags = s_flags;
-    if (flags & 1) {
-        if (a.overlap)
-            pdl_launch_dependents();
+    // The successor may take its tickets only after all of ours are taken
+    // (a successor in overlap mode does not wait for this kernel to end).
+    if (!a.overlap || (flags & 1))
+        pdl_launch_dependents();
+    if (flags & 1)
         return false;
-    }
     c.drop = (flags & 2) != 0;
     c.par = (flags & 4) ? 0 : (int)(c.e & 1u);
     c.mid_delay_ns = 0;
@@ -324,7 +332,7 @@ __device__ __forceinline__ bool sfar_prologue(const SfarArgs &a, int r, int k, S
                 const volatile SfarCtl *ctl = a.ctl;
                 const uint32_t len = ctl->strag_len;
                 if (len) {
-                    const uint32_t idx = c.e - ctl->strag_base[k] - 1u;
+                    const uint32_t idx = c.e - ctl->strag_base - 1u;
                     const int who = ctl->strag_rank < 0 ? (int)(idx % (uint32_t)a.R) : ctl->strag_rank;
                     if (who == r && idx < 0x40000000u) {
                         const uint32_t d = ctl->strag_delays[idx % len];

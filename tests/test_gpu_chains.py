@@ -229,6 +229,47 @@ def test_message_sweep(R, proto):
         h.close()
 
 
+# ------------------------------------------------- mixed sizes on one handle
+@pytest.mark.parametrize("mode", ["serial", "overlap"])
+@pytest.mark.parametrize("proto", ALL_PROTOS)
+def test_alternating_sizes_on_one_handle(proto, mode):
+    """Sizes whose launch geometries differ (16 KB: 16 CTAs x 64 threads per
+    rank, 20 KB: 10 x 128, ...) alternate on one handle inside one graph.  A
+    receive-buffer address then belongs to different CTAs from call to call,
+    so a flag left by one call must never pass for the next call's."""
+    R = 8
+    sizes = [8192, 10240, 8192 + 3000, 2000, 10240, 8192]
+    calls = 240
+    h = sfar.Sfar(R, 1 << 20, "bf16")
+    try:
+        h.set_mode(mode)
+        xs, outs, exps = [], [], []
+        for c in range(calls):
+            n = sizes[c % len(sizes)]
+            x = inputs.draw(21, c, R, n, "normal", 1.0, "bf16")
+            xs.append(x.cuda())
+            outs.append(torch.empty_like(xs[-1]))
+            exps.append(expected_bits(x))
+        for n in set(sizes):
+            warm(h, proto, R, n, "bf16")
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for c in range(calls):
+                code = sfar.sfar_allreduce(h.h, [xs[c][r].data_ptr() for r in range(R)],
+                                           [outs[c][r].data_ptr() for r in range(R)], xs[c].shape[1], proto)
+                assert code == sfar.SFAR_OK
+        for rep in range(2):
+            for o in outs:
+                o.view(torch.int16).fill_(-1)
+            g.replay()
+            torch.cuda.synchronize()
+            status_ok(h.h, f"{proto} {mode} replay {rep}")
+            for c in range(calls):
+                assert_bits_equal(list(outs[c]), exps[c], f"{proto} {mode} call {c} n={xs[c].shape[1]}")
+    finally:
+        h.close()
+
+
 # ------------------------------------------------------------ failure paths
 @pytest.mark.parametrize("proto", ALL_PROTOS)
 def test_dropped_rank_times_out_and_reset_recovers(proto):
