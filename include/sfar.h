@@ -93,7 +93,7 @@ typedef struct {
     int rank;         /* simulated rank whose wait gave up                    */
     int cta;          /* CTA index within that rank                           */
     int peer;         /* rank it was waiting for (-1 if not one rank)         */
-    uint32_t epoch;   /* call epoch (starts at 1, +1 per call per CTA)        */
+    uint32_t epoch;   /* call epoch (1 for the handle's first call, +1 per call) */
     int where;        /* SFAR_WAIT_*                                          */
 } sfar_fault;
 
@@ -102,8 +102,9 @@ typedef struct {
  * CUDA device, for messages of up to max_bytes per rank (> 0) of type dt.
  * Allocates, on the current device, the receive regions of every protocol
  * (double-buffered: [rank][parity][sender][wire bytes]; the sentinel region
- * prefilled with all-ones), the flag arrays, per-(rank, CTA) epoch counters
- * and a status block, and zero-initialises them.  The receive-buffer
+ * prefilled with all-ones), the flag arrays, one call counter per rank (the
+ * epoch of every call) and a status block, and zero-initialises them.  The
+ * receive-buffer
  * protocols (every protocol but SFAR_TWOSHOT_TMA) handle up to
  * min(max_bytes, 2 MiB) per rank; SFAR_TWOSHOT_TMA handles up to max_bytes.
  * The library owns everything it allocates.  Returns NULL on error and sets
