@@ -51,6 +51,8 @@ _SIGS = [
     ("sfar_query_launch", ctypes.c_int, [ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int,
                                          ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_int)]),
     ("sfar_max_bytes", ctypes.c_size_t, [ctypes.c_void_p, ctypes.c_int]),
+    ("sfar_allreduce_noalloc", ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t,
+                                              ctypes.c_int, ctypes.c_void_p]),
     ("sfar_test_set_straggler", ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_uint32, ctypes.c_int,
                                                ctypes.c_int, ctypes.c_void_p]),
     ("sfar_test_drop_rank", ctypes.c_int, [ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p]),
@@ -119,6 +121,11 @@ def sfar_create(R: int, max_bytes: int, dtype="bf16"):
 def sfar_allreduce(h, in_ptrs, out_ptrs, n: int, proto="ll", stream=None) -> int:
     p = PROTOS[proto] if isinstance(proto, str) else int(proto)
     return lib().sfar_allreduce(h, _ptr_array(in_ptrs), _ptr_array(out_ptrs), n, p, _stream(stream))
+
+
+def sfar_allreduce_noalloc(in_ptrs, out_ptrs, R: int, n: int, dtype="bf16", stream=None) -> int:
+    dt = DTYPES[dtype] if isinstance(dtype, str) else int(dtype)
+    return lib().sfar_allreduce_noalloc(_ptr_array(in_ptrs), _ptr_array(out_ptrs), R, n, dt, _stream(stream))
 
 
 def sfar_status_get(h):

@@ -166,6 +166,38 @@ sfar_status sfar_query_launch(const sfar_t *h, size_t n, sfar_proto p, int *ctas
 /* Largest n * element size per rank that protocol p accepts on this handle. */
 size_t sfar_max_bytes(const sfar_t *h, sfar_proto p);
 
+/*
+ * sfar_allreduce_noalloc: the same AllReduce as sfar_allreduce(h, in, out, n,
+ * SFAR_LL, s) on a handle of R ranks and type dt, for callers that cannot
+ * allocate device memory at the moment they need it: code running under
+ * stream capture (cudaMalloc is not allowed there), code inside a framework
+ * whose allocator owns all device memory, and latency paths that cannot pay
+ * for cudaMalloc's implicit synchronisation.  There is no counterpart in the
+ * pages; it is a convenience of this library.
+ *
+ * No handle and no allocation: the kernel's working memory is one fixed
+ * array of about 13 MiB compiled into the library, present on every GPU that
+ * loads the library until the process exits.  in/out are host arrays of R
+ * device pointers as for sfar_allreduce (16-byte aligned, no output
+ * overlapping an input or another output).  Limits: 2 <= R <=
+ * SFAR_NOALLOC_MAX_RANKS and n * element size <= SFAR_NOALLOC_MAX_BYTES;
+ * anything larger returns SFAR_ERR_INVALID and enqueues nothing.
+ *
+ * The first call on each device sets the array up (finds its address,
+ * checks that the grid fits, clears it) and synchronises stream s, so make
+ * that first call before any stream capture; later calls only enqueue one
+ * kernel and can be captured.  All calls share the array and it keeps what
+ * the last call left (its call counters keep counting); calls whose kernels
+ * overlap on the GPU, e.g. on two streams at once, race on it.  Returns
+ * SFAR_ERR_UNSUPPORTED on a device that is not sm_103 and SFAR_ERR_CUDA if a
+ * CUDA call fails.  A device-side failure stays recorded in the array and
+ * makes later calls return without writing their outputs.
+ */
+#define SFAR_NOALLOC_MAX_RANKS 8
+#define SFAR_NOALLOC_MAX_BYTES 16384
+sfar_status sfar_allreduce_noalloc(const void *const in[], void *const out[], int R, size_t n, sfar_dtype dt,
+                                   sfar_stream_t s);
+
 #ifdef __cplusplus
 }
 #endif

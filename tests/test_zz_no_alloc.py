@@ -1,0 +1,95 @@
+"""The allocation-free entry point (sfar_allreduce_noalloc) against the
+regular one.
+
+sfar_allreduce_noalloc exists for callers that cannot allocate device memory
+when they need an AllReduce (under stream capture, inside a framework whose
+allocator owns all device memory, or on a path that cannot afford
+cudaMalloc's implicit synchronisation); it takes its working memory from a
+fixed array compiled into the library.  This file is named so that pytest
+collects it last.  It must pass on its own in a fresh process and after the
+other tests.
+"""
+import numpy as np
+import pytest
+import torch
+
+from barrier_free_message_gb300 import inputs, sfar
+from gpu_helpers import as_uint, device_io, ensure_built, expected_bits, status_ok
+
+pytestmark = pytest.mark.gpu
+
+MAX_RANKS = 8
+MAX_BYTES = 16384
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    ensure_built()
+
+
+def _bits(t):
+    return as_uint(inputs.to_bits(t.cpu()))
+
+
+@pytest.mark.parametrize("dtype,R,n", [("bf16", 8, 8192), ("bf16", 4, 4099), ("fp32", 8, 4096), ("fp32", 3, 37)])
+def test_noalloc_matches_the_handle_path_on_two_calls(dtype, R, n):
+    h = sfar.Sfar(R, MAX_BYTES, dtype)
+    try:
+        for call in range(2):      # two calls in a row: the second reuses the shared array
+            x = inputs.draw(31, call, R, n, "normal", 1.0, dtype)
+            ins, outs_ref = device_io(x)
+            outs_na = [torch.empty_like(t) for t in ins]
+            for o in outs_na:
+                o.view(torch.uint8).fill_(0x5A)
+            h.allreduce(ins, outs_ref, "ll")
+            code = sfar.sfar_allreduce_noalloc([t.data_ptr() for t in ins], [t.data_ptr() for t in outs_na],
+                                               R, n, dtype)
+            assert code == sfar.SFAR_OK, sfar.strerror(code)
+            torch.cuda.synchronize()
+            status_ok(h.h)
+            want = expected_bits(x)
+            for r in range(R):
+                # bit-exact: the same fixed-order reduction on both paths
+                assert np.array_equal(_bits(outs_na[r]), _bits(outs_ref[r])), (call, r)
+                assert np.array_equal(_bits(outs_na[r]), as_uint(want[r])), (call, r)
+    finally:
+        h.close()
+
+
+def test_noalloc_in_a_graph_after_setup():
+    R, n = 8, 8192
+    xs = [inputs.draw(32, c, R, n, "normal", 1.0, "bf16") for c in range(4)]
+    io = [device_io(x) for x in xs]
+    # the first call sets the array up (not under capture)
+    ins, outs = io[0]
+    assert sfar.sfar_allreduce_noalloc([t.data_ptr() for t in ins], [t.data_ptr() for t in outs], R, n) == 0
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for ins, outs in io:
+            assert sfar.sfar_allreduce_noalloc([t.data_ptr() for t in ins], [t.data_ptr() for t in outs], R,
+                                               n) == 0
+    for _ in range(2):
+        for _, outs in io:
+            for o in outs:
+                o.view(torch.int16).fill_(-1)
+        g.replay()
+        torch.cuda.synchronize()
+        for x, (_, outs) in zip(xs, io):
+            want = expected_bits(x)
+            for r in range(R):
+                assert np.array_equal(_bits(outs[r]), as_uint(want[r]))
+
+
+def test_noalloc_rejects_what_does_not_fit():
+    R, n = 8, MAX_BYTES // 2
+    x = torch.zeros(R, n + 8, dtype=torch.bfloat16)
+    ins, outs = device_io(x)
+    ip, op = [t.data_ptr() for t in ins], [t.data_ptr() for t in outs]
+    assert sfar.sfar_allreduce_noalloc(ip, op, R, n + 1, "bf16") == sfar.SFAR_ERR_INVALID          # too many bytes
+    assert sfar.sfar_allreduce_noalloc(ip * 2, op * 2, 9, 64, "bf16") == sfar.SFAR_ERR_INVALID     # too many ranks
+    assert sfar.sfar_allreduce_noalloc(ip, op, 1, 64, "bf16") == sfar.SFAR_ERR_INVALID             # too few ranks
+    assert sfar.sfar_allreduce_noalloc(ip, [op[0] + 2] + op[1:], R, 64, "bf16") == sfar.SFAR_ERR_INVALID
+    assert sfar.sfar_allreduce_noalloc(ip, [ip[0]] + op[1:], R, 64, "bf16") == sfar.SFAR_ERR_INVALID
+    assert sfar.sfar_allreduce_noalloc(ip, op, R, 0, "bf16") == sfar.SFAR_OK                       # empty: no-op
+    torch.cuda.synchronize()
