@@ -56,12 +56,18 @@ __device__ __forceinline__ uint32_t pp_load(const uint32_t *p, int relaxed)
     return relaxed ? ld_relaxed_u32(p) : ld_acquire_u32(p);
 }
 
-__global__ void k_pingpong(uint32_t *flags, int trips, int relaxed, unsigned long long *ns_out)
+// The grid has one CTA per SM (shared-memory size); CTA 0 and CTA `partner`
+// play, the others leave at once.  out[1], out[2] get the two SM ids.
+__global__ void k_pingpong(uint32_t *flags, int trips, int relaxed, int partner, unsigned long long *out)
 {
     extern __shared__ uint8_t pad[];
-    if (threadIdx.x != 0)
+    if (threadIdx.x != 0 || (blockIdx.x != 0 && (int)blockIdx.x != partner))
         return;
     pad[0] = 0;
+    uint32_t smid;
+    asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
+    out[blockIdx.x == 0 ? 1 : 2] = smid;
+    unsigned long long *ns_out = out;
     uint32_t *ping = flags, *pong = flags + 32;
     const unsigned long long limit = 1000000000ull;
     const unsigned long long start = globaltimer();

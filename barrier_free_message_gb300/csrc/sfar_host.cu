@@ -663,17 +663,27 @@ sfar_status sfar_probe_empty(sfar_stream_t s)
     return SFAR_OK;
 }
 
-sfar_status sfar_probe_pingpong(uint32_t *flags, int trips, int relaxed, uint64_t *ns_out, sfar_stream_t s)
+sfar_status sfar_probe_pingpong(uint32_t *flags, int trips, int relaxed, int partner, uint64_t *out,
+                                sfar_stream_t s)
 {
-    if (!flags || !ns_out || trips < 1)
+    if (!flags || !out || trips < 1 || partner < 1)
         return SFAR_ERR_INVALID;
-    // > half of an SM's shared memory each, so the two CTAs sit on different SMs
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+        cudaGetLastError();
+        return SFAR_ERR_CUDA;
+    }
+    if (partner >= sms)
+        return SFAR_ERR_INVALID;
+    // > half of an SM's shared memory each: one CTA per SM, all resident at once
     const int smem = 120 * 1024;
-    unsigned long long *ns = reinterpret_cast<unsigned long long *>(ns_out);
-    void *args[] = {&flags, &trips, &relaxed, &ns};
+    unsigned long long *o = reinterpret_cast<unsigned long long *>(out);
+    void *args[] = {&flags, &trips, &relaxed, &partner, &o};
     if (cudaFuncSetAttribute(sfar_kernel_pingpong(), cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess ||
         cudaMemsetAsync(flags, 0, 64 * sizeof(uint32_t), (cudaStream_t)s) != cudaSuccess ||
-        cudaLaunchKernel(sfar_kernel_pingpong(), dim3(2), dim3(32), args, smem, (cudaStream_t)s) != cudaSuccess) {
+        cudaLaunchKernel(sfar_kernel_pingpong(), dim3(partner + 1), dim3(32), args, smem, (cudaStream_t)s) !=
+            cudaSuccess) {
         cudaGetLastError();
         return SFAR_ERR_CUDA;
     }

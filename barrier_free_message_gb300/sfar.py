@@ -62,8 +62,8 @@ _SIGS = [
     ("sfar_test_set_geometry", ctypes.c_int, [ctypes.c_void_p, ctypes.c_int, ctypes.c_int]),
     ("sfar_test_set_trace", ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_uint32]),
     ("sfar_probe_empty", ctypes.c_int, [ctypes.c_void_p]),
-    ("sfar_probe_pingpong", ctypes.c_int, [ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_void_p,
-                                           ctypes.c_void_p]),
+    ("sfar_probe_pingpong", ctypes.c_int, [ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                           ctypes.c_void_p, ctypes.c_void_p]),
 ]
 
 
@@ -188,8 +188,9 @@ def sfar_probe_empty(stream=None) -> int:
     return lib().sfar_probe_empty(_stream(stream))
 
 
-def sfar_probe_pingpong(flags_ptr: int, trips: int, ns_ptr: int, relaxed: bool = False, stream=None) -> int:
-    return lib().sfar_probe_pingpong(flags_ptr, trips, 1 if relaxed else 0, ns_ptr, _stream(stream))
+def sfar_probe_pingpong(flags_ptr: int, trips: int, out_ptr: int, relaxed: bool = False, partner: int = 1,
+                        stream=None) -> int:
+    return lib().sfar_probe_pingpong(flags_ptr, trips, 1 if relaxed else 0, partner, out_ptr, _stream(stream))
 
 
 # --------------------------------------------------------- convenience class

@@ -145,11 +145,19 @@ def measured_peaks():
         return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}, "fallback"
 
 
-def kernel_sources_hash():
+KERNEL_SOURCES = {"k_ll": "k_ll.cu", "k_sentinel": "k_sentinel.cu", "k_db": "k_db.cu", "k_baseline": "k_db.cu",
+                  "k_ll128": "k_ll128.cu", "k_tma": "k_tma.cu"}
+
+
+def kernel_sources_hash(kernel: str) -> str:
+    """Hash of the files that make up one kernel (its .cu and the shared headers)."""
     h = hashlib.sha256()
-    for p in sorted(glob.glob(os.path.join(ROOT, "barrier_free_message_gb300", "csrc", "*"))):
-        with open(p, "rb") as f:
-            h.update(f.read())
+    csrc = os.path.join(ROOT, "barrier_free_message_gb300", "csrc")
+    for name in (KERNEL_SOURCES.get(kernel, ""), "sfar_prims.cuh", "sfar_internal.h"):
+        p = os.path.join(csrc, name)
+        if os.path.isfile(p):
+            with open(p, "rb") as f:
+                h.update(f.read())
     return h.hexdigest()[:16]
 
 
@@ -160,7 +168,7 @@ def profiled_traffic(kernel: str):
         with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
             t = json.load(f)
         e = t.get(kernel)
-        if e and e.get("sources") == kernel_sources_hash():
+        if e and e.get("sources") == kernel_sources_hash(kernel):
             return e.get("dram_bytes_per_launch")
     except Exception:
         pass
@@ -235,23 +243,34 @@ def floor_probe():
     torch.cuda.synchronize()
     empty_us = s.elapsed_time(e) * 1000.0 / (reps * CALLS_PER_STEP)
     flags = torch.zeros(64, dtype=torch.int32, device="cuda")
-    ns = torch.zeros(1, dtype=torch.int64, device="cuda")
-    trips = 100000
+    out = torch.zeros(3, dtype=torch.int64, device="cuda")
+    trips = 20000
+    sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+    # partners spread over the grid: which SMs the two CTAs land on (same die
+    # or not) sets the round trip, and the AllReduce's CTAs cover every SM
+    partners = sorted(set(max(1, min(sms - 1, round(i * (sms - 1) / 15))) for i in range(16)))
 
-    def rtt(relaxed):
+    def rtt(relaxed, partner):
         best = None
-        for _ in range(3):
-            assert sfar.sfar_probe_pingpong(flags.data_ptr(), trips, ns.data_ptr(), relaxed) == sfar.SFAR_OK
+        for _ in range(2):
+            assert sfar.sfar_probe_pingpong(flags.data_ptr(), trips, out.data_ptr(), relaxed, partner) == sfar.SFAR_OK
             torch.cuda.synchronize()
-            v = int(ns.item())
-            if v < 0:
+            v = out.cpu().tolist()
+            if v[0] < 0:
                 raise RuntimeError("ping-pong probe timed out")
-            best = v / trips / 1000.0 if best is None else min(best, v / trips / 1000.0)
+            us = v[0] / trips / 1000.0
+            best = (us, v[1], v[2]) if best is None or us < best[0] else best
         return best
 
-    rtt_us = rtt(False)
-    return {"empty_kernel_us": empty_us, "flag_rtt_us": rtt_us, "floor_us": empty_us + rtt_us,
-            "relaxed_flag_rtt_us": rtt(True)}
+    acq = [rtt(False, p) for p in partners]
+    rel = [rtt(True, p) for p in partners]
+    a_us = sorted(x[0] for x in acq)
+    r_us = sorted(x[0] for x in rel)
+    slow = max(acq)
+    return {"empty_kernel_us": empty_us, "flag_rtt_us": a_us[-1], "floor_us": empty_us + a_us[-1],
+            "flag_rtt_min_us": a_us[0], "flag_rtt_median_us": a_us[len(a_us) // 2],
+            "relaxed_flag_rtt_us": r_us[-1], "relaxed_flag_rtt_min_us": r_us[0],
+            "slowest_pair_sm": [slow[1], slow[2]], "pairs": len(partners)}
 
 
 def spot_check(out_dev, x_host, calls):
@@ -462,7 +481,8 @@ def run_ours(args, world, rank):
                        "threads_per_cta": threads,
                        "l2": "inputs larger than L2: 64 token buffers, 1.34 GB, cycled",
                        "parallelism": f"replicas x{args.gpus}"},
-            "protocols": per_proto, "floor": {k2: round(v, 3) for k2, v in floor.items()},
+            "protocols": per_proto,
+            "floor": {k2: (round(v, 3) if isinstance(v, float) else v) for k2, v in floor.items()},
             "vs_floor": round(us / floor["floor_us"], 3),
             "roofline": roofline, "roofline_large": large,
             "e2e": ({"value": round(e2e_us, 3), "unit": "us/call", "h2d_bytes_per_step": step_bytes,

@@ -88,16 +88,19 @@ sfar_status sfar_test_set_geometry(sfar_t *h, int ctas_per_rank, int threads_per
 /*
  * Latency floor probes.
  * sfar_probe_empty: enqueue one empty kernel (1 CTA, 32 threads) on s.
- * sfar_probe_pingpong: enqueue one kernel of two CTAs on different SMs that
- *   pass a token `trips` times through two flags in global memory
- *   (relaxed == 0: st.release / ld.acquire at GPU scope; relaxed != 0:
- *   relaxed GPU-scope stores and loads); ns_out (device, 1 uint64) gets the
- *   elapsed %globaltimer nanoseconds.  flags is a device array of 64 uint32
- *   that the probe zeroes first.  Waits are bounded (1 s); on timeout ns_out
- *   gets UINT64_MAX.
+ * sfar_probe_pingpong: enqueue one kernel of partner + 1 CTAs, one per SM;
+ *   CTA 0 and CTA `partner` (1 <= partner < SM count) pass a token `trips`
+ *   times through two flags in global memory (relaxed == 0: st.release /
+ *   ld.acquire at GPU scope; relaxed != 0: relaxed GPU-scope stores and
+ *   loads).  out (device, 3 uint64) gets the elapsed %globaltimer
+ *   nanoseconds and the SM ids of the two CTAs; which SMs they land on
+ *   decides the round trip (on the same die or across dies), so callers
+ *   sweep `partner`.  flags is a device array of 64 uint32 that the probe
+ *   zeroes first.  Waits are bounded (1 s); on timeout out[0] = UINT64_MAX.
  */
 sfar_status sfar_probe_empty(sfar_stream_t s);
-sfar_status sfar_probe_pingpong(uint32_t *flags, int trips, int relaxed, uint64_t *ns_out, sfar_stream_t s);
+sfar_status sfar_probe_pingpong(uint32_t *flags, int trips, int relaxed, int partner, uint64_t *out,
+                                sfar_stream_t s);
 
 #ifdef __cplusplus
 }

@@ -67,7 +67,7 @@ def test_null_handle_calls(lib):
     assert lib.sfar_status_get(None, None) == sfar.SFAR_ERR_INVALID
     assert lib.sfar_set_launch_mode(None, 0) == sfar.SFAR_ERR_INVALID
     assert lib.sfar_max_bytes(None, 2) == 0
-    assert lib.sfar_probe_pingpong(None, 1, 0, None, None) == sfar.SFAR_ERR_INVALID
+    assert lib.sfar_probe_pingpong(None, 1, 0, 1, None, None) == sfar.SFAR_ERR_INVALID
     assert lib.sfar_test_set_geometry(None, 0, 0) == sfar.SFAR_ERR_INVALID
     lib.sfar_destroy(None)
 
