@@ -9,13 +9,17 @@
 // reduced chunk once into every rank's output, with no staging buffers.
 //
 // Owner CTA (j, k) takes a contiguous range of chunk j and streams it in
-// tiles through a ring of shared-memory stages.  Per tile, the lanes of warp
-// 0 issue one 1-D bulk copy each (lane q: rank q's input, global -> shared,
-// completion counted in bytes on the stage's mbarrier); all threads fold the
-// R tiles from shared memory in rank order, round once and write the tile
-// into one of three shared output buffers; then lane p of warp 0 issues the
-// bulk copy shared -> global into rank p's output.  A buffer is reused only
-// after the copies that read it have finished reading (wait_group.read).
+// tiles through a ring of shared-memory stages, with the work split by warp:
+//   * the producer warp: lane q issues the 1-D bulk copy of rank q's tile
+//     (global -> shared, completion counted in bytes on the stage's "full"
+//     mbarrier), after the stage's "empty" mbarrier says it was consumed;
+//   * eight consumer warps: fold the R tiles from shared memory in rank
+//     order, round once, write the tile into one of three output buffers
+//     (after its "free" mbarrier), then arrive on the stage's "empty" and the
+//     buffer's "full" mbarriers;
+//   * the store warp: lane p issues the bulk copy shared -> global into rank
+//     p's output, and frees a buffer once the copies reading it are done.
+// No CTA-wide barrier in the steady state; every mbarrier wait is bounded.
 // No multicast and no bulk reduction (its order of additions is not fixed).
 // Streaming copies carry an L2 evict-first hint: every byte is touched once.
 //
@@ -87,14 +91,33 @@ __device__ __forceinline__ void fence_proxy_async_global()
     asm volatile("fence.proxy.async.global;" ::: "memory");
 }
 
+__device__ __forceinline__ void mbar_arrive(uint32_t bar)
+{
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+// Bounded wait for phase `parity` of an mbarrier; false if it gave up.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const SfarCtl *ctl)
+{
+    SfarWaiter w;
+    while (!mbar_try_wait(bar, parity))
+        if (w.tick(ctl))
+            return false;
+    return true;
+}
+
+#define TMA_CONSUMER_WARPS 8
+#define TMA_PRODUCER_WARP 8
+#define TMA_STORE_WARP 9
+
 template <int DT, bool TEST>
 __global__ void __launch_bounds__(SFAR_TMA_THREADS, 1) k_tma(const __grid_constant__ SfarArgs a)
 {
     constexpr int ES = DT == 0 ? 2 : 4;
+    constexpr int NB = TMA_OUT_BUFS;
     const SfarEntry ent = sfar_entry(a);
     const int R = a.R, K = a.K;
     const int r = blockIdx.x / K, k = blockIdx.x - r * K;
-    const int tid = threadIdx.x, lane = tid & 31;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     SfarCall c;
     if (!sfar_prologue<TEST>(a, r, k, c, ent))
         return;
@@ -123,6 +146,7 @@ __global__ void __launch_bounds__(SFAR_TMA_THREADS, 1) k_tma(const __grid_consta
     __syncthreads();
     bool ok = s_ok != 0;
     sfar_mid_delay<TEST>(c);
+    sfar_stamp(c, TP_SENT);
 
     // this CTA's byte range [b0, b1) of chunk r
     const unsigned long long nbytes = a.n * ES;
@@ -140,103 +164,131 @@ __global__ void __launch_bounds__(SFAR_TMA_THREADS, 1) k_tma(const __grid_consta
 
     extern __shared__ __align__(128) uint8_t smem[];
     uint8_t *stage0 = smem;                                           // [NS][R][TB]
-    uint8_t *obuf = smem + (size_t)NS * R * TB;                       // [TMA_OUT_BUFS][TB]
-    uint64_t *bars = reinterpret_cast<uint64_t *>(obuf + (size_t)TMA_OUT_BUFS * TB);
+    uint8_t *obuf = smem + (size_t)NS * R * TB;                       // [NB][TB]
+    uint64_t *full = reinterpret_cast<uint64_t *>(obuf + (size_t)NB * TB);   // [NS]
+    uint64_t *empty = full + NS;                                      // [NS]
+    uint64_t *ofull = empty + NS;                                     // [NB]
+    uint64_t *ofree = ofull + NB;                                     // [NB]
+    __shared__ int s_fail;
 
     if (ok && ntiles > 0) {
-        const uint64_t pol = policy_evict_first();
         if (tid == 0) {
-            for (int s = 0; s < NS; ++s)
-                mbar_init(smem_u32(bars + s), 1);
+            for (int s = 0; s < NS; ++s) {
+                mbar_init(smem_u32(full + s), 1);
+                mbar_init(smem_u32(empty + s), TMA_CONSUMER_WARPS);
+            }
+            for (int b = 0; b < NB; ++b) {
+                mbar_init(smem_u32(ofull + b), TMA_CONSUMER_WARPS);
+                mbar_init(smem_u32(ofree + b), 1);
+            }
+            s_fail = 0;
             asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
             fence_proxy_async_smem();
         }
         __syncthreads();
-        // warp 0 only: lane 0 arms the stage's byte count, lane q copies rank q's tile
-        auto issue = [&](unsigned long long t) {
-            const int s = (int)(t % NS);
+        const auto tile_len = [&](unsigned long long t) {
             const unsigned long long off = t * TB;
-            const uint32_t tb = (uint32_t)((len16 - off) < TB ? (len16 - off) : TB);
-            const uint32_t bar = smem_u32(bars + s);
-            if (lane == 0)
-                mbar_expect_tx(bar, tb * (uint32_t)R);
-            __syncwarp();
-            for (int q = lane; q < R; q += 32)
-                bulk_g2s(smem_u32(stage0 + ((size_t)s * R + q) * TB), (const uint8_t *)a.in[q] + b0 + off, tb, bar,
-                         pol);
+            return (uint32_t)((len16 - off) < TB ? (len16 - off) : TB);
         };
-        if (tid < 32)
-            for (unsigned long long t = 0; t < ntiles && t < (unsigned long long)NS; ++t)
-                issue(t);
-
-        for (unsigned long long t = 0; t < ntiles; ++t) {
-            const int s = (int)(t % NS);
-            const uint32_t phase = (uint32_t)((t / NS) & 1ull);
-            const unsigned long long off = t * TB;
-            const uint32_t tb = (uint32_t)((len16 - off) < TB ? (len16 - off) : TB);
-            int tok = 1;
-            {
-                SfarWaiter w;
-                const uint32_t bar = smem_u32(bars + s);
-                while (!mbar_try_wait(bar, phase)) {
-                    if (w.tick(a.ctl)) {
+        if (warp == TMA_PRODUCER_WARP) {
+            const uint64_t pol = policy_evict_first();
+            for (unsigned long long t = 0; t < ntiles; ++t) {
+                const int s = (int)(t % NS);
+                int wok = 1;
+                if (t >= (unsigned long long)NS)
+                    wok = mbar_wait(smem_u32(empty + s), (uint32_t)(((t / NS) - 1) & 1ull), a.ctl);
+                if (!__all_sync(SFAR_FULL, wok)) {
+                    if (lane == 0) {
                         sfar_record_fault(a.ctl, r, k, -1, e, SFAR_WAIT_COPY);
-                        tok = 0;
-                        break;
+                        s_fail = 1;
                     }
+                    break;
                 }
+                const uint32_t tb = tile_len(t), bar = smem_u32(full + s);
+                if (lane == 0)
+                    mbar_expect_tx(bar, tb * (uint32_t)R);
+                __syncwarp();
+                for (int q = lane; q < R; q += 32)
+                    bulk_g2s(smem_u32(stage0 + ((size_t)s * R + q) * TB), (const uint8_t *)a.in[q] + b0 + t * TB, tb,
+                             bar, pol);
             }
-            const uint8_t *st = stage0 + (size_t)s * R * TB;
-            uint8_t *ob = obuf + (size_t)(t % TMA_OUT_BUFS) * TB;
-            if (tok) {
-                for (uint32_t u = tid * 16u; u < tb; u += SFAR_TMA_THREADS * 16u) {
+        } else if (warp == TMA_STORE_WARP) {
+            const uint64_t pol = policy_evict_first();
+            for (unsigned long long t = 0; t < ntiles; ++t) {
+                const int b = (int)(t % NB);
+                const int wok = mbar_wait(smem_u32(ofull + b), (uint32_t)((t / NB) & 1ull), a.ctl);
+                if (!__all_sync(SFAR_FULL, wok)) {
+                    if (lane == 0) {
+                        sfar_record_fault(a.ctl, r, k, -1, e, SFAR_WAIT_COPY);
+                        s_fail = 1;
+                    }
+                    break;
+                }
+                const uint32_t tb = tile_len(t);
+                for (int p = lane; p < R; p += 32)
+                    bulk_s2g((uint8_t *)a.out[p] + b0 + t * TB, smem_u32(obuf + (size_t)b * TB), tb, pol);
+                bulk_commit();
+                // the copies of tile t - 1 have read their buffer: free it
+                bulk_wait_read1();
+                __syncwarp();
+                if (t >= 1 && lane == 0)
+                    mbar_arrive(smem_u32(ofree + (int)((t - 1) % NB)));
+            }
+            bulk_wait0();               // stores complete before completion is signalled
+            fence_proxy_async_global();
+        } else {
+            const int ct = tid;         // consumer threads 0 .. 32 * TMA_CONSUMER_WARPS - 1
+            for (unsigned long long t = 0; t < ntiles; ++t) {
+                const int s = (int)(t % NS), b = (int)(t % NB);
+                int wok = mbar_wait(smem_u32(full + s), (uint32_t)((t / NS) & 1ull), a.ctl);
+                if (wok && t >= (unsigned long long)NB)
+                    wok = mbar_wait(smem_u32(ofree + b), (uint32_t)(((t / NB) - 1) & 1ull), a.ctl);
+                if (!__all_sync(SFAR_FULL, wok)) {
+                    if (lane == 0) {
+                        sfar_record_fault(a.ctl, r, k, -1, e, SFAR_WAIT_COPY);
+                        s_fail = 1;
+                    }
+                    break;
+                }
+                const uint32_t tb = tile_len(t);
+                const uint8_t *st = stage0 + (size_t)s * R * TB;
+                uint8_t *ob = obuf + (size_t)b * TB;
+                for (uint32_t u = ct * 16u; u < tb; u += TMA_CONSUMER_WARPS * 32 * 16u) {
                     SfarAcc<DT> acc;
                     acc.set(*reinterpret_cast<const uint4 *>(st + u));
                     for (int q = 1; q < R; ++q)
                         acc.add(*reinterpret_cast<const uint4 *>(st + (size_t)q * TB + u));
                     *reinterpret_cast<uint4 *>(ob + u) = acc.get();
                 }
-                fence_proxy_async_smem();
-            }
-            // the stores of tile t - 1 may still be reading; those of t - 2
-            // (whose buffer tile t + 1 reuses) must be done
-            if (tid < 32)
-                bulk_wait_read1();
-            if (!__syncthreads_and(tok)) {
-                ok = false;
-                break;
-            }
-            if (tid < 32) {
-                for (int p = lane; p < R; p += 32)
-                    bulk_s2g((uint8_t *)a.out[p] + b0 + off, smem_u32(ob), tb, pol);
-                bulk_commit();
-                if (t + NS < ntiles)
-                    issue(t + NS);      // every thread has finished reading stage s
+                fence_proxy_async_smem();   // our writes to the buffer, before the bulk stores read it
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(smem_u32(empty + s));
+                    mbar_arrive(smem_u32(ofull + b));
+                }
             }
         }
-        if (tid < 32) {
-            bulk_wait0();               // stores complete before completion is signalled
-            fence_proxy_async_global();
-        }
+        __syncthreads();
+        ok = ok && s_fail == 0;
     }
     // a ragged end shorter than 16 bytes: element by element
     if (ok && tid == 0 && b1 == nbytes && (b1 - b0) > len16) {
-        for (unsigned long long b = b0 + len16; b < b1; b += ES) {
+        for (unsigned long long bb = b0 + len16; bb < b1; bb += ES) {
             float acc = 0.f;
             for (int q = 0; q < R; ++q) {
                 float x;
                 if (ES == 2)
-                    x = __uint_as_float((uint32_t)(*(const uint16_t *)((const uint8_t *)a.in[q] + b)) << 16);
+                    x = __uint_as_float((uint32_t)(*(const uint16_t *)((const uint8_t *)a.in[q] + bb)) << 16);
                 else
-                    x = *(const float *)((const uint8_t *)a.in[q] + b);
+                    x = *(const float *)((const uint8_t *)a.in[q] + bb);
                 acc = q == 0 ? x : __fadd_rn(acc, x);
             }
             for (int p = 0; p < R; ++p) {
                 if (ES == 2) {
                     __nv_bfloat16 h = __float2bfloat16_rn(acc);
-                    *(uint16_t *)((uint8_t *)a.out[p] + b) = *reinterpret_cast<uint16_t *>(&h);
+                    *(uint16_t *)((uint8_t *)a.out[p] + bb) = *reinterpret_cast<uint16_t *>(&h);
                 } else {
-                    *(float *)((uint8_t *)a.out[p] + b) = acc;
+                    *(float *)((uint8_t *)a.out[p] + bb) = acc;
                 }
             }
         }

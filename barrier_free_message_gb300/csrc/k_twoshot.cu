@@ -131,30 +131,41 @@ __global__ void __launch_bounds__(SFAR_THREADS) k_twoshot(const __grid_constant_
             }
     }
 
-    // 3. all-gather receive
+    // 3. all-gather receive: lane (g, m) polls line g of owner peer m (and
+    // m + 8), so all owners are waited for at once; then every owner's line
+    // is read in one round and unpacked into this rank's output
     const uint8_t *ag_mine = ag + (size_t)(r * 2 + c.par) * R * slot;
-    for (int i = 0; i < R - 1 && ok; ++i) {
-        const int j = peer_of(r, i);
-        for (unsigned long long it = it0; it < nitc; it += its) {
-            const uint8_t *line = ag_mine + (size_t)j * slot + (it * 4ull + g) * 128ull;
-            int lok = 1;
-            if (m == 0) {
-                SfarWaiter w(true);
-                while (ld_relaxed_u32((const uint32_t *)line) != e) {
-                    if (w.tick(a.ctl)) {
-                        sfar_record_fault(a.ctl, r, k, j, e, SFAR_WAIT_AG);
-                        lok = 0;
-                        break;
-                    }
+    for (unsigned long long it = it0; it < nitc && ok; it += its) {
+        const size_t loff = (it * 4ull + g) * 128ull;
+        int lok = 1;
+        for (int i = m; i < R - 1 && lok; i += 8) {
+            const int j = peer_of(r, i);
+            const uint32_t *f = (const uint32_t *)(ag_mine + (size_t)j * slot + loff);
+            SfarWaiter w(true);
+            while (ld_relaxed_u32(f) != e) {
+                if (w.tick(a.ctl)) {
+                    sfar_record_fault(a.ctl, r, k, j, e, SFAR_WAIT_AG);
+                    lok = 0;
+                    break;
                 }
             }
-            ok = __all_sync(SFAR_FULL, lok) != 0;
-            if (!ok)
-                break;
-            fence_acq_rel_gpu();
-            const uint4 o = ll128_unpack(ld_relaxed_v4(line + 16 * m), lane);
-            if (lane < 31)
-                store_vec<ES>(a.out[r], j * cvec + it * 31ull + lane, nbytes, o);
+        }
+        ok = __all_sync(SFAR_FULL, lok) != 0;
+        if (!ok)
+            break;
+        fence_acq_rel_gpu();
+        uint4 y[RB];
+#pragma unroll
+        for (int q = 0; q < RB; ++q)
+            if (q < R && q != r)
+                y[q] = ld_relaxed_v4(ag_mine + (size_t)q * slot + loff + 16 * m);
+#pragma unroll
+        for (int q = 0; q < RB; ++q) {
+            if (q < R && q != r) {
+                const uint4 o = ll128_unpack(y[q], lane);
+                if (lane < 31)
+                    store_vec<ES>(a.out[r], q * cvec + it * 31ull + lane, nbytes, o);
+            }
         }
     }
     sfar_stamp(c, TP_RECEIVED);

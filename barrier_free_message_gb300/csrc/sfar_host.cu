@@ -304,7 +304,7 @@ sfar_t *sfar_create(int R, size_t max_bytes, sfar_dtype dt)
         if (ns > 8) ns = 8;
         h->tma_tb = (int)tb;
         h->tma_ns = (int)ns;
-        h->tma_smem = ns * R * tb + outb + ns * 8;
+        h->tma_smem = ns * R * tb + outb + (2 * ns + 2 * 3) * 8;   // + full/empty and buffer mbarriers
     }
 
     SfarCtl init;

@@ -10,7 +10,7 @@
 #define SFAR_RECV_MAX_BYTES (2ull << 20)    // per-rank limit of the receive-buffer protocols
 #define SFAR_LL128_PAYLOAD 124              // bytes of payload per 128-byte LL128 line
 #define SFAR_ITER_BYTES (4 * SFAR_LL128_PAYLOAD)   // payload of the 4 lines one warp moves at once
-#define SFAR_TMA_THREADS 256
+#define SFAR_TMA_THREADS 320                // TMA path: 8 consumer warps, a producer and a store warp
 #define SFAR_NTHREAD_OPTS 3                 // receive-buffer kernels: 64, 128 or 256 threads
 
 // Device status block of one handle.  The first 32 bytes are the sticky

@@ -143,7 +143,7 @@ def test_query_launch_geometry():
     try:
         for proto in ALL_PROTOS:
             k, t = h.launch(8192, proto)
-            assert 1 <= k <= 128 and t in (64, 128, 256)
+            assert 1 <= k <= 128 and t in (64, 128, 256, 320)
             assert 8 * k <= torch.cuda.get_device_properties(0).multi_processor_count * 8
         assert sfar.sfar_test_set_geometry(h.h, 3, 128) == sfar.SFAR_OK
         assert h.launch(8192, "ll") == (3, 128)
