@@ -345,6 +345,88 @@ def oracle_cpu_time(x_host, budget_s=10.0, calls_per_step=None):
     return dt / done * 1e6, done, dt
 
 
+# ----------------------------------------------------------------- suites
+ALL = PROTOS + ["twoshot", "twoshot_tma"]
+
+
+def _time_chain(h, x_dev, out_dev, proto, reps=40, warm=3):
+    """Capture one graph of all calls in x_dev and time `reps` replays (µs per call)."""
+    calls, R, n = x_dev.shape
+    h.allreduce([x_dev[0, r] for r in range(R)], [out_dev[0, r] for r in range(R)], proto)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for c in range(calls):
+            code = sfar.sfar_allreduce(h.h, [x_dev[c, r].data_ptr() for r in range(R)],
+                                       [out_dev[c, r].data_ptr() for r in range(R)], n, proto)
+            if code != sfar.SFAR_OK:
+                raise sfar.SfarError(code, "capture")
+    for _ in range(warm):
+        g.replay()
+    torch.cuda.synchronize()
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s.record()
+    for _ in range(reps):
+        g.replay()
+    e.record()
+    torch.cuda.synchronize()
+    check_status(h, proto)
+    return s.elapsed_time(e) * 1000.0 / (reps * calls)
+
+
+def run_suite(args):
+    """Sweeps printed as JSON lines: the latency curve of every protocol over
+    message sizes (R = 4, 8; both launch modes), the bandwidth of the TMA path
+    (R = 2..16, bf16 and fp32, 4-256 MB per rank), and the cost of the
+    barriers against the rank count (BASELINE vs DB vs LL vs sentinel,
+    16 KB per rank, R = 2..16)."""
+    _build.build()
+    l2 = torch.cuda.get_device_properties(torch.cuda.current_device()).L2_cache_size
+    if "latency" in args.suite:
+        for R in (4, 8):
+            h = sfar.Sfar(R, 1 << 20, "bf16")
+            for b in inputs.SWEEP_BYTES:
+                n, calls = b // 2, 32
+                x = torch.stack([inputs.draw(2, c, R, n, "uniform", 1.0, "bf16") for c in range(calls)])
+                xd = x.cuda()
+                od = torch.empty_like(xd)
+                for mode in ("serial", "overlap"):
+                    h.set_mode(mode)
+                    for proto in ALL:
+                        us = _time_chain(h, xd, od, proto)
+                        k, t = h.launch(n, proto)
+                        print(json.dumps({"suite": "latency", "R": R, "bytes": b, "mode": mode, "proto": proto,
+                                          "us": round(us, 3), "ctas_per_rank": k, "threads": t,
+                                          "l2_resident": 2 * calls * R * b < l2,
+                                          "bit_exact_sample": spot_check(od, x, [0, calls - 1])}), flush=True)
+                del xd, od
+            h.close()
+    if "bandwidth" in args.suite:
+        peaks, _ = measured_peaks()
+        for dtype in ("bf16", "fp32"):
+            for R in (2, 4, 8, 16):
+                for mb in (4, 16, 64, 256):
+                    d = large_message_roofline(float(peaks["hbm_gbs"]), R=R, mb=mb, dtype=dtype)
+                    d.update({"suite": "bandwidth", "R": R, "mb": mb, "dtype": dtype})
+                    print(json.dumps(d), flush=True)
+                    torch.cuda.empty_cache()
+    if "barriers" in args.suite:
+        n, calls = 8192, 160
+        for R in (2, 3, 4, 6, 8, 12, 16):
+            x = torch.stack([inputs.draw(1, c, R, n, "normal", 1.0, "bf16") for c in range(calls)])
+            xd = x.cuda()
+            od = torch.empty_like(xd)
+            h = sfar.Sfar(R, 2 * n, "bf16")
+            row = {"suite": "barriers", "R": R, "bytes": 2 * n}
+            for proto in ("baseline", "db", "ll", "sentinel"):
+                row[proto] = round(_time_chain(h, xd, od, proto), 3)
+                row[proto + "_exact"] = spot_check(od, x, [0, calls - 1])
+            row["two_barriers_minus_ll"] = round(row["baseline"] - row["ll"], 3)
+            row["bottom_barrier"] = round(row["baseline"] - row["db"], 3)
+            print(json.dumps(row), flush=True)
+            h.close()
+
+
 # ----------------------------------------------------------------- arms
 def run_reference(args, world, rank):
     if rank != 0:
@@ -513,10 +595,13 @@ def main():
     ap.add_argument("--large-r", type=int, default=8)
     ap.add_argument("--large-mb", type=int, default=64)
     ap.add_argument("--large-dtype", choices=["bf16", "fp32"], default="bf16")
+    ap.add_argument("--suite", default="", help="comma list of latency,bandwidth,barriers: sweeps as JSON lines")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
     world, rank, _ = dist_setup(args.gpus)
-    if args.impl == "reference":
+    if args.suite:
+        run_suite(args)
+    elif args.impl == "reference":
         run_reference(args, world, rank)
     else:
         run_ours(args, world, rank)
