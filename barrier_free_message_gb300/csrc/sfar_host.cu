@@ -46,7 +46,8 @@ struct sfar {
     SfarCtl *ctl = nullptr;
     uint8_t *r_raw = nullptr, *r_ll = nullptr, *r_ll128 = nullptr, *r_sent = nullptr;
     uint8_t *r_rs = nullptr, *r_ag = nullptr;
-    size_t s_raw = 0, s_ll = 0, s_ll128 = 0, s_2s = 0, sent_bytes = 0;
+    uint8_t *r_acc = nullptr, *r_agx = nullptr;   // atomic path: accumulator and all-gather lines
+    size_t s_raw = 0, s_ll = 0, s_ll128 = 0, s_2s = 0, s_at = 0, sent_bytes = 0;
     int mode = SFAR_LAUNCH_SERIAL;
     int ctas_override = 0, threads_override = 0;
     long long last_key = -1;            // overlap mode: geometry of the previous call
@@ -74,6 +75,7 @@ static const void *kernel_for(const sfar *h, int p, int test)
     case SFAR_SENTINEL: return sfar_kernel_sentinel(h->dt, wide, test);
     case SFAR_TWOSHOT: return sfar_kernel_twoshot(h->dt, wide, test);
     case SFAR_TWOSHOT_TMA: return sfar_kernel_tma(h->dt, test);
+    case SFAR_LL128_ATOMIC: return sfar_kernel_atomic(h->dt, wide, test);
     default: return nullptr;
     }
 }
@@ -92,7 +94,8 @@ static int thread_index(int threads)
 }
 
 // Work units of a call: 16-byte vectors (one-shot vector protocols), 4-line
-// groups per warp (LL128, two-shot), or bytes of a chunk (TMA path).
+// groups per warp (LL128, two-shot), lines of a chunk per warp (atomic path),
+// or bytes of a chunk (TMA path).
 static size_t work_units(const sfar *h, int p, size_t n, size_t *chunk)
 {
     const size_t nvec = ceil_div(n * (size_t)h->es, 16);
@@ -108,6 +111,9 @@ static size_t work_units(const sfar *h, int p, size_t n, size_t *chunk)
     case SFAR_TWOSHOT_TMA:
         *chunk = align_up(ceil_div(n, (size_t)h->R), 16 / (size_t)h->es);
         return *chunk * (size_t)h->es;
+    case SFAR_LL128_ATOMIC:
+        *chunk = align_up(ceil_div(n, (size_t)h->R), 31);
+        return *chunk / 31;
     default:
         return nvec;
     }
@@ -122,7 +128,7 @@ static int geometry(const sfar *h, int p, size_t n, size_t *chunk, size_t *sub, 
 {
     const size_t units = work_units(h, p, n, chunk);
     *sub = 0;
-    const bool warp_units = p == SFAR_LL128 || p == SFAR_TWOSHOT;
+    const bool warp_units = p == SFAR_LL128 || p == SFAR_TWOSHOT || p == SFAR_LL128_ATOMIC;
     int ti = SFAR_NTHREAD_OPTS - 1;
     size_t K = 1;
     if (p == SFAR_TWOSHOT_TMA) {
@@ -246,6 +252,8 @@ sfar_t *sfar_create(int R, size_t max_bytes, sfar_dtype dt)
         const size_t epi = SFAR_ITER_BYTES / (size_t)h->es;
         const size_t c = align_up(ceil_div(nmax, (size_t)R), epi);
         h->s_2s = align_up(c / epi * 512, 256);
+        // atomic path: 128-byte lines of 31 elements per (owner, parity)
+        h->s_at = align_up(ceil_div(ceil_div(nmax, (size_t)R), 31) * 128, 256);
     }
     const size_t RR2 = (size_t)R * 2 * R;
     size_t off = 0;
@@ -268,6 +276,8 @@ sfar_t *sfar_create(int R, size_t max_bytes, sfar_dtype dt)
     const size_t o_rs = carve(RR2 * h->s_2s);
     const size_t o_ag = carve(RR2 * h->s_2s);
     const size_t o_sent = carve(RR2 * h->s_raw);
+    const size_t o_acc = carve((size_t)R * 2 * h->s_at);
+    const size_t o_agx = carve(RR2 * h->s_at);
     h->sent_bytes = RR2 * h->s_raw;
     h->ws_bytes = off;
 
@@ -290,6 +300,8 @@ sfar_t *sfar_create(int R, size_t max_bytes, sfar_dtype dt)
     h->r_rs = h->ws + o_rs;
     h->r_ag = h->ws + o_ag;
     h->r_sent = h->ws + o_sent;
+    h->r_acc = h->ws + o_acc;
+    h->r_agx = h->ws + o_agx;
 
     // TMA path: a stage holds R tiles (about 48 KB in all); as many stages as
     // fit in 220 KB of shared memory next to 3 output buffers, 2 to 8
@@ -497,6 +509,11 @@ sfar_status sfar_allreduce(sfar_t *h, const void *const in[], void *const out[],
         a.region = h->r_rs;
         a.region2 = h->r_ag;
         a.slot = h->s_2s;
+        break;
+    case SFAR_LL128_ATOMIC:
+        a.region = h->r_acc;
+        a.region2 = h->r_agx;
+        a.slot = h->s_at;
         break;
     case SFAR_TWOSHOT_TMA:
         a.fa = h->fc;

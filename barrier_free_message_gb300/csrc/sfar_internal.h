@@ -41,8 +41,8 @@ struct SfarArgs {
     unsigned long long slot;      // bytes per (receiver, parity, sender) slot of `region`
     unsigned long long chunk;     // two-shot: elements per owner chunk
     unsigned long long sub;       // TMA path: elements per CTA range within a chunk
-    uint8_t *region;              // receive region of the protocol
-    uint8_t *region2;             // two-shot: all-gather region
+    uint8_t *region;              // receive region of the protocol (atomic path: accumulator lines)
+    uint8_t *region2;             // two-shot and atomic path: all-gather region
     unsigned long long *epoch;    // [R] call counters: + SFAR_KMAX per call (see the prologue)
     uint32_t *done;               // [R][SFAR_KMAX] last finished epoch (overlap mode)
     uint32_t *fa;                 // flags [R][R][SFAR_KMAX]: ready / top barrier / arrival
@@ -61,6 +61,7 @@ const void *sfar_kernel_sentinel(int dt, int wide, int test);
 const void *sfar_kernel_db(int dt, int wide, int test, int baseline);
 const void *sfar_kernel_twoshot(int dt, int wide, int test);
 const void *sfar_kernel_tma(int dt, int test);
+const void *sfar_kernel_atomic(int dt, int wide, int test);
 const void *sfar_kernel_set_knob();
 const void *sfar_kernel_empty();
 const void *sfar_kernel_pingpong();

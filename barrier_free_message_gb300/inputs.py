@@ -7,8 +7,10 @@ inputs from it.
 Recipe (the same for every workload): call ``c`` of a workload with seed ``s``
 draws its ``[R, n]`` block from its own CPU generator,
 ``torch.Generator().manual_seed(s * 2**32 + c)``; ``uniform`` is
-``rand * 2 - 1`` (uniform on [-1, 1)), ``normal`` is ``randn * sigma``; the
-binary32 draw is then rounded to nearest-even into bf16, or kept as fp32.
+``rand * 2 - 1`` (uniform on [-1, 1)), ``normal`` is ``randn * sigma``,
+``int`` is a uniform integer in [-sigma, sigma] (sigma <= 256 keeps every
+value exact in bf16); the binary32 draw is then rounded to nearest-even into
+bf16, or kept as fp32.
 Because every call has its own generator, any single call can be redrawn on
 its own (the sampled parity checks at full size rely on this).  Values are
 finite, so they never equal the sentinel bit patterns (all ones).
@@ -61,6 +63,9 @@ def draw(seed: int, call: int, R: int, n: int, dist: str = "uniform", sigma: flo
         x = torch.rand(R, n, generator=g) * 2.0 - 1.0
     elif dist == "normal":
         x = torch.randn(R, n, generator=g) * sigma
+    elif dist == "int":
+        k = int(sigma)
+        x = torch.randint(-k, k + 1, (R, n), generator=g).to(torch.float32)
     else:
         raise ValueError(f"unknown distribution {dist!r}")
     return x.to(torch.bfloat16) if dtype == "bf16" else x.to(torch.float32)

@@ -13,16 +13,20 @@ import os
 from . import _build
 
 SFAR_BF16, SFAR_FP32 = 0, 1
-SFAR_BASELINE, SFAR_DB, SFAR_LL, SFAR_LL128, SFAR_SENTINEL, SFAR_TWOSHOT, SFAR_TWOSHOT_TMA = range(7)
+SFAR_BASELINE, SFAR_DB, SFAR_LL, SFAR_LL128, SFAR_SENTINEL, SFAR_TWOSHOT, SFAR_TWOSHOT_TMA, \
+    SFAR_LL128_ATOMIC = range(8)
 PROTOS = {"baseline": SFAR_BASELINE, "db": SFAR_DB, "ll": SFAR_LL, "ll128": SFAR_LL128,
-          "sentinel": SFAR_SENTINEL, "twoshot": SFAR_TWOSHOT, "twoshot_tma": SFAR_TWOSHOT_TMA}
+          "sentinel": SFAR_SENTINEL, "twoshot": SFAR_TWOSHOT, "twoshot_tma": SFAR_TWOSHOT_TMA,
+          "ll128_atomic": SFAR_LL128_ATOMIC}
+# every protocol but ll128_atomic returns the rank-order fold bit for bit
+EXACT_PROTOS = [p for p in PROTOS if p != "ll128_atomic"]
 DTYPES = {"bf16": SFAR_BF16, "fp32": SFAR_FP32}
 SFAR_OK, SFAR_ERR_INVALID, SFAR_ERR_CUDA, SFAR_ERR_OOM, SFAR_ERR_TIMEOUT, SFAR_ERR_UNSUPPORTED, \
     SFAR_ERR_POISONED = range(7)
 SFAR_LAUNCH_SERIAL, SFAR_LAUNCH_OVERLAP, SFAR_LAUNCH_PLAIN = 0, 1, 2
 MODES = {"serial": SFAR_LAUNCH_SERIAL, "overlap": SFAR_LAUNCH_OVERLAP, "plain": SFAR_LAUNCH_PLAIN}
 WAIT_NAMES = {1: "done", 2: "ll", 3: "sentinel", 4: "ready", 5: "bottom", 6: "ll128", 7: "rs", 8: "ag",
-              9: "arrive", 10: "complete", 11: "copy"}
+              9: "arrive", 10: "complete", 11: "copy", 12: "counter"}
 
 
 class SfarFault(ctypes.Structure):

@@ -284,6 +284,19 @@ def spot_check(out_dev, x_host, calls):
     return True
 
 
+def admissible_check(out_dev, x_host, calls):
+    """The order-free (atomic) protocol: every rank equal and every element of
+    a few calls inside the oracle's admissible interval."""
+    from oracle import atomic
+    for c in calls:
+        got = inputs.to_bits(out_dev[c].cpu())
+        if not all(np.array_equal(got[r], got[0]) for r in range(1, got.shape[0])):
+            return False
+        if not atomic.check(inputs.to_bits(x_host[c]), got[0]).all():
+            return False
+    return True
+
+
 def large_message_roofline(peak_gbs, R=8, mb=64, dtype="bf16", iters=10):
     """HBM roofline of the two-shot TMA path: 2*R*S bytes per call."""
     tdt = torch.bfloat16 if dtype == "bf16" else torch.float32
@@ -377,9 +390,10 @@ def _time_chain(h, x_dev, out_dev, proto, reps=40, warm=3):
 def run_suite(args):
     """Sweeps printed as JSON lines: the latency curve of every protocol over
     message sizes (R = 4, 8; both launch modes), the bandwidth of the TMA path
-    (R = 2..16, bf16 and fp32, 4-256 MB per rank), and the cost of the
-    barriers against the rank count (BASELINE vs DB vs LL vs sentinel,
-    16 KB per rank, R = 2..16)."""
+    (R = 2..16, bf16 and fp32, 4-256 MB per rank), the cost of the barriers
+    against the rank count (BASELINE vs DB vs LL vs sentinel, 16 KB per rank,
+    R = 2..16), and the atomic-accumulation two-shot against the two-shot,
+    LL128 and LL protocols (R = 4, 8, 16 over message sizes)."""
     _build.build()
     l2 = torch.cuda.get_device_properties(torch.cuda.current_device()).L2_cache_size
     if "latency" in args.suite:
@@ -424,6 +438,25 @@ def run_suite(args):
             row["two_barriers_minus_ll"] = round(row["baseline"] - row["ll"], 3)
             row["bottom_barrier"] = round(row["baseline"] - row["db"], 3)
             print(json.dumps(row), flush=True)
+            h.close()
+    if "atomic" in args.suite:
+        # the atomic-accumulation two-shot against the flag-line protocols
+        for R in (4, 8, 16):
+            h = sfar.Sfar(R, 1 << 20, "bf16")
+            for b in inputs.SWEEP_BYTES:
+                n, calls = b // 2, 32
+                x = torch.stack([inputs.draw(5, c, R, n, "normal", 1.0, "bf16") for c in range(calls)])
+                xd = x.cuda()
+                od = torch.empty_like(xd)
+                row = {"suite": "atomic", "R": R, "bytes": b}
+                for proto in ("ll128_atomic", "twoshot", "ll128", "ll"):
+                    row[proto] = round(_time_chain(h, xd, od, proto), 3)
+                    row[proto + "_ok"] = (admissible_check(od, x, [0, calls - 1]) if proto == "ll128_atomic"
+                                          else spot_check(od, x, [0, calls - 1]))
+                k, t = h.launch(n, "ll128_atomic")
+                row["atomic_ctas_per_rank"], row["atomic_threads"] = k, t
+                print(json.dumps(row), flush=True)
+                del xd, od
             h.close()
 
 
@@ -595,7 +628,7 @@ def main():
     ap.add_argument("--large-r", type=int, default=8)
     ap.add_argument("--large-mb", type=int, default=64)
     ap.add_argument("--large-dtype", choices=["bf16", "fp32"], default="bf16")
-    ap.add_argument("--suite", default="", help="comma list of latency,bandwidth,barriers: sweeps as JSON lines")
+    ap.add_argument("--suite", default="", help="comma list of latency,bandwidth,barriers,atomic: sweeps as JSON lines")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
     world, rank, _ = dist_setup(args.gpus)

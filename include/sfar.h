@@ -11,7 +11,8 @@
  * The sum is a left fold in rank order 0..R-1 with binary32 accumulation
  * (round to nearest even after every add) and one rounding to the output
  * type, so the result is unique bit for bit and identical on every rank,
- * whatever the protocol.
+ * whatever the protocol -- except SFAR_LL128_ATOMIC, whose binary32
+ * accumulation happens in the order of the hardware atomics (see there).
  *
  * Simulated ranks: rank r is a group of CTAs of one kernel with its own
  * receive buffers in HBM; ranks exchange data only by stores into each
@@ -59,11 +60,21 @@ typedef enum {
     SFAR_SENTINEL = 4,    /* one-shot, receive buffers prefilled with a NaN pattern   */
     SFAR_TWOSHOT = 5,     /* reduce-scatter + all-gather over LL128 lines, double
                              buffered (medium messages)                               */
-    SFAR_TWOSHOT_TMA = 6  /* reduce-scatter + all-gather straight from the inputs to
+    SFAR_TWOSHOT_TMA = 6, /* reduce-scatter + all-gather straight from the inputs to
                              the outputs with TMA bulk copies (large messages)        */
+    SFAR_LL128_ATOMIC = 7 /* reduce-scatter by hardware atomic adds into 128-byte
+                             lines whose first word counts the arrivals, then an
+                             all-gather over flagged lines (page 1, "Four
+                             barrier-free mechanisms", part 4).  NOT bit-exact: the
+                             binary32 accumulation runs in the atomics' order, and
+                             each element lies within 2 (R-1) 2^-24 sum|x| +
+                             2 R 2^-126 of the exact sum before its one rounding to
+                             the output type (exact when every partial sum is
+                             representable, e.g. small integers).  Identical on
+                             every rank.                                               */
 } sfar_proto;
 
-#define SFAR_NUM_PROTOS 7
+#define SFAR_NUM_PROTOS 8
 
 typedef int sfar_status;
 #define SFAR_OK 0
@@ -87,6 +98,7 @@ typedef int sfar_status;
 #define SFAR_WAIT_ARRIVE 9    /* TMA path: peer arrival (top barrier)                  */
 #define SFAR_WAIT_COMPLETE 10 /* TMA path: owner completion flags                      */
 #define SFAR_WAIT_COPY 11     /* TMA path: bulk copy completion                        */
+#define SFAR_WAIT_COUNTER 12  /* atomic path: a line's arrival counter stayed below R  */
 
 typedef struct {
     sfar_status code; /* SFAR_OK or SFAR_ERR_TIMEOUT                          */

@@ -39,6 +39,8 @@ def _lib(mutant: int = 0):
         lib.sfar_oracle_widen_bf16.argtypes = [ctypes.c_uint16]
         lib.sfar_oracle_widen_bf16.restype = ctypes.c_float
         lib.sfar_oracle_mutant.restype = ctypes.c_int
+        lib.sfar_oracle_narrow_bf16_n.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t]
+        lib.sfar_oracle_narrow_bf16_n.restype = None
         _libs[mutant] = lib
     return _libs[mutant]
 
@@ -89,3 +91,11 @@ def narrow_bf16(f: float, mutant: int = 0) -> int:
 
 def widen_bf16(b: int, mutant: int = 0) -> float:
     return float(_lib(mutant).sfar_oracle_widen_bf16(b))
+
+
+def narrow_bf16_array(f: np.ndarray, mutant: int = 0) -> np.ndarray:
+    """binary32 array -> bf16 bits (uint16), element by element with :func:`narrow_bf16`."""
+    f = np.ascontiguousarray(f, dtype=np.float32)
+    out = np.empty(f.shape, dtype=np.uint16)
+    _lib(mutant).sfar_oracle_narrow_bf16_n(f.ctypes.data, out.ctypes.data, f.size)
+    return out

@@ -242,5 +242,12 @@ int sfar_oracle_allreduce_mt(int R, size_t n, int dtype, const void *const *in,
 
 /* The two conversions on their own, so that tests can pin them directly. */
 uint16_t sfar_oracle_narrow_bf16(float f) { return narrow_bf16(f); }
+
+/* The same conversion over an array: out[i] = bf16 bits of in[i], i < n. */
+void sfar_oracle_narrow_bf16_n(const float *in, uint16_t *out, size_t n)
+{
+    for (size_t i = 0; i < n; ++i)
+        out[i] = narrow_bf16(in[i]);
+}
 float sfar_oracle_widen_bf16(uint16_t b) { return widen_bf16(b); }
 int sfar_oracle_mutant(void) { return ORACLE_MUTANT; }
