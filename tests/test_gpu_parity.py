@@ -114,7 +114,7 @@ def test_argument_checks():
         assert call(ip, [ip[0]] + op[1:], 1024) == sfar.SFAR_ERR_INVALID              # output overlaps input
         assert call(ip, [op[1]] + op[1:], 1024) == sfar.SFAR_ERR_INVALID              # two outputs alias
         assert call(ip, op, (1 << 16) // 2 + 1) == sfar.SFAR_ERR_INVALID              # over max_bytes
-        assert call(ip, op, 1024, 7) == sfar.SFAR_ERR_INVALID                         # unknown protocol
+        assert call(ip, op, 1024, len(sfar.PROTOS)) == sfar.SFAR_ERR_INVALID          # unknown protocol
         assert call([0] + ip[1:], op, 1024) == sfar.SFAR_ERR_INVALID                  # null pointer
         torch.cuda.synchronize()
         status_ok(h.h)
