@@ -17,6 +17,7 @@
 #include <new>
 
 #include "sfar.h"
+#include "sfar_fused.h"
 #include "sfar_internal.h"
 #include "sfar_test.h"
 
@@ -62,6 +63,9 @@ struct sfar {
     int kmax[SFAR_NUM_PROTOS][SFAR_NTHREAD_OPTS] = {};   // co-resident CTAs per rank
     int tma_tb = 0, tma_ns = 0;
     size_t tma_smem = 0;
+    // fused normalisation: co-resident clusters per launch shape, queried once
+    // ([allreduce][test][cluster size][threads index], 0 = not yet known)
+    int norm_clusters[2][2][SFAR_NORM_CLMAX + 1][4] = {};
 };
 
 static const void *kernel_for(const sfar *h, int p, int test)
@@ -550,6 +554,272 @@ sfar_status sfar_allreduce(sfar_t *h, const void *const in[], void *const out[],
         return SFAR_ERR_CUDA;
     }
     return SFAR_OK;
+}
+
+// ------------------------------------------------- fused AllReduce + RMSNorm
+static const int kNormThreads[4] = {32, 64, 128, 256};
+
+// Cluster size and threads for a row of VR vectors: 128 threads per CTA up
+// to 4096 vectors (256 beyond, up to 8192), preferably one vector per thread
+// over a cluster of up to 8 CTAs (*CL); *CLmin is the smallest cluster that
+// still gives every thread at most SFAR_NORM_VMAX vectors.  Rows of up to
+// 128 vectors take one CTA.
+static bool norm_shape(unsigned long long VR, int *CL, int *CLmin, int *ti)
+{
+    if (VR <= 128) {
+        *CL = *CLmin = 1;
+        *ti = VR <= 32 ? 0 : VR <= 64 ? 1 : 2;
+        return true;
+    }
+    const int t = VR <= 4096 ? 128 : 256;
+    *ti = t == 128 ? 2 : 3;
+    int cl = (int)ceil_div(VR, (size_t)t);
+    if (cl > SFAR_NORM_CLMAX)
+        cl = SFAR_NORM_CLMAX;
+    *CL = cl;
+    *CLmin = (int)ceil_div(VR, (size_t)t * SFAR_NORM_VMAX);
+    return *CLmin <= cl;
+}
+
+static int norm_max_clusters(sfar *h, int allreduce, int test, int CL, int ti)
+{
+    int &slot = h->norm_clusters[allreduce][test][CL][ti];
+    if (slot)
+        return slot;
+    cudaLaunchConfig_t cfg;
+    memset(&cfg, 0, sizeof cfg);
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)CL;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.gridDim = dim3((unsigned)CL);
+    cfg.blockDim = dim3((unsigned)kNormThreads[ti]);
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, sfar_kernel_fused(h->dt, h->R > 8, allreduce, test), &cfg) !=
+        cudaSuccess) {
+        cudaGetLastError();
+        return -1;
+    }
+    slot = n > 0 ? n : -1;
+    return slot;
+}
+
+// Launch shape of a fused call: threads per CTA, cluster size (shrunk from
+// the preferred one while R clusters cannot be resident at once) and
+// clusters per rank G (one row per cluster at a time, K = G * CL <= KMAX).
+static sfar_status norm_geometry(sfar *h, int allreduce, int test, size_t rows, unsigned long long VR, int *CL_out,
+                                 int *G_out, int *threads_out)
+{
+    int CL = 0, CLmin = 0, ti = 0;
+    if (!norm_shape(VR, &CL, &CLmin, &ti))
+        return SFAR_ERR_INVALID;
+    int cur = -1;
+    cudaGetDevice(&cur);
+    if (cur != h->dev)
+        cudaSetDevice(h->dev);
+    int maxc = -1;
+    for (; CL >= CLmin; --CL) {
+        maxc = norm_max_clusters(h, allreduce, test, CL, ti);
+        if (maxc < 0 || maxc >= h->R)
+            break;
+    }
+    if (cur != h->dev && cur >= 0)
+        cudaSetDevice(cur);
+    if (maxc < 0)
+        return SFAR_ERR_CUDA;
+    if (CL < CLmin)
+        return SFAR_ERR_UNSUPPORTED;
+    size_t G = (size_t)maxc / (size_t)h->R;
+    if (G > (size_t)(SFAR_KMAX / CL))
+        G = (size_t)(SFAR_KMAX / CL);
+    if (G > rows)
+        G = rows;
+    if (G < 1)
+        G = 1;
+    *CL_out = CL;
+    *G_out = (int)G;
+    *threads_out = kNormThreads[ti];
+    return SFAR_OK;
+}
+
+static bool ranges_overlap(const void *a, const void *b, size_t bytes)
+{
+    const uintptr_t a0 = (uintptr_t)a, b0 = (uintptr_t)b;
+    return a0 < b0 + bytes && b0 < a0 + bytes;
+}
+
+static sfar_status fused_call(sfar *h, const void *const in[], const void *const residual[], const void *weight,
+                              void *const out[], void *const residual_out[], size_t rows, size_t hidden, float eps,
+                              int allreduce, sfar_stream_t s)
+{
+    if (!h)
+        return SFAR_ERR_INVALID;
+    if (allreduce && h->poisoned)
+        return SFAR_ERR_POISONED;
+    if (rows == 0)
+        return SFAR_OK;
+    if (!in || !residual || !weight || !out || !residual_out || hidden == 0 || ((uintptr_t)weight & 15u))
+        return SFAR_ERR_INVALID;
+    const int R = h->R;
+    const size_t es = (size_t)h->es;
+    if ((hidden * es) % 16 || rows > ((size_t)-1) / 16 / (hidden * es))
+        return SFAR_ERR_INVALID;
+    const size_t bytes = rows * hidden * es;
+    if (allreduce && bytes > h->rb)
+        return SFAR_ERR_INVALID;
+    const unsigned long long VR = hidden * es / 16;
+    if (VR > 8192 || (R > 8 && VR > 4096))
+        return SFAR_ERR_INVALID;
+    for (int r = 0; r < R; ++r)
+        if (!in[r] || !residual[r] || !out[r] || !residual_out[r] || ((uintptr_t)in[r] & 15u) ||
+            ((uintptr_t)residual[r] & 15u) || ((uintptr_t)out[r] & 15u) || ((uintptr_t)residual_out[r] & 15u))
+            return SFAR_ERR_INVALID;
+    // writes (out, residual_out) overlap no read (in, residual, weight) and no
+    // other write; residual_out[r] == residual[r] (in place) is the exception
+    for (int i = 0; i < R; ++i) {
+        const void *w[2] = {out[i], residual_out[i]};
+        for (int m = 0; m < 2; ++m) {
+            if (ranges_overlap(w[m], weight, hidden * es))
+                return SFAR_ERR_INVALID;
+            for (int j = 0; j < R; ++j) {
+                if (ranges_overlap(w[m], in[j], bytes))
+                    return SFAR_ERR_INVALID;
+                if (ranges_overlap(w[m], residual[j], bytes) && !(m == 1 && j == i && w[m] == residual[j]))
+                    return SFAR_ERR_INVALID;
+                for (int n = 0; n < 2; ++n) {
+                    const void *o = n == 0 ? out[j] : residual_out[j];
+                    if ((j != i || n != m) && ranges_overlap(w[m], o, bytes))
+                        return SFAR_ERR_INVALID;
+                }
+            }
+        }
+    }
+    const int test = allreduce && (h->k_strag || h->k_drop || h->k_single) ? 1 : 0;
+    int CL = 0, G = 0, threads = 0;
+    const sfar_status gst = norm_geometry(h, allreduce, test, rows, VR, &CL, &G, &threads);
+    if (gst != SFAR_OK)
+        return gst;
+    const int K = G * CL;
+    int cur = -1;
+    cudaGetDevice(&cur);
+
+    SfarArgs a;
+    memset(&a, 0, sizeof a);
+    SfarNormArgs na;
+    memset(&na, 0, sizeof na);
+    for (int r = 0; r < R; ++r) {
+        a.in[r] = in[r];
+        a.out[r] = out[r];
+        na.res[r] = residual[r];
+        na.res_out[r] = residual_out[r];
+    }
+    a.n = rows * hidden;
+    a.epoch = h->epoch;
+    a.done = h->done;
+    a.ctl = h->ctl;
+    a.R = R;
+    a.K = K;
+    a.region = h->r_ll;
+    a.slot = h->s_ll;
+    a.trace = allreduce ? h->trace : nullptr;
+    a.trace_calls = allreduce ? h->trace_calls : 0;
+    na.weight = weight;
+    na.rows = rows;
+    na.hidden = hidden;
+    na.eps = eps;
+    na.G = (int)G;
+    na.CL = CL;
+    int c = 0;
+    while (((size_t)1 << c) < hidden)
+        ++c;
+    na.F = 53 - c;
+    a.overlap = 0;
+    if (allreduce && h->mode == SFAR_LAUNCH_OVERLAP) {
+        // the vector -> CTA mapping depends on the cluster shape and the row
+        // length too, so all of them are part of the overlap key
+        cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+        unsigned long long cap = 0;
+        if (cudaStreamGetCaptureInfo((cudaStream_t)s, &cs, &cap) != cudaSuccess) {
+            cudaGetLastError();
+            cs = cudaStreamCaptureStatusNone;
+        }
+        if (cs != cudaStreamCaptureStatusActive)
+            cap = 0;
+        const long long key = (31ll << 40) | ((long long)CL << 36) | ((long long)K << 27) |
+                              ((long long)threads << 16) | (long long)VR;
+        a.overlap = (key == h->last_key && s == h->last_stream && cap == h->last_capture) ? 1 : 0;
+        h->last_key = key;
+        h->last_stream = s;
+        h->last_capture = cap;
+    }
+
+    cudaLaunchConfig_t cfg;
+    memset(&cfg, 0, sizeof cfg);
+    cfg.gridDim = dim3((unsigned)(R * K));
+    cfg.blockDim = dim3((unsigned)threads);
+    cfg.stream = (cudaStream_t)s;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)CL;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    int na_attr = 1;
+    if (h->mode != SFAR_LAUNCH_PLAIN) {
+        attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[1].val.programmaticStreamSerializationAllowed = 1;
+        na_attr = 2;
+    }
+    cfg.attrs = attr;
+    cfg.numAttrs = na_attr;
+    void *args[] = {&a, &na};
+    if (cur != h->dev)
+        cudaSetDevice(h->dev);
+    cudaError_t err = cudaLaunchKernelExC(&cfg, sfar_kernel_fused(h->dt, R > 8, allreduce, test), args);
+    if (cur != h->dev && cur >= 0)
+        cudaSetDevice(cur);
+    if (err != cudaSuccess) {
+        cudaGetLastError();
+        return SFAR_ERR_CUDA;
+    }
+    return SFAR_OK;
+}
+
+sfar_status sfar_test_query_norm_launch(sfar_t *h, size_t rows, size_t hidden, int allreduce, int *ctas_per_rank,
+                                        int *cluster_size, int *threads_per_cta)
+{
+    if (!h || hidden == 0 || rows == 0 || (hidden * (size_t)h->es) % 16)
+        return SFAR_ERR_INVALID;
+    const unsigned long long VR = hidden * (size_t)h->es / 16;
+    if (VR > 8192 || (h->R > 8 && VR > 4096))
+        return SFAR_ERR_INVALID;
+    int CL = 0, G = 0, threads = 0;
+    const sfar_status st = norm_geometry(h, allreduce ? 1 : 0, 0, rows, VR, &CL, &G, &threads);
+    if (st != SFAR_OK)
+        return st;
+    if (ctas_per_rank)
+        *ctas_per_rank = G * CL;
+    if (cluster_size)
+        *cluster_size = CL;
+    if (threads_per_cta)
+        *threads_per_cta = threads;
+    return SFAR_OK;
+}
+
+sfar_status sfar_allreduce_add_rmsnorm(sfar_t *h, const void *const in[], const void *const residual[],
+                                       const void *weight, void *const out[], void *const residual_out[],
+                                       size_t rows, size_t hidden, float eps, sfar_stream_t s)
+{
+    return fused_call(h, in, residual, weight, out, residual_out, rows, hidden, eps, 1, s);
+}
+
+sfar_status sfar_add_rmsnorm(sfar_t *h, const void *const a[], const void *const residual[], const void *weight,
+                             void *const out[], void *const residual_out[], size_t rows, size_t hidden, float eps,
+                             sfar_stream_t s)
+{
+    return fused_call(h, a, residual, weight, out, residual_out, rows, hidden, eps, 0, s);
 }
 
 sfar_status sfar_status_get(sfar_t *h, sfar_fault *info)

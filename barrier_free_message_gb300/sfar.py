@@ -26,7 +26,8 @@ SFAR_OK, SFAR_ERR_INVALID, SFAR_ERR_CUDA, SFAR_ERR_OOM, SFAR_ERR_TIMEOUT, SFAR_E
 SFAR_LAUNCH_SERIAL, SFAR_LAUNCH_OVERLAP, SFAR_LAUNCH_PLAIN = 0, 1, 2
 MODES = {"serial": SFAR_LAUNCH_SERIAL, "overlap": SFAR_LAUNCH_OVERLAP, "plain": SFAR_LAUNCH_PLAIN}
 WAIT_NAMES = {1: "done", 2: "ll", 3: "sentinel", 4: "ready", 5: "bottom", 6: "ll128", 7: "rs", 8: "ag",
-              9: "arrive", 10: "complete", 11: "copy", 12: "counter"}
+              9: "arrive", 10: "complete", 11: "copy", 12: "counter",
+              13: "cluster"}
 
 
 class SfarFault(ctypes.Structure):
@@ -57,6 +58,12 @@ _SIGS = [
     ("sfar_max_bytes", ctypes.c_size_t, [ctypes.c_void_p, ctypes.c_int]),
     ("sfar_allreduce_noalloc", ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t,
                                               ctypes.c_int, ctypes.c_void_p]),
+    ("sfar_allreduce_add_rmsnorm", ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                                                  ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t,
+                                                  ctypes.c_size_t, ctypes.c_float, ctypes.c_void_p]),
+    ("sfar_add_rmsnorm", ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                                        ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_size_t,
+                                        ctypes.c_float, ctypes.c_void_p]),
     ("sfar_test_set_straggler", ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_uint32, ctypes.c_int,
                                                ctypes.c_int, ctypes.c_void_p]),
     ("sfar_test_drop_rank", ctypes.c_int, [ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p]),
@@ -65,6 +72,9 @@ _SIGS = [
     ("sfar_set_launch_mode", ctypes.c_int, [ctypes.c_void_p, ctypes.c_int]),
     ("sfar_test_set_geometry", ctypes.c_int, [ctypes.c_void_p, ctypes.c_int, ctypes.c_int]),
     ("sfar_test_set_trace", ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_uint32]),
+    ("sfar_test_query_norm_launch", ctypes.c_int, [ctypes.c_void_p, ctypes.c_size_t, ctypes.c_size_t, ctypes.c_int,
+                                                   ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_int),
+                                                   ctypes.POINTER(ctypes.c_int)]),
     ("sfar_probe_empty", ctypes.c_int, [ctypes.c_void_p]),
     ("sfar_probe_pingpong", ctypes.c_int, [ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                            ctypes.c_void_p, ctypes.c_void_p]),
@@ -125,6 +135,27 @@ def sfar_create(R: int, max_bytes: int, dtype="bf16"):
 def sfar_allreduce(h, in_ptrs, out_ptrs, n: int, proto="ll", stream=None) -> int:
     p = PROTOS[proto] if isinstance(proto, str) else int(proto)
     return lib().sfar_allreduce(h, _ptr_array(in_ptrs), _ptr_array(out_ptrs), n, p, _stream(stream))
+
+
+def sfar_allreduce_add_rmsnorm(h, in_ptrs, res_ptrs, weight_ptr: int, out_ptrs, res_out_ptrs, rows: int,
+                               hidden: int, eps: float, stream=None) -> int:
+    return lib().sfar_allreduce_add_rmsnorm(h, _ptr_array(in_ptrs), _ptr_array(res_ptrs), int(weight_ptr),
+                                            _ptr_array(out_ptrs), _ptr_array(res_out_ptrs), rows, hidden, eps,
+                                            _stream(stream))
+
+
+def sfar_add_rmsnorm(h, a_ptrs, res_ptrs, weight_ptr: int, out_ptrs, res_out_ptrs, rows: int, hidden: int,
+                     eps: float, stream=None) -> int:
+    return lib().sfar_add_rmsnorm(h, _ptr_array(a_ptrs), _ptr_array(res_ptrs), int(weight_ptr),
+                                  _ptr_array(out_ptrs), _ptr_array(res_out_ptrs), rows, hidden, eps, _stream(stream))
+
+
+def sfar_test_query_norm_launch(h, rows: int, hidden: int, allreduce: bool = True):
+    """(status, ctas_per_rank, cluster_size, threads_per_cta) of a fused call."""
+    k, cl, t = ctypes.c_int(0), ctypes.c_int(0), ctypes.c_int(0)
+    code = lib().sfar_test_query_norm_launch(h, rows, hidden, 1 if allreduce else 0, ctypes.byref(k),
+                                             ctypes.byref(cl), ctypes.byref(t))
+    return code, k.value, cl.value, t.value
 
 
 def sfar_allreduce_noalloc(in_ptrs, out_ptrs, R: int, n: int, dtype="bf16", stream=None) -> int:
@@ -212,6 +243,22 @@ class Sfar:
             n = ins[0].numel()
         code = sfar_allreduce(self.h, [t.data_ptr() for t in ins], [t.data_ptr() for t in outs], n, proto, stream)
         _check(code, "sfar_allreduce")
+
+    def allreduce_add_rmsnorm(self, ins, residuals, weight, outs, residual_outs, hidden: int, eps: float,
+                              stream=None) -> None:
+        """Tensors of rows * hidden elements per rank; weight of hidden elements."""
+        rows = ins[0].numel() // hidden
+        code = sfar_allreduce_add_rmsnorm(self.h, [t.data_ptr() for t in ins], [t.data_ptr() for t in residuals],
+                                          weight.data_ptr(), [t.data_ptr() for t in outs],
+                                          [t.data_ptr() for t in residual_outs], rows, hidden, eps, stream)
+        _check(code, "sfar_allreduce_add_rmsnorm")
+
+    def add_rmsnorm(self, a, residuals, weight, outs, residual_outs, hidden: int, eps: float, stream=None) -> None:
+        rows = a[0].numel() // hidden
+        code = sfar_add_rmsnorm(self.h, [t.data_ptr() for t in a], [t.data_ptr() for t in residuals],
+                                weight.data_ptr(), [t.data_ptr() for t in outs], [t.data_ptr() for t in residual_outs],
+                                rows, hidden, eps, stream)
+        _check(code, "sfar_add_rmsnorm")
 
     def status(self):
         return sfar_status_get(self.h)

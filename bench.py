@@ -387,13 +387,42 @@ def _time_chain(h, x_dev, out_dev, proto, reps=40, warm=3):
     return s.elapsed_time(e) * 1000.0 / (reps * calls)
 
 
+def _time_calls(h, calls, steps, reps=40, warm=3):
+    """One graph of `calls` iterations of the call sequence `steps` (each a
+    function of the call index returning a status); µs per iteration."""
+    for f in steps:
+        code = f(0)
+        if code != sfar.SFAR_OK:
+            raise sfar.SfarError(code, "warm-up")
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for c in range(calls):
+            for f in steps:
+                code = f(c)
+                if code != sfar.SFAR_OK:
+                    raise sfar.SfarError(code, "capture")
+    for _ in range(warm):
+        g.replay()
+    torch.cuda.synchronize()
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s.record()
+    for _ in range(reps):
+        g.replay()
+    e.record()
+    torch.cuda.synchronize()
+    check_status(h, "suite")
+    return s.elapsed_time(e) * 1000.0 / (reps * calls)
+
+
 def run_suite(args):
     """Sweeps printed as JSON lines: the latency curve of every protocol over
     message sizes (R = 4, 8; both launch modes), the bandwidth of the TMA path
     (R = 2..16, bf16 and fp32, 4-256 MB per rank), the cost of the barriers
     against the rank count (BASELINE vs DB vs LL vs sentinel, 16 KB per rank,
-    R = 2..16), and the atomic-accumulation two-shot against the two-shot,
-    LL128 and LL protocols (R = 4, 8, 16 over message sizes)."""
+    R = 2..16), the atomic-accumulation two-shot against the two-shot,
+    LL128 and LL protocols (R = 4, 8, 16 over message sizes), and the fused
+    AllReduce + residual add + RMSNorm against the two-kernel pipeline."""
     _build.build()
     l2 = torch.cuda.get_device_properties(torch.cuda.current_device()).L2_cache_size
     if "latency" in args.suite:
@@ -439,6 +468,48 @@ def run_suite(args):
             row["bottom_barrier"] = round(row["baseline"] - row["db"], 3)
             print(json.dumps(row), flush=True)
             h.close()
+    if "fused" in args.suite:
+        # AllReduce + residual add + RMSNorm in one kernel against the two-kernel
+        # pipeline (LL AllReduce, then the normalisation kernel)
+        import oracle
+        for R, rows, hidden in ((8, 1, 8192), (8, 64, 7168), (4, 1, 8192), (16, 1, 8192), (8, 4, 8192)):
+            calls, eps = 32, 1e-5
+            n = rows * hidden
+            x = torch.stack([inputs.draw(6, c, R, n, "normal", 1.0, "bf16") for c in range(calls)])
+            res = torch.stack([inputs.draw(7, c, R, n, "normal", 2.0, "bf16") for c in range(calls)])
+            w = inputs.draw(8, 0, 1, hidden, "normal", 1.0, "bf16")[0]
+            xd, rd, wd = x.cuda(), res.cuda(), w.cuda()
+            od, zd, ad = torch.empty_like(xd), torch.empty_like(xd), torch.empty_like(xd)
+            h = sfar.Sfar(R, 2 * n, "bf16")
+            P = lambda t, c: [t[c, r].data_ptr() for r in range(R)]
+
+            def fused(c):
+                return sfar.sfar_allreduce_add_rmsnorm(h.h, P(xd, c), P(rd, c), wd.data_ptr(), P(od, c), P(zd, c),
+                                                       rows, hidden, eps)
+
+            def allreduce(c):
+                return sfar.sfar_allreduce(h.h, P(xd, c), P(ad, c), n, "ll")
+
+            def norm(c):
+                return sfar.sfar_add_rmsnorm(h.h, P(ad, c), P(rd, c), wd.data_ptr(), P(od, c), P(zd, c), rows,
+                                             hidden, eps)
+
+            row = {"suite": "fused", "R": R, "rows": rows, "hidden": hidden, "bytes_per_rank": 2 * n}
+            row["fused_us"] = round(_time_calls(h, calls, [fused]), 3)
+            ok = True
+            for c in (0, calls - 1):
+                wy, wz = oracle.add_rmsnorm(inputs.to_bits(x[c]), inputs.to_bits(res[c]),
+                                            inputs.to_bits(w[None, :])[0], eps, hidden)
+                ok = ok and np.array_equal(inputs.to_bits(od[c].cpu()), wy) and \
+                    np.array_equal(inputs.to_bits(zd[c].cpu()), wz)
+            row["fused_bit_exact_sample"] = bool(ok)
+            row["unfused_us"] = round(_time_calls(h, calls, [allreduce, norm]), 3)
+            row["allreduce_ll_us"] = round(_time_calls(h, calls, [allreduce]), 3)
+            row["norm_alone_us"] = round(_time_calls(h, calls, [norm]), 3)
+            row["saved_us"] = round(row["unfused_us"] - row["fused_us"], 3)
+            print(json.dumps(row), flush=True)
+            h.close()
+            del xd, rd, od, zd, ad
     if "atomic" in args.suite:
         # the atomic-accumulation two-shot against the flag-line protocols
         for R in (4, 8, 16):
@@ -628,7 +699,7 @@ def main():
     ap.add_argument("--large-r", type=int, default=8)
     ap.add_argument("--large-mb", type=int, default=64)
     ap.add_argument("--large-dtype", choices=["bf16", "fp32"], default="bf16")
-    ap.add_argument("--suite", default="", help="comma list of latency,bandwidth,barriers,atomic: sweeps as JSON lines")
+    ap.add_argument("--suite", default="", help="comma list of latency,bandwidth,barriers,atomic,fused: sweeps as JSON lines")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
     world, rank, _ = dist_setup(args.gpus)

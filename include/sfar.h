@@ -99,6 +99,8 @@ typedef int sfar_status;
 #define SFAR_WAIT_COMPLETE 10 /* TMA path: owner completion flags                      */
 #define SFAR_WAIT_COPY 11     /* TMA path: bulk copy completion                        */
 #define SFAR_WAIT_COUNTER 12  /* atomic path: a line's arrival counter stayed below R  */
+#define SFAR_WAIT_CLUSTER 13  /* fused normalisation: a cluster peer's row statistics
+                                 (8 times the limit: every peer always sends)           */
 
 typedef struct {
     sfar_status code; /* SFAR_OK or SFAR_ERR_TIMEOUT                          */
@@ -177,6 +179,56 @@ sfar_status sfar_query_launch(const sfar_t *h, size_t n, sfar_proto p, int *ctas
 
 /* Largest n * element size per rank that protocol p accepts on this handle. */
 size_t sfar_max_bytes(const sfar_t *h, sfar_proto p);
+
+/*
+ * sfar_allreduce_add_rmsnorm: the AllReduce of sfar_allreduce(..., SFAR_LL,
+ * ...) followed, in the same kernel, by the residual add and the RMS
+ * normalisation that come next in a decode layer ("vLLM distributed
+ * inference core" (page 2), sections one and two: the normalisation runs on
+ * the compute stream right after the AllReduce of the attention output and
+ * of the MLP down projection).  The pages give no formula; the one
+ * implemented, with every rounding fixed so the result is unique bit for bit
+ * whatever the launch geometry, is, per rank r and row i of `hidden`
+ * elements (T = the handle's dtype):
+ *   a   = the AllReduce result of the row, in T (as sfar_allreduce stores it);
+ *   z   = T(a + residual[r])                      binary32 add;
+ *   ms  = ldexp(float(S) / hidden, 2E - F), S = the sum of z^2 over the row
+ *         in units of 2^(2E - F), each term truncated to a whole unit (2^E
+ *         the smallest power of two above every |z|, F = 53 -
+ *         ceil(log2 hidden)): an exact integer sum below 2^53, short of the
+ *         exact sum of squares by less than 2^(2c - 51) of the largest square
+ *         (c = ceil(log2 hidden)); float(S) and the division are binary32,
+ *         each rounded once;
+ *         a NaN in the row gives NaN, else an infinity gives +inf;
+ *   y   = T((z * (1 / sqrt(ms + eps))) * weight)  each binary32 operation
+ *         rounded to nearest even.
+ * out[r] receives y and residual_out[r] receives z (rows x hidden each).
+ * in, residual, out, residual_out: HOST arrays of R DEVICE pointers, each
+ * buffer rows * hidden elements, row-major, 16-byte aligned; weight: one
+ * device buffer of hidden elements shared by all ranks, 16-byte aligned.
+ * hidden * element size must be a multiple of 16 and at most 128 KiB (64 KiB
+ * for R > 8); rows * hidden * element size must not exceed
+ * sfar_max_bytes(h, SFAR_LL).
+ * residual_out[r] may be residual[r] (in place); otherwise no output may
+ * overlap an input, the weight or another output.  rows == 0 is a no-op.
+ * One kernel on stream s (thread-block clusters, one cluster per row at a
+ * time); capturable; errors as for sfar_allreduce.
+ */
+sfar_status sfar_allreduce_add_rmsnorm(sfar_t *h, const void *const in[], const void *const residual[],
+                                       const void *weight, void *const out[], void *const residual_out[],
+                                       size_t rows, size_t hidden, float eps, sfar_stream_t s);
+
+/*
+ * sfar_add_rmsnorm: the same residual add and normalisation on its own:
+ * a[r] is taken as rank r's AllReduce result (rows x hidden elements of the
+ * handle's dtype).  The arguments, the definition and the rules are those of
+ * sfar_allreduce_add_rmsnorm (minus the AllReduce and its size limit); it
+ * uses none of the handle's buffers, only its rank count and dtype.  One
+ * kernel on stream s.
+ */
+sfar_status sfar_add_rmsnorm(sfar_t *h, const void *const a[], const void *const residual[], const void *weight,
+                             void *const out[], void *const residual_out[], size_t rows, size_t hidden, float eps,
+                             sfar_stream_t s);
 
 /*
  * sfar_allreduce_noalloc: the same AllReduce as sfar_allreduce(h, in, out, n,

@@ -82,8 +82,17 @@ sfar_status sfar_test_set_trace(sfar_t *h, uint64_t *trace, uint32_t calls);
 /* Launch geometry of every later call of the receive-buffer protocols:
  * CTAs per rank (0 = automatic; clamped to what can be co-resident) and
  * threads per CTA (0 = automatic, else 64, 128 or 256; the TMA path always
- * uses 256).  SFAR_ERR_INVALID for another thread count. */
+ * uses 320).  SFAR_ERR_INVALID for another thread count.  The fused
+ * normalisation calls choose their own shape and ignore this. */
 sfar_status sfar_test_set_geometry(sfar_t *h, int ctas_per_rank, int threads_per_cta);
+
+/* Launch shape of sfar_allreduce_add_rmsnorm (allreduce = 1) or
+ * sfar_add_rmsnorm (allreduce = 0) for rows x hidden: CTAs per rank, CTAs per
+ * thread-block cluster (a row is spread over one cluster) and threads per
+ * CTA.  Returns what the call itself would return for the shape
+ * (SFAR_ERR_INVALID, SFAR_ERR_UNSUPPORTED) without launching anything. */
+sfar_status sfar_test_query_norm_launch(sfar_t *h, size_t rows, size_t hidden, int allreduce, int *ctas_per_rank,
+                                        int *cluster_size, int *threads_per_cta);
 
 /*
  * Latency floor probes.

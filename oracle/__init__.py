@@ -41,6 +41,9 @@ def _lib(mutant: int = 0):
         lib.sfar_oracle_mutant.restype = ctypes.c_int
         lib.sfar_oracle_narrow_bf16_n.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t]
         lib.sfar_oracle_narrow_bf16_n.restype = None
+        lib.sfar_oracle_add_rmsnorm.argtypes = [ctypes.c_int, ctypes.c_size_t, ctypes.c_size_t, ctypes.c_int, vpp,
+                                                vpp, ctypes.c_void_p, ctypes.c_float, vpp, vpp, ctypes.c_int]
+        lib.sfar_oracle_add_rmsnorm.restype = ctypes.c_int
         _libs[mutant] = lib
     return _libs[mutant]
 
@@ -99,3 +102,31 @@ def narrow_bf16_array(f: np.ndarray, mutant: int = 0) -> np.ndarray:
     out = np.empty(f.shape, dtype=np.uint16)
     _lib(mutant).sfar_oracle_narrow_bf16_n(f.ctypes.data, out.ctypes.data, f.size)
     return out
+
+
+def add_rmsnorm(x: np.ndarray, res: np.ndarray, weight: np.ndarray, eps: float, hidden: int,
+                allreduce_first: bool = True, mutant: int = 0):
+    """AllReduce (or not) + residual add + RMS normalisation, as defined in
+    ``sfar_oracle.c``.  x, res: [R, rows * hidden]; weight: [hidden]; same
+    dtype (uint16 bf16 bits or float32).  Returns (out, res_out), each
+    [R, rows * hidden]."""
+    x = np.ascontiguousarray(x)
+    res = np.ascontiguousarray(res)
+    weight = np.ascontiguousarray(weight)
+    if x.ndim != 2 or res.shape != x.shape or weight.shape != (hidden,) or x.shape[1] % hidden:
+        raise ValueError("x, res must be [R, rows * hidden] and weight [hidden]")
+    if res.dtype != x.dtype or weight.dtype != x.dtype:
+        raise TypeError("x, res and weight must share one dtype")
+    R, total = x.shape
+    code = _dtype_code(x)
+    out = np.empty_like(x)
+    res_out = np.empty_like(x)
+    vp = ctypes.c_void_p * R
+    rc = _lib(mutant).sfar_oracle_add_rmsnorm(
+        R, total // hidden, hidden, code, vp(*[x[r].ctypes.data for r in range(R)]),
+        vp(*[res[r].ctypes.data for r in range(R)]), weight.ctypes.data, float(eps),
+        vp(*[out[r].ctypes.data for r in range(R)]), vp(*[res_out[r].ctypes.data for r in range(R)]),
+        1 if allreduce_first else 0)
+    if rc != 0:
+        raise ValueError("oracle rejected the arguments")
+    return out, res_out

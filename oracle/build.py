@@ -23,7 +23,7 @@ def build_oracle(mutant: int = 0, force: bool = False) -> str:
     if not force and os.path.exists(out) and os.path.getmtime(out) >= os.path.getmtime(SRC):
         return out
     tmp = out + f".tmp{os.getpid()}"
-    cmd = ["gcc", *CFLAGS, f"-DORACLE_MUTANT={int(mutant)}", SRC, "-o", tmp]
+    cmd = ["gcc", *CFLAGS, f"-DORACLE_MUTANT={int(mutant)}", SRC, "-o", tmp, "-lm"]
     subprocess.run(cmd, check=True)
     os.replace(tmp, out)
     return out

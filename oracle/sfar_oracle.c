@@ -33,9 +33,11 @@
  * this oracle catch it.  The shipped object is always built with 0.
  */
 #include <float.h>
+#include <math.h>
 #include <pthread.h>
 #include <stddef.h>
 #include <stdint.h>
+#include <stdlib.h>
 #include <string.h>
 
 #if FLT_EVAL_METHOD != 0
@@ -237,6 +239,144 @@ int sfar_oracle_allreduce_mt(int R, size_t n, int dtype, const void *const *in,
     }
     for (int t = 0; t < started; ++t)
         if (tid[t]) pthread_join(tid[t], NULL);
+    return 0;
+}
+
+/* ------------------------------------------------------------------------
+ * The step after the AllReduce: residual add and RMS normalisation.
+ *
+ * "vLLM distributed inference core" (page 2), section one: in a decode step
+ * the compute stream runs the normalisation right after the AllReduce of the
+ * attention output projection and of the MLP down projection; section two
+ * puts it on the compute stream after the wait for the AllReduce.  The pages
+ * give no formula and no precision.  Readings taken (root-mean-square
+ * normalisation of the residual stream, the form used by current decoder
+ * models; every rounding spelled out so the result is unique):
+ *
+ *   a[j]   = the AllReduce result of element j of the row, in the element
+ *            type (exactly what sfar_oracle_allreduce stores);
+ *   z[j]   = T(a[j] (+) res[j])      binary32 add, one rounding to type T;
+ *   ms     = ldexp(float(S) (/) h, 2E - F)
+ *                                    S = sum_j z[j]^2 with every term
+ *            truncated to a multiple of 2^(2E - F), where 2^E is the
+ *            smallest power of two above every |z[j]| of the row and
+ *            F = 53 - c, c = ceil(log2 h): the sum is then exact in 64-bit
+ *            integers (< 2^53) and independent of the order (S counts
+ *            units of 2^(2E - F)); float(S) rounds once to binary32, the
+ *            division by h is a binary32 division, and the scaling by
+ *            2^(2E - F) rounds only in the subnormal range; against the
+ *            largest square of the row (>= 2^(2E - 2)) it is short of the
+ *            exact sum of squares by less than h 2^(2 - F) <= 2^(2c - 51)
+ *            (2^-25 for h = 8192); a NaN in the row makes ms NaN, otherwise
+ *            an infinity makes it +inf, and an all-zero row gives 0;
+ *   rstd   = 1 (/) sqrt(ms (+) eps)  binary32, each operation rounded;
+ *   y[j]   = T((z[j] (*) rstd) (*) w[j])   binary32 products, one rounding
+ *            to T.
+ * Outputs per rank r: out[r] = y, res_out[r] = z.
+ * ------------------------------------------------------------------------ */
+
+/* smallest c >= 0 with 2^c >= h */
+static int ceil_log2(size_t h)
+{
+    int c = 0;
+    while (((size_t)1 << c) < h)
+        ++c;
+    return c;
+}
+
+/* ms of one row of z (h binary32 values, already rounded to the type). */
+static float row_mean_square(const float *z, size_t h)
+{
+    int any_nan = 0, any_inf = 0;
+    double maxabs = 0.0;
+    for (size_t j = 0; j < h; ++j) {
+        if (isnan(z[j])) any_nan = 1;
+        else if (isinf(z[j])) any_inf = 1;
+        else if (fabs((double)z[j]) > maxabs) maxabs = fabs((double)z[j]);
+    }
+    if (any_nan) return NAN;
+    if (any_inf) return INFINITY;
+    if (maxabs == 0.0) return 0.0f;
+    int E;
+    (void)frexp(maxabs, &E);                    /* maxabs = m 2^E, 1/2 <= m < 1 */
+#if ORACLE_MUTANT == 17
+    E += 8;                                      /* mutant: coarser fixed point */
+#endif
+    const int F = 53 - ceil_log2(h);
+    uint64_t S = 0;
+    for (size_t j = 0; j < h; ++j) {
+        const double u = ldexp((double)z[j], -E);   /* |u| < 1, exact */
+        S += (uint64_t)floor(ldexp(u * u, F));      /* u*u exact: <= 48 bits */
+    }
+#if ORACLE_MUTANT == 13
+    const float q = (float)S / (float)(h > 1 ? h - 1 : 1);                     /* mutant: h - 1 */
+#else
+    const float q = (float)S / (float)h;
+#endif
+    return ldexpf(q, 2 * E - F);
+}
+
+static float round_to(int dtype, float v)
+{
+    return dtype == ORACLE_BF16 ? widen_bf16(narrow_bf16(v)) : v;
+}
+
+/*
+ * sfar_oracle_add_rmsnorm: for every rank r and row i (rows x h elements per
+ * rank, row-major), the definitions above.  do_allreduce = 1: a = the
+ * AllReduce of in[0..R-1]; do_allreduce = 0: a = in[r] itself (the
+ * normalisation step alone).  weight holds h elements (shared by all ranks);
+ * res[r] / res_out[r] / out[r] hold rows x h elements.  res_out[r] may be
+ * res[r].  Host memory owned by the caller.  Returns 0, or -1 for a bad
+ * argument.
+ */
+int sfar_oracle_add_rmsnorm(int R, size_t rows, size_t h, int dtype, const void *const *in,
+                            const void *const *res, const void *weight, float eps, void *const *out,
+                            void *const *res_out, int do_allreduce)
+{
+    if (R < 1 || R > 64 || h == 0 || (dtype != ORACLE_BF16 && dtype != ORACLE_FP32))
+        return -1;
+    if (rows == 0)
+        return 0;
+    if (!in || !res || !weight || !out || !res_out)
+        return -1;
+    float *z = (float *)malloc(h * sizeof(float));
+    if (!z)
+        return -1;
+    for (int r = 0; r < R; ++r) {
+        for (size_t i = 0; i < rows; ++i) {
+            for (size_t j = 0; j < h; ++j) {
+                const size_t e = i * h + j;
+                const float a = do_allreduce ? round_to(dtype, fold(R, dtype, in, rows * h, e))
+                                             : load_elem(in[r], dtype, e);
+#if ORACLE_MUTANT == 12
+                z[j] = a;                                        /* mutant: residual dropped */
+#elif ORACLE_MUTANT == 16
+                z[j] = a + load_elem(res[r], dtype, e);          /* mutant: z not rounded */
+#else
+                z[j] = round_to(dtype, a + load_elem(res[r], dtype, e));
+#endif
+            }
+            const float ms = row_mean_square(z, h);
+#if ORACLE_MUTANT == 14
+            const float rstd = 1.0f / sqrtf(ms) + eps;          /* mutant: eps outside */
+#else
+            const float rstd = 1.0f / sqrtf(ms + eps);
+#endif
+            for (size_t j = 0; j < h; ++j) {
+                const size_t e = i * h + j;
+                const float t = z[j] * rstd;
+#if ORACLE_MUTANT == 15
+                const float y = t;                               /* mutant: weight dropped */
+#else
+                const float y = t * load_elem(weight, dtype, j);
+#endif
+                store_elem(out[r], dtype, e, y);
+                store_elem(res_out[r], dtype, e, z[j]);
+            }
+        }
+    }
+    free(z);
     return 0;
 }
 

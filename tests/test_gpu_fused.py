@@ -1,0 +1,264 @@
+"""The fused AllReduce + residual add + RMS normalisation (and the
+normalisation on its own) against the oracle, bit for bit on every rank.
+
+NaN results are compared as NaN (the oracle's NaN payloads follow the host
+CPU, the GPU's are canonical); every other element is compared bit for bit.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from barrier_free_message_gb300 import inputs, sfar
+from gpu_helpers import ensure_built, status_ok
+
+pytestmark = pytest.mark.gpu
+TDT = {"bf16": torch.bfloat16, "fp32": torch.float32}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    ensure_built()
+
+
+def draw_case(seed, R, rows, h, dtype, sigma=1.0):
+    x = inputs.draw(seed, 0, R, rows * h, "normal", sigma, dtype)
+    res = inputs.draw(seed, 1, R, rows * h, "normal", 2.0, dtype)
+    w = inputs.draw(seed, 2, 1, h, "normal", 1.0, dtype)[0]
+    return x, res, w
+
+
+def bits(t):
+    b = inputs.to_bits(t.detach().cpu())
+    return b.view(np.uint32) if b.dtype == np.float32 else b
+
+
+def assert_equal_nan_aware(got_t, want, ctx):
+    got = bits(got_t)
+    want = want.view(np.uint32) if want.dtype == np.float32 else want
+    if want.dtype == np.uint16:
+        gn = ((got & 0x7F80) == 0x7F80) & ((got & 0x7F) != 0)
+        wn = ((want & 0x7F80) == 0x7F80) & ((want & 0x7F) != 0)
+    else:
+        gn = ((got & 0x7F800000) == 0x7F800000) & ((got & 0x7FFFFF) != 0)
+        wn = ((want & 0x7F800000) == 0x7F800000) & ((want & 0x7FFFFF) != 0)
+    bad = (got != want) & ~(gn & wn)
+    if bad.any():
+        i = int(np.nonzero(bad)[0][0])
+        raise AssertionError(f"{ctx}: {int(bad.sum())} of {bad.size} elements differ; first at {i}: "
+                             f"got {int(got[i]):#x} want {int(want[i]):#x}")
+
+
+def run_fused(h, x, res, w, hidden, eps, allreduce=True, in_place=False):
+    R = x.shape[0]
+    ins = [x[r].contiguous().cuda() for r in range(R)]
+    rs = [res[r].contiguous().cuda() for r in range(R)]
+    wd = w.contiguous().cuda()
+    outs = [torch.empty_like(t) for t in ins]
+    for o in outs:
+        o.view(torch.uint8).fill_(0xA5)
+    routs = rs if in_place else [torch.empty_like(t) for t in rs]
+    if allreduce:
+        h.allreduce_add_rmsnorm(ins, rs, wd, outs, routs, hidden, eps)
+    else:
+        h.add_rmsnorm(ins, rs, wd, outs, routs, hidden, eps)
+    torch.cuda.synchronize()
+    status_ok(h.h, "fused")
+    return outs, routs
+
+
+def check(h, x, res, w, hidden, eps, ctx, allreduce=True, in_place=False):
+    want_y, want_z = oracle.add_rmsnorm(inputs.to_bits(x), inputs.to_bits(res), inputs.to_bits(w[None, :])[0],
+                                        eps, hidden, allreduce_first=allreduce)
+    outs, routs = run_fused(h, x, res, w, hidden, eps, allreduce, in_place)
+    for r in range(x.shape[0]):
+        assert_equal_nan_aware(routs[r], want_z[r], f"{ctx} z rank {r}")
+        assert_equal_nan_aware(outs[r], want_y[r], f"{ctx} y rank {r}")
+
+
+SHAPES = {"bf16": [(1, 8192), (3, 7168), (5, 64), (2, 8), (1, 24), (4, 1000), (2, 32768), (1, 65536), (64, 7168)],
+          "fp32": [(1, 8192), (3, 7168), (5, 64), (2, 4), (1, 20), (4, 1000), (1, 32768), (32, 4096)]}
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp32"])
+@pytest.mark.parametrize("R", [2, 3, 8, 16])
+def test_fused_parity(R, dtype):
+    h = sfar.Sfar(R, 1 << 20, dtype)
+    es = 2 if dtype == "bf16" else 4
+    try:
+        for rows, hidden in SHAPES[dtype]:
+            code, k, cl, t = sfar.sfar_test_query_norm_launch(h.h, rows, hidden)
+            if R > 8 and hidden * es > 65536:
+                assert code == sfar.SFAR_ERR_INVALID          # rows above 64 KiB need R <= 8
+                continue
+            assert code == sfar.SFAR_OK and k % cl == 0 and 1 <= cl <= 8 and t in (32, 64, 128, 256)
+            x, res, w = draw_case(500 + R + rows, R, rows, hidden, dtype)
+            check(h, x, res, w, hidden, 1e-5, f"R={R} {rows}x{hidden} {dtype} ({k} CTAs/rank, cluster {cl}, {t})")
+    finally:
+        h.close()
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp32"])
+@pytest.mark.parametrize("R", [8, 16])
+def test_norm_alone_parity(R, dtype):
+    h = sfar.Sfar(R, 1 << 20, dtype)
+    es = 2 if dtype == "bf16" else 4
+    try:
+        for rows, hidden in SHAPES[dtype]:
+            if R > 8 and hidden * es > 65536:
+                continue
+            x, res, w = draw_case(600 + rows, R, rows, hidden, dtype, sigma=5.0)
+            check(h, x, res, w, hidden, 1e-6, f"alone {rows}x{hidden} {dtype}", allreduce=False)
+    finally:
+        h.close()
+
+
+def test_in_place_residual():
+    R, rows, hidden = 8, 4, 8192
+    h = sfar.Sfar(R, 1 << 20, "bf16")
+    try:
+        x, res, w = draw_case(700, R, rows, hidden, "bf16")
+        check(h, x, res, w, hidden, 1e-5, "in place", in_place=True)
+        check(h, x, res, w, hidden, 1e-5, "alone in place", allreduce=False, in_place=True)
+    finally:
+        h.close()
+
+
+def test_special_rows_and_ranges():
+    R, hidden = 4, 1024
+    h = sfar.Sfar(R, 1 << 20, "fp32")
+    try:
+        x, res, w = draw_case(701, R, 6, hidden, "fp32")
+        res[:, :hidden] = 0.0
+        x[:, :hidden] = 0.0                          # row 0: all zero
+        x[1, hidden + 7] = float("nan")              # row 1: NaN
+        res[2, 2 * hidden + 9] = float("inf")        # row 2: an infinity on rank 2 only
+        x[:, 3 * hidden:4 * hidden] *= 2.0 ** 60     # row 3: large
+        x[:, 4 * hidden:5 * hidden] *= 2.0 ** -70    # row 4: tiny (subnormal squares)
+        res[:, 4 * hidden:5 * hidden] *= 2.0 ** -70
+        check(h, x, res, w, hidden, 1e-6, "special rows")
+    finally:
+        h.close()
+
+
+@pytest.mark.parametrize("mode", ["serial", "overlap"])
+def test_fused_chain_1024_calls(mode):
+    """The decode shape (R = 8, one row of 8192 bf16) for 1,024 graph-chained
+    calls, each with its own inputs and residual."""
+    R, hidden, calls = 8, 8192, 1024
+    x = torch.stack([inputs.draw(800, c, R, hidden, "normal", 1.0, "bf16") for c in range(calls)])
+    res = torch.stack([inputs.draw(801, c, R, hidden, "normal", 2.0, "bf16") for c in range(calls)])
+    w = inputs.draw(802, 0, 1, hidden, "normal", 1.0, "bf16")[0]
+    want_y, want_z = oracle.add_rmsnorm(inputs.to_bits(x.transpose(0, 1).reshape(R, calls * hidden)),
+                                        inputs.to_bits(res.transpose(0, 1).reshape(R, calls * hidden)),
+                                        inputs.to_bits(w[None, :])[0], 1e-5, hidden)
+    h = sfar.Sfar(R, 2 * hidden, "bf16")
+    try:
+        h.set_mode(mode)
+        xd, rd, wd = x.cuda(), res.cuda(), w.cuda()
+        od, zd = torch.empty_like(xd), torch.empty_like(xd)
+        # warm-up call outside the graph (sets up the launch shape)
+        h.allreduce_add_rmsnorm([xd[0, r] for r in range(R)], [rd[0, r] for r in range(R)], wd,
+                                [od[0, r] for r in range(R)], [zd[0, r] for r in range(R)], hidden, 1e-5)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for c in range(calls):
+                code = sfar.sfar_allreduce_add_rmsnorm(h.h, [xd[c, r].data_ptr() for r in range(R)],
+                                                       [rd[c, r].data_ptr() for r in range(R)], wd.data_ptr(),
+                                                       [od[c, r].data_ptr() for r in range(R)],
+                                                       [zd[c, r].data_ptr() for r in range(R)], 1, hidden, 1e-5)
+                assert code == sfar.SFAR_OK
+        for rep in range(2):
+            od.view(torch.int16).fill_(-1)
+            g.replay()
+            torch.cuda.synchronize()
+            status_ok(h.h, f"chain {mode} replay {rep}")
+            got_y = od.transpose(0, 1).reshape(R, calls * hidden)
+            got_z = zd.transpose(0, 1).reshape(R, calls * hidden)
+            for r in range(R):
+                assert_equal_nan_aware(got_z[r], want_z[r], f"chain {mode} z rank {r}")
+                assert_equal_nan_aware(got_y[r], want_y[r], f"chain {mode} y rank {r}")
+    finally:
+        h.close()
+
+
+def test_shares_the_ll_region_with_plain_calls():
+    R, hidden = 8, 8192
+    h = sfar.Sfar(R, 1 << 20, "bf16")
+    try:
+        for i in range(12):
+            x, res, w = draw_case(900 + i, R, 1 + i % 3, hidden, "bf16")
+            if i % 2:
+                check(h, x, res, w, hidden, 1e-5, f"interleaved fused {i}")
+            else:
+                xi = x.contiguous()
+                ins = [xi[r].cuda() for r in range(R)]
+                outs = [torch.empty_like(t) for t in ins]
+                h.allreduce(ins, outs, "ll")
+                torch.cuda.synchronize()
+                status_ok(h.h, "ll")
+                want = oracle.allreduce(inputs.to_bits(xi))
+                for r in range(R):
+                    assert np.array_equal(inputs.to_bits(outs[r].cpu()), want[r])
+    finally:
+        h.close()
+
+
+def test_argument_checks():
+    R, hidden = 4, 1024
+    h = sfar.Sfar(R, 1 << 16, "bf16")
+    try:
+        x, res, w = draw_case(950, R, 2, hidden, "bf16")
+        ins = [t.cuda() for t in x]
+        rs = [t.cuda() for t in res]
+        wd = w.cuda()
+        outs = [torch.empty_like(t) for t in ins]
+        zs = [torch.empty_like(t) for t in ins]
+        P = lambda ts: [t.data_ptr() for t in ts]
+        call = lambda i=P(ins), rr=P(rs), ww=wd.data_ptr(), o=P(outs), z=P(zs), rows=2, hid=hidden: \
+            sfar.sfar_allreduce_add_rmsnorm(h.h, i, rr, ww, o, z, rows, hid, 1e-5)
+        assert call() == sfar.SFAR_OK
+        assert call(rows=0) == sfar.SFAR_OK
+        assert call(hid=1020) == sfar.SFAR_ERR_INVALID                         # row not whole vectors
+        assert call(ww=wd.data_ptr() + 2) == sfar.SFAR_ERR_INVALID             # misaligned weight
+        assert call(o=[P(rs)[0]] + P(outs)[1:]) == sfar.SFAR_ERR_INVALID        # out over a residual
+        assert call(z=[P(ins)[1]] + P(zs)[1:]) == sfar.SFAR_ERR_INVALID         # z over an input
+        assert call(z=[P(rs)[1]] + P(zs)[1:]) == sfar.SFAR_ERR_INVALID         # z over another rank's residual
+        assert call(rows=40) == sfar.SFAR_ERR_INVALID                          # over the handle's 64 KiB
+        big = sfar.Sfar(2, 1 << 20, "bf16")
+        try:
+            t = torch.zeros(2 * 65544, dtype=torch.bfloat16, device="cuda")
+            assert sfar.sfar_add_rmsnorm(big.h, [t.data_ptr()] * 2, [t.data_ptr()] * 2, t.data_ptr(),
+                                         [t.data_ptr()] * 2, [t.data_ptr()] * 2, 1, 65544, 0.0) == \
+                sfar.SFAR_ERR_INVALID                                          # row above 128 KiB
+        finally:
+            big.close()
+        torch.cuda.synchronize()
+        status_ok(h.h)
+    finally:
+        h.close()
+
+
+def test_dropped_rank_times_out_and_reset_recovers():
+    R, rows, hidden = 4, 2, 4096
+    h = sfar.Sfar(R, 1 << 16, "bf16")
+    try:
+        x, res, w = draw_case(960, R, rows, hidden, "bf16")
+        check(h, x, res, w, hidden, 1e-5, "before")
+        assert sfar.sfar_test_set_timeout(h.h, 2_000_000) == sfar.SFAR_OK
+        assert sfar.sfar_test_drop_rank(h.h, 1) == sfar.SFAR_OK
+        ins = [t.cuda() for t in x]
+        rs = [t.cuda() for t in res]
+        outs = [torch.empty_like(t) for t in ins]
+        zs = [torch.empty_like(t) for t in ins]
+        h.allreduce_add_rmsnorm(ins, rs, w.cuda(), outs, zs, hidden, 1e-5)
+        torch.cuda.synchronize()
+        code, f = sfar.sfar_status_get(h.h)
+        assert code == sfar.SFAR_ERR_TIMEOUT and sfar.WAIT_NAMES[f.where] == "ll" and f.peer in (1, -1)
+        h.reset()
+        assert sfar.sfar_test_drop_rank(h.h, -1) == sfar.SFAR_OK
+        torch.cuda.synchronize()
+        check(h, x, res, w, hidden, 1e-5, "after reset")
+    finally:
+        h.close()
