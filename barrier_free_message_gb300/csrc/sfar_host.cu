@@ -17,7 +17,9 @@
 #include <new>
 
 #include "sfar.h"
+#include "sfar_decode.h"
 #include "sfar_fused.h"
+#include "sfar_gemv.h"
 #include "sfar_internal.h"
 #include "sfar_test.h"
 
@@ -820,6 +822,71 @@ sfar_status sfar_add_rmsnorm(sfar_t *h, const void *const a[], const void *const
                              sfar_stream_t s)
 {
     return fused_call(h, a, residual, weight, out, residual_out, rows, hidden, eps, 0, s);
+}
+
+// ------------------------------------------------ row-parallel projection
+sfar_status sfar_rowpar_gemv(sfar_t *h, const void *const x[], const void *const w[], void *const y[], size_t k,
+                             size_t hidden, size_t prefetch_rows, sfar_stream_t s)
+{
+    if (!h || !x || !w || !y || h->dt != SFAR_BF16 || k == 0 || hidden == 0 || hidden % 8 ||
+        k > ((size_t)-1) / 2 / hidden)
+        return SFAR_ERR_INVALID;
+    const int R = h->R;
+    const size_t wbytes = k * hidden * 2, ybytes = hidden * 2, xbytes = k * 2;
+    for (int r = 0; r < R; ++r) {
+        if (!x[r] || !w[r] || !y[r] || ((uintptr_t)x[r] & 1u) || ((uintptr_t)w[r] & 15u) || ((uintptr_t)y[r] & 15u))
+            return SFAR_ERR_INVALID;
+    }
+    for (int i = 0; i < R; ++i)
+        for (int j = 0; j < R; ++j) {
+            const uintptr_t y0 = (uintptr_t)y[i], y1 = y0 + ybytes;
+            const uintptr_t x0 = (uintptr_t)x[j], x1 = x0 + xbytes, w0 = (uintptr_t)w[j], w1 = w0 + wbytes;
+            if ((y0 < x1 && x0 < y1) || (y0 < w1 && w0 < y1))
+                return SFAR_ERR_INVALID;
+            if (i != j) {
+                const uintptr_t z0 = (uintptr_t)y[j], z1 = z0 + ybytes;
+                if (y0 < z1 && z0 < y1)
+                    return SFAR_ERR_INVALID;
+            }
+        }
+    SfarGemvArgs g;
+    memset(&g, 0, sizeof g);
+    for (int r = 0; r < R; ++r) {
+        g.x[r] = x[r];
+        g.w[r] = w[r];
+        g.y[r] = y[r];
+    }
+    g.k = k;
+    g.h = hidden;
+    g.seg = ceil_div(k, SFAR_GEMV_SEGMENTS);
+    g.prefetch = prefetch_rows < g.seg ? prefetch_rows : g.seg;
+    g.tiles = (int)ceil_div(hidden, SFAR_GEMV_COLS);
+
+    cudaLaunchConfig_t cfg;
+    memset(&cfg, 0, sizeof cfg);
+    cfg.gridDim = dim3((unsigned)(R * g.tiles));
+    cfg.blockDim = dim3(SFAR_GEMV_SEGMENTS * 32);
+    cfg.stream = (cudaStream_t)s;
+    cudaLaunchAttribute attr[1];
+    if (h->mode != SFAR_LAUNCH_PLAIN) {
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+    }
+    void *args[] = {&g};
+    int cur = -1;
+    cudaGetDevice(&cur);
+    if (cur != h->dev)
+        cudaSetDevice(h->dev);
+    cudaError_t err = cudaLaunchKernelExC(&cfg, sfar_kernel_gemv(), args);
+    if (cur != h->dev && cur >= 0)
+        cudaSetDevice(cur);
+    if (err != cudaSuccess) {
+        cudaGetLastError();
+        return SFAR_ERR_CUDA;
+    }
+    return SFAR_OK;
 }
 
 sfar_status sfar_status_get(sfar_t *h, sfar_fault *info)

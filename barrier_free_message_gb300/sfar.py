@@ -72,6 +72,8 @@ _SIGS = [
     ("sfar_set_launch_mode", ctypes.c_int, [ctypes.c_void_p, ctypes.c_int]),
     ("sfar_test_set_geometry", ctypes.c_int, [ctypes.c_void_p, ctypes.c_int, ctypes.c_int]),
     ("sfar_test_set_trace", ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_uint32]),
+    ("sfar_rowpar_gemv", ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                                        ctypes.c_size_t, ctypes.c_size_t, ctypes.c_size_t, ctypes.c_void_p]),
     ("sfar_test_query_norm_launch", ctypes.c_int, [ctypes.c_void_p, ctypes.c_size_t, ctypes.c_size_t, ctypes.c_int,
                                                    ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_int),
                                                    ctypes.POINTER(ctypes.c_int)]),
@@ -148,6 +150,11 @@ def sfar_add_rmsnorm(h, a_ptrs, res_ptrs, weight_ptr: int, out_ptrs, res_out_ptr
                      eps: float, stream=None) -> int:
     return lib().sfar_add_rmsnorm(h, _ptr_array(a_ptrs), _ptr_array(res_ptrs), int(weight_ptr),
                                   _ptr_array(out_ptrs), _ptr_array(res_out_ptrs), rows, hidden, eps, _stream(stream))
+
+
+def sfar_rowpar_gemv(h, x_ptrs, w_ptrs, y_ptrs, k: int, hidden: int, prefetch_rows: int = 0, stream=None) -> int:
+    return lib().sfar_rowpar_gemv(h, _ptr_array(x_ptrs), _ptr_array(w_ptrs), _ptr_array(y_ptrs), k, hidden,
+                                  prefetch_rows, _stream(stream))
 
 
 def sfar_test_query_norm_launch(h, rows: int, hidden: int, allreduce: bool = True):
@@ -259,6 +266,13 @@ class Sfar:
                                 weight.data_ptr(), [t.data_ptr() for t in outs], [t.data_ptr() for t in residual_outs],
                                 rows, hidden, eps, stream)
         _check(code, "sfar_add_rmsnorm")
+
+    def rowpar_gemv(self, x, w, y, prefetch_rows: int = 0, stream=None) -> None:
+        """x: R tensors of k; w: R tensors of k x hidden; y: R tensors of hidden (bf16, on the device)."""
+        k, hidden = w[0].shape[0], w[0].shape[1]
+        code = sfar_rowpar_gemv(self.h, [t.data_ptr() for t in x], [t.data_ptr() for t in w],
+                                [t.data_ptr() for t in y], k, hidden, prefetch_rows, stream)
+        _check(code, "sfar_rowpar_gemv")
 
     def status(self):
         return sfar_status_get(self.h)

@@ -421,8 +421,10 @@ def run_suite(args):
     (R = 2..16, bf16 and fp32, 4-256 MB per rank), the cost of the barriers
     against the rank count (BASELINE vs DB vs LL vs sentinel, 16 KB per rank,
     R = 2..16), the atomic-accumulation two-shot against the two-shot,
-    LL128 and LL protocols (R = 4, 8, 16 over message sizes), and the fused
-    AllReduce + residual add + RMSNorm against the two-kernel pipeline."""
+    LL128 and LL protocols (R = 4, 8, 16 over message sizes), the fused
+    AllReduce + residual add + RMSNorm against the two-kernel pipeline, and
+    a synthetic tensor-parallel decode step (row-parallel projections and
+    their AllReduces) under three launch configurations."""
     _build.build()
     l2 = torch.cuda.get_device_properties(torch.cuda.current_device()).L2_cache_size
     if "latency" in args.suite:
@@ -510,6 +512,92 @@ def run_suite(args):
             print(json.dumps(row), flush=True)
             h.close()
             del xd, rd, od, zd, ad
+    if "decode" in args.suite:
+        # a synthetic tensor-parallel decode step: 80 layers x (attention output
+        # projection, MLP down projection), each a row-parallel projection of
+        # every rank followed by the AllReduce of the partial sums (fused with
+        # the residual add + RMSNorm, or plain LL); random bf16 weights of
+        # 4 distinct layers (2.4 GB, far above L2) cycled over the 80
+        import oracle
+        peaks, _ = measured_peaks()
+        hbm = float(peaks["hbm_gbs"])
+        R, h, layers, distinct, eps, nx = 8, 8192, 80, 4, 1e-5, 8
+        ks = (8192 // R, 28672 // R)
+        g = torch.Generator(device="cuda").manual_seed(90)
+        W = [[[(torch.randn(k, h, generator=g, device="cuda") * 0.02).to(torch.bfloat16) for _ in range(R)]
+              for k in ks] for _ in range(distinct)]
+        X = [[[torch.randn(k, generator=g, device="cuda").to(torch.bfloat16) for _ in range(R)] for _ in range(nx)]
+             for k in ks]
+        calls = 2 * layers
+        part = [[torch.empty(h, dtype=torch.bfloat16, device="cuda") for _ in range(R)] for _ in range(calls)]
+        out = [[torch.empty(h, dtype=torch.bfloat16, device="cuda") for _ in range(R)] for _ in range(calls)]
+        res = [torch.randn(h, generator=g, device="cuda").to(torch.bfloat16) for _ in range(R)]
+        wn = torch.randn(h, generator=g, device="cuda").to(torch.bfloat16)
+        hd = sfar.Sfar(R, 2 * h, "bf16")          # the AllReduces
+        hg = sfar.Sfar(R, 2 * h, "bf16")          # the projections (own launch mode)
+        P = lambda ts: [t.data_ptr() for t in ts]
+        wbytes = layers * R * sum(ks) * h * 2
+        # (projection launch, AllReduce launch, prefetch rows): "serial" = as a
+        # programmatic dependent of the kernel before it
+        configs = (("plain", "plain", 0), ("serial", "serial", 0), ("serial", "serial", 32), ("serial", "plain", 32))
+        for ar in ("fused", "ll"):
+            for gmode, amode, prefetch in configs:
+                hd.set_mode(amode)
+                hg.set_mode(gmode)
+
+                def gemv_call(c):
+                    kind = c % 2
+                    return sfar.sfar_rowpar_gemv(hg.h, P(X[kind][(c // 2) % nx]), P(W[(c // 2) % distinct][kind]),
+                                                 P(part[c]), ks[kind], h, prefetch)
+
+                def ar_call(c):
+                    if ar == "fused":
+                        return sfar.sfar_allreduce_add_rmsnorm(hd.h, P(part[c]), P(res), wn.data_ptr(), P(out[c]),
+                                                               P(res), 1, h, eps)
+                    return sfar.sfar_allreduce(hd.h, P(part[c]), P(out[c]), h, "ll")
+
+                for f in (gemv_call, ar_call):
+                    assert f(0) == sfar.SFAR_OK
+                torch.cuda.synchronize()
+                graph = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(graph):
+                    for c in range(calls):
+                        for f in (gemv_call, ar_call):
+                            code = f(c)
+                            if code != sfar.SFAR_OK:
+                                raise sfar.SfarError(code, "decode capture")
+                for _ in range(2):
+                    graph.replay()
+                torch.cuda.synchronize()
+                reps = 10
+                t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                t0.record()
+                for _ in range(reps):
+                    graph.replay()
+                t1.record()
+                torch.cuda.synchronize()
+                check_status(hd, "decode")
+                us_token = t0.elapsed_time(t1) * 1000.0 / reps
+                # parity sample: call 1 (an MLP down projection) and, for LL, its AllReduce
+                xs1 = np.stack([inputs.to_bits(t.cpu()) for t in X[1][0]])
+                w1 = np.stack([inputs.to_bits(t.cpu()) for t in W[0][1]])
+                got = np.stack([inputs.to_bits(t.cpu()) for t in part[1]])
+                ok = bool(np.array_equal(got, oracle.gemv(xs1, w1)))
+                if ar == "ll":
+                    ok = ok and bool(np.array_equal(np.stack([inputs.to_bits(t.cpu()) for t in out[1]]),
+                                                    oracle.allreduce(got)))
+                print(json.dumps({"suite": "decode", "ar": ar, "projection_launch": gmode, "allreduce_launch": amode,
+                                  "prefetch_rows": prefetch, "R": R,
+                                  "hidden": h, "layers": layers, "calls_per_token": calls,
+                                  "us_per_token": round(us_token, 1),
+                                  "us_per_projection_and_allreduce": round(us_token / calls, 3),
+                                  "weight_bytes_per_token": wbytes,
+                                  "weight_gbs": round(wbytes / us_token / 1e3, 1),
+                                  "frac_of_measured_hbm": round(wbytes / us_token / 1e3 / hbm, 4),
+                                  "bit_exact_sample": ok}), flush=True)
+                del graph
+        hd.close()
+        hg.close()
     if "atomic" in args.suite:
         # the atomic-accumulation two-shot against the flag-line protocols
         for R in (4, 8, 16):
@@ -699,7 +787,7 @@ def main():
     ap.add_argument("--large-r", type=int, default=8)
     ap.add_argument("--large-mb", type=int, default=64)
     ap.add_argument("--large-dtype", choices=["bf16", "fp32"], default="bf16")
-    ap.add_argument("--suite", default="", help="comma list of latency,bandwidth,barriers,atomic,fused: sweeps as JSON lines")
+    ap.add_argument("--suite", default="", help="comma list of latency,bandwidth,barriers,atomic,fused,decode: sweeps as JSON lines")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
     world, rank, _ = dist_setup(args.gpus)

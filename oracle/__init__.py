@@ -44,6 +44,8 @@ def _lib(mutant: int = 0):
         lib.sfar_oracle_add_rmsnorm.argtypes = [ctypes.c_int, ctypes.c_size_t, ctypes.c_size_t, ctypes.c_int, vpp,
                                                 vpp, ctypes.c_void_p, ctypes.c_float, vpp, vpp, ctypes.c_int]
         lib.sfar_oracle_add_rmsnorm.restype = ctypes.c_int
+        lib.sfar_oracle_gemv.argtypes = [ctypes.c_int, ctypes.c_size_t, ctypes.c_size_t, vpp, vpp, vpp]
+        lib.sfar_oracle_gemv.restype = ctypes.c_int
         _libs[mutant] = lib
     return _libs[mutant]
 
@@ -130,3 +132,24 @@ def add_rmsnorm(x: np.ndarray, res: np.ndarray, weight: np.ndarray, eps: float, 
     if rc != 0:
         raise ValueError("oracle rejected the arguments")
     return out, res_out
+
+
+def gemv(x: np.ndarray, W: np.ndarray, mutant: int = 0) -> np.ndarray:
+    """Row-parallel projection of every rank, as defined in ``sfar_oracle.c``.
+    x: [R, k] bf16 bits (uint16); W: [R, k, h] bf16 bits.  Returns [R, h]."""
+    x = np.ascontiguousarray(x)
+    W = np.ascontiguousarray(W)
+    if x.dtype != np.uint16 or W.dtype != np.uint16:
+        raise TypeError("gemv takes bf16 bit patterns (uint16)")
+    if x.ndim != 2 or W.ndim != 3 or W.shape[:2] != x.shape:
+        raise ValueError("x must be [R, k] and W [R, k, h]")
+    R, k = x.shape
+    h = W.shape[2]
+    y = np.empty((R, h), dtype=np.uint16)
+    vp = ctypes.c_void_p * R
+    rc = _lib(mutant).sfar_oracle_gemv(R, k, h, vp(*[x[r].ctypes.data for r in range(R)]),
+                                       vp(*[W[r].ctypes.data for r in range(R)]),
+                                       vp(*[y[r].ctypes.data for r in range(R)]))
+    if rc != 0:
+        raise ValueError("oracle rejected the arguments")
+    return y

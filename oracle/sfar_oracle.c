@@ -380,6 +380,78 @@ int sfar_oracle_add_rmsnorm(int R, size_t rows, size_t h, int dtype, const void 
     return 0;
 }
 
+/* ------------------------------------------------------------------------
+ * The producer of the AllReduce in a tensor-parallel decode layer: the
+ * row-parallel projection (GEMV) of every rank.
+ *
+ * "vLLM distributed inference core" (page 2), section one: with tensor
+ * parallelism each layer's attention output projection and MLP down
+ * projection end in an AllReduce; section three: the compute stream runs
+ * the matrix product, records an event, and the communication stream runs
+ * the AllReduce after it.  Rank r holds the rows of the weight matrix that
+ * match its slice of the input: y_r = x_r W_r, x_r of k elements, W_r of
+ * k x h (row-major), y_r of h elements -- the partial sums the AllReduce
+ * adds.  The pages fix no summation order.  Reading taken (bf16 inputs and
+ * output): every product x[i] * W[i][j] is rounded to binary32 (exact
+ * unless it under- or overflows: the significands have 8 bits); the k rows
+ * are cut into S = 8 segments of c = ceil(k / 8)
+ * consecutive rows (the last ones shorter or empty); within a segment the
+ * products are added to a binary32 accumulator that starts at +0, in row
+ * order; the S segment sums are folded left to right (segment 0 first);
+ * one rounding to bf16.
+ * ------------------------------------------------------------------------ */
+#define ORACLE_GEMV_SEGMENTS 8
+
+static float gemv_column(const uint16_t *x, const uint16_t *W, size_t k, size_t h, size_t j)
+{
+    const size_t c = (k + ORACLE_GEMV_SEGMENTS - 1) / ORACLE_GEMV_SEGMENTS;
+    float P[ORACLE_GEMV_SEGMENTS];
+    for (int sg = 0; sg < ORACLE_GEMV_SEGMENTS; ++sg) {
+        float acc = 0.0f;
+        for (size_t i = (size_t)sg * c; i < (size_t)(sg + 1) * c && i < k; ++i) {
+#if ORACLE_MUTANT == 20
+            const float p = widen_bf16(x[i]) * widen_bf16(W[j * k + i]);     /* mutant: W transposed */
+#else
+            const float p = widen_bf16(x[i]) * widen_bf16(W[i * h + j]);
+#endif
+#if ORACLE_MUTANT == 19
+            if (i + 1 == k) continue;                                        /* mutant: last row dropped */
+#endif
+            acc = acc + p;
+        }
+        P[sg] = acc;
+    }
+#if ORACLE_MUTANT == 18
+    float y = P[ORACLE_GEMV_SEGMENTS - 1];                                   /* mutant: reversed fold */
+    for (int sg = ORACLE_GEMV_SEGMENTS - 2; sg >= 0; --sg)
+        y = y + P[sg];
+#else
+    float y = P[0];
+    for (int sg = 1; sg < ORACLE_GEMV_SEGMENTS; ++sg)
+        y = y + P[sg];
+#endif
+    return y;
+}
+
+/*
+ * sfar_oracle_gemv: for every rank r, y[r][j] = the definition above for
+ * x[r] (k bf16), W[r] (k x h bf16, row-major), j < h.  Host memory owned by
+ * the caller.  Returns 0, or -1 for a bad argument.
+ */
+int sfar_oracle_gemv(int R, size_t k, size_t h, const void *const *x, const void *const *W, void *const *y)
+{
+    if (R < 1 || R > 64 || k == 0 || h == 0 || !x || !W || !y)
+        return -1;
+    for (int r = 0; r < R; ++r) {
+        if (!x[r] || !W[r] || !y[r])
+            return -1;
+        for (size_t j = 0; j < h; ++j)
+            ((uint16_t *)y[r])[j] =
+                narrow_bf16(gemv_column((const uint16_t *)x[r], (const uint16_t *)W[r], k, h, j));
+    }
+    return 0;
+}
+
 /* The two conversions on their own, so that tests can pin them directly. */
 uint16_t sfar_oracle_narrow_bf16(float f) { return narrow_bf16(f); }
 
