@@ -25,7 +25,8 @@
 // Outputs: out[r] = y, res_out[r] = z.
 //
 // Layout: a row is spread over one thread-block cluster of CL CTAs; thread t
-// of cluster CTA c holds in-row vectors c*T + t + j*CL*T (j < 4).  The row
+// of cluster CTA c holds in-row vectors c*T + t + j*CL*T (j < vpt), for B
+// rows at a time (B * vpt <= 4), whose statistics share each round.  The row
 // statistics (the largest |z| as magnitude bits, then the integer S) are
 // reduced within each warp, and every warp stores its partial into its slot
 // in every cluster CTA's shared memory (st.async, distributed shared memory),
@@ -231,6 +232,19 @@ __device__ __forceinline__ void st_async_u64(uint32_t raddr, unsigned long long 
                  "r"(rmbar)
                  : "memory");
 }
+__device__ __forceinline__ void st_async_v4u32(uint32_t raddr, uint4 v, uint32_t rmbar)
+{
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(raddr),
+                 "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w), "r"(rmbar)
+                 : "memory");
+}
+__device__ __forceinline__ void st_async_v2u64(uint32_t raddr, unsigned long long a, unsigned long long b,
+                                               uint32_t rmbar)
+{
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v2.b64 [%0], {%1, %2}, [%3];" ::"r"(raddr),
+                 "l"(a), "l"(b), "r"(rmbar)
+                 : "memory");
+}
 __device__ __forceinline__ void cluster_arrive_relaxed()
 {
     asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
@@ -277,7 +291,7 @@ __device__ __forceinline__ unsigned long long warp_sum_u64(unsigned long long x)
 
 }  // namespace
 
-template <int DT, int RB, bool AR, bool TEST>
+template <int DT, int RB, bool AR, bool TEST, int NB>
 __global__ void __launch_bounds__(SFAR_NORM_THREADS, 1) k_fused(const __grid_constant__ SfarArgs a,
                                                              const __grid_constant__ SfarNormArgs na)
 {
@@ -295,9 +309,9 @@ __global__ void __launch_bounds__(SFAR_NORM_THREADS, 1) k_fused(const __grid_con
     // one slot per (cluster CTA, warp): every warp sends its partial straight
     // to every cluster CTA
     constexpr int WMAX = SFAR_NORM_THREADS / 32;
-    __shared__ __align__(8) unsigned long long s_sum[SFAR_NORM_CLMAX * WMAX];
+    __shared__ __align__(16) unsigned long long s_sum[SFAR_NORM_CLMAX * WMAX][SFAR_NORM_VMAX];
+    __shared__ __align__(16) uint4 s_max[SFAR_NORM_CLMAX * WMAX];
     __shared__ __align__(8) unsigned long long s_mbar[2];      // [0]: row maxima, [1]: row sums
-    __shared__ uint32_t s_max[SFAR_NORM_CLMAX * WMAX];
     const uint32_t mb_max = smem_u32(&s_mbar[0]), mb_sum = smem_u32(&s_mbar[1]);
     const int W = T >> 5, nslots = CL * W, slot = cr * W + warp;
 
@@ -386,100 +400,151 @@ __global__ void __launch_bounds__(SFAR_NORM_THREADS, 1) k_fused(const __grid_con
     uint32_t phase = 0;
 
 
-    // 2. per row: the AllReduce result, z, the row statistics, y
-    for (unsigned long long i = g; i < rows; i += G) {
+    // 2. rows in batches of B: the AllReduce result, z, then the row
+    // statistics of the whole batch in two cluster rounds (each warp sends its
+    // B maxima, then its B sums), then y.  NB = 1: one row, slot q of a thread
+    // is its vector q of the row; NB = 4 (one vector per row and thread): slot
+    // q is row i0 + q*G.
+    const int vpt = na.vpt, B = na.B;
+    for (unsigned long long i0 = g; i0 < rows; i0 += (unsigned long long)G * B) {
         uint4 zv[SFAR_NORM_VMAX], wv[SFAR_NORM_VMAX], rv[SFAR_NORM_VMAX], xv[SFAR_NORM_VMAX];
-        // independent loads first: residual, weight and own input of every vector
+        bool valid[SFAR_NORM_VMAX];
+        unsigned long long vq[SFAR_NORM_VMAX];
+        // independent loads first: residual, weight and own input of every slot
 #pragma unroll
-        for (int j = 0; j < SFAR_NORM_VMAX; ++j) {
-            const unsigned long long u = u0 + j * ustride;
-            zv[j] = wv[j] = rv[j] = xv[j] = make_uint4(0, 0, 0, 0);
-            if (u < VR) {
-                const unsigned long long v = i * VR + u;
+        for (int q = 0; q < SFAR_NORM_VMAX; ++q) {
+            const int bq = NB == 1 ? 0 : q, j = NB == 1 ? q : 0;
+            const unsigned long long i = i0 + (unsigned long long)bq * G, u = u0 + j * ustride;
+            zv[q] = wv[q] = rv[q] = xv[q] = make_uint4(0, 0, 0, 0);
+            valid[q] = bq < B && j < vpt && i < rows && u < VR;
+            vq[q] = i * VR + u;
+            if (valid[q]) {
                 if (i == (unsigned long long)g && j == 0) {
-                    rv[j] = r00;
-                    wv[j] = w00;
-                    xv[j] = x00;
+                    rv[q] = r00;
+                    wv[q] = w00;
+                    xv[q] = x00;
                 } else {
-                    rv[j] = ld_v4((const char *)na.res[r] + v * 16ull);
-                    wv[j] = ld_nc_v4((const char *)na.weight + u * 16ull);
-                    xv[j] = ld_nc_v4((const char *)a.in[r] + v * 16ull);
+                    rv[q] = ld_v4((const char *)na.res[r] + vq[q] * 16ull);
+                    wv[q] = ld_nc_v4((const char *)na.weight + u * 16ull);
+                    xv[q] = ld_nc_v4((const char *)a.in[r] + vq[q] * 16ull);
                 }
             }
         }
-        uint32_t lmax = 0;
+        uint32_t lmax[NB];                                        // per row of the batch
 #pragma unroll
-        for (int j = 0; j < SFAR_NORM_VMAX; ++j) {
-            const unsigned long long u = u0 + j * ustride;
-            if (u < VR && ok) {
-                const unsigned long long v = i * VR + u;
-                const uint4 av = AR ? ll_recv_fold<DT, RB>(a, r, k, e, c.par, v, xv[j], ok) : xv[j];
+        for (int bb = 0; bb < NB; ++bb)
+            lmax[bb] = 0u;
+#pragma unroll
+        for (int q = 0; q < SFAR_NORM_VMAX; ++q) {
+            if (valid[q] && ok) {
+                const uint4 av = AR ? ll_recv_fold<DT, RB>(a, r, k, e, c.par, vq[q], xv[q], ok) : xv[q];
                 float zf[V::N];
 #pragma unroll
                 for (int t = 0; t < V::N; ++t)
-                    zf[t] = __fadd_rn(V::get(av, t), V::get(rv[j], t));
-                zv[j] = V::pack(zf);
+                    zf[t] = __fadd_rn(V::get(av, t), V::get(rv[q], t));
+                zv[q] = V::pack(zf);
+                uint32_t m = 0;
 #pragma unroll
                 for (int t = 0; t < V::N; ++t)
-                    lmax = max(lmax, mag_bits(V::get(zv[j], t)));
+                    m = max(m, mag_bits(V::get(zv[q], t)));
+                lmax[NB == 1 ? 0 : q] = max(lmax[NB == 1 ? 0 : q], m);
             }
         }
-        if (i == (unsigned long long)g)
-            sfar_stamp(c, TP_INPUT);          // first row: AllReduce result and z in registers
-        // row maximum of the magnitude bits: each warp's maximum goes to its
-        // slot in every cluster CTA
-        lmax = __reduce_max_sync(SFAR_FULL, lmax);
+        if (i0 == (unsigned long long)g)
+            sfar_stamp(c, TP_INPUT);          // first batch: AllReduce result and z in registers
+        // row maxima of the magnitude bits: each warp's B maxima go to its slot
+        // in every cluster CTA
+#pragma unroll
+        for (int bb = 0; bb < NB; ++bb)
+            if (bb < B)
+                lmax[bb] = __reduce_max_sync(SFAR_FULL, lmax[bb]);
         if (!cluster_ready) {
             cluster_wait();                    // every peer's mbarriers are initialised
             cluster_ready = true;
         }
         if (tid == 0)
-            mbar_arrive_expect_tx(mb_max, (uint32_t)nslots * 4u);
-        if (lane < CL)
-            st_async_u32(map_cta(smem_u32(&s_max[slot]), lane), lmax, map_cta(mb_max, lane));
+            mbar_arrive_expect_tx(mb_max, (uint32_t)nslots * (NB == 1 ? 4u : 16u));
+        if (lane < CL) {
+            if (NB == 1)
+                st_async_u32(map_cta(smem_u32(&s_max[slot]), lane), lmax[0], map_cta(mb_max, lane));
+            else
+                st_async_v4u32(map_cta(smem_u32(&s_max[slot]), lane),
+                               make_uint4(lmax[0], lmax[NB > 1 ? 1 : 0], lmax[NB > 2 ? 2 : 0], lmax[NB > 3 ? 3 : 0]),
+                               map_cta(mb_max, lane));
+        }
         if (!cluster_mbar_wait(mb_max, phase, a.ctl, r, k, e))
             ok = false;
-        uint32_t M = 0;
-        for (int q = 0; q < nslots; ++q)
-            M = max(M, s_max[q]);
-        // the truncated squares, summed as integers
-        unsigned long long lsum = 0;
-        if (M != 0 && M < 0x7f800000u) {
-            const int E = exp_above(M);
+        uint32_t M[NB];
 #pragma unroll
-            for (int j = 0; j < SFAR_NORM_VMAX; ++j)
-                if (u0 + j * ustride < VR) {
-#pragma unroll
-                    for (int t = 0; t < V::N; ++t)
-                        lsum += sq_term(V::get(zv[j], t), E, na.F);
-                }
+        for (int bb = 0; bb < NB; ++bb)
+            M[bb] = 0u;
+        for (int qs = 0; qs < nslots; ++qs) {
+            const uint4 m4 = s_max[qs];
+            M[0] = max(M[0], m4.x);
+            if (NB > 1) {
+                M[NB > 1 ? 1 : 0] = max(M[NB > 1 ? 1 : 0], m4.y);
+                M[NB > 2 ? 2 : 0] = max(M[NB > 2 ? 2 : 0], m4.z);
+                M[NB > 3 ? 3 : 0] = max(M[NB > 3 ? 3 : 0], m4.w);
+            }
         }
-        lsum = warp_sum_u64(lsum);
+        // the truncated squares of each row, summed as integers
+        unsigned long long lsum[NB];
+#pragma unroll
+        for (int bb = 0; bb < NB; ++bb)
+            lsum[bb] = 0ull;
+#pragma unroll
+        for (int q = 0; q < SFAR_NORM_VMAX; ++q) {
+            const int bq = NB == 1 ? 0 : q;
+            if (valid[q] && M[bq] != 0 && M[bq] < 0x7f800000u) {
+                const int E = exp_above(M[bq]);
+#pragma unroll
+                for (int t = 0; t < V::N; ++t)
+                    lsum[bq] += sq_term(V::get(zv[q], t), E, na.F);
+            }
+        }
+#pragma unroll
+        for (int bb = 0; bb < NB; ++bb)
+            if (bb < B)
+                lsum[bb] = warp_sum_u64(lsum[bb]);
         if (tid == 0)
-            mbar_arrive_expect_tx(mb_sum, (uint32_t)nslots * 8u);
-        if (lane < CL)
-            st_async_u64(map_cta(smem_u32(&s_sum[slot]), lane), lsum, map_cta(mb_sum, lane));
+            mbar_arrive_expect_tx(mb_sum, (uint32_t)nslots * (NB == 1 ? 8u : 32u));
+        if (lane < CL) {
+            if (NB == 1) {
+                st_async_u64(map_cta(smem_u32(&s_sum[slot][0]), lane), lsum[0], map_cta(mb_sum, lane));
+            } else {
+                st_async_v2u64(map_cta(smem_u32(&s_sum[slot][0]), lane), lsum[0], lsum[NB > 1 ? 1 : 0],
+                               map_cta(mb_sum, lane));
+                st_async_v2u64(map_cta(smem_u32(&s_sum[slot][2]), lane), lsum[NB > 2 ? 2 : 0], lsum[NB > 3 ? 3 : 0],
+                               map_cta(mb_sum, lane));
+            }
+        }
         if (!cluster_mbar_wait(mb_sum, phase, a.ctl, r, k, e))
             ok = false;
         phase ^= 1u;
-        unsigned long long S = 0;
-        for (int q = 0; q < nslots; ++q)
-            S += s_sum[q];
-        if (i == (unsigned long long)g)
-            sfar_stamp(c, TP_RECEIVED);       // first row: both cluster reductions done
-        const float ms = mean_square(M, S, h, na.F);
-        const float rstd = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(ms, na.eps)));
+        float rstd[NB];
 #pragma unroll
-        for (int j = 0; j < SFAR_NORM_VMAX; ++j) {
-            const unsigned long long u = u0 + j * ustride;
-            if (u < VR && ok) {
-                const unsigned long long v = i * VR + u;
+        for (int bb = 0; bb < NB; ++bb) {
+            rstd[bb] = 0.f;
+            if (bb >= B)
+                continue;
+            unsigned long long S = 0;
+            for (int qs = 0; qs < nslots; ++qs)
+                S += s_sum[qs][bb];
+            const float ms = mean_square(M[bb], S, h, na.F);
+            rstd[bb] = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(ms, na.eps)));
+        }
+        if (i0 == (unsigned long long)g)
+            sfar_stamp(c, TP_RECEIVED);       // first batch: both cluster rounds done
+#pragma unroll
+        for (int q = 0; q < SFAR_NORM_VMAX; ++q) {
+            if (valid[q] && ok) {
+                const float rs = rstd[NB == 1 ? 0 : q];
                 float yf[V::N];
 #pragma unroll
                 for (int t = 0; t < V::N; ++t)
-                    yf[t] = __fmul_rn(__fmul_rn(V::get(zv[j], t), rstd), V::get(wv[j], t));
-                st_v4((char *)na.res_out[r] + v * 16ull, zv[j]);
-                st_v4((char *)a.out[r] + v * 16ull, V::pack(yf));
+                    yf[t] = __fmul_rn(__fmul_rn(V::get(zv[q], t), rs), V::get(wv[q], t));
+                st_v4((char *)na.res_out[r] + vq[q] * 16ull, zv[q]);
+                st_v4((char *)a.out[r] + vq[q] * 16ull, V::pack(yf));
             }
         }
     }
@@ -494,16 +559,19 @@ __global__ void __launch_bounds__(SFAR_NORM_THREADS, 1) k_fused(const __grid_con
     }
 }
 
-const void *sfar_kernel_fused(int dt, int wide, int allreduce, int test)
+const void *sfar_kernel_fused(int dt, int wide, int allreduce, int test, int batch)
 {
     if (!allreduce)
         wide = test = 0;            // the normalisation alone neither receives nor reads knobs
-#define SFAR_PICK(D, W, A, T)                                                    \
-    if (dt == D && wide == W && allreduce == A && test == T)                    \
-        return (const void *)k_fused<D, (W ? 16 : 8), (A != 0), (T != 0)>;
-    SFAR_PICK(0, 0, 1, 0) SFAR_PICK(0, 0, 1, 1) SFAR_PICK(0, 1, 1, 0) SFAR_PICK(0, 1, 1, 1)
-    SFAR_PICK(1, 0, 1, 0) SFAR_PICK(1, 0, 1, 1) SFAR_PICK(1, 1, 1, 0) SFAR_PICK(1, 1, 1, 1)
-    SFAR_PICK(0, 0, 0, 0) SFAR_PICK(1, 0, 0, 0)
+    const int nb = batch > 1 ? 4 : 1;
+#define SFAR_PICK(D, W, A, T, N)                                                       \
+    if (dt == D && wide == W && allreduce == A && test == T && nb == N)               \
+        return (const void *)k_fused<D, (W ? 16 : 8), (A != 0), (T != 0), N>;
+#define SFAR_PICK_NB(D, W, A, T) SFAR_PICK(D, W, A, T, 1) SFAR_PICK(D, W, A, T, 4)
+    SFAR_PICK_NB(0, 0, 1, 0) SFAR_PICK_NB(0, 0, 1, 1) SFAR_PICK_NB(0, 1, 1, 0) SFAR_PICK_NB(0, 1, 1, 1)
+    SFAR_PICK_NB(1, 0, 1, 0) SFAR_PICK_NB(1, 0, 1, 1) SFAR_PICK_NB(1, 1, 1, 0) SFAR_PICK_NB(1, 1, 1, 1)
+    SFAR_PICK_NB(0, 0, 0, 0) SFAR_PICK_NB(1, 0, 0, 0)
+#undef SFAR_PICK_NB
 #undef SFAR_PICK
     return nullptr;
 }

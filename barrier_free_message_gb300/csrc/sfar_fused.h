@@ -16,8 +16,12 @@ struct SfarNormArgs {
     int G;                        // clusters per rank (rows g, g + G, ...)
     int CL;                       // CTAs per cluster: a row is spread over one cluster
     int F;                        // fixed-point fraction bits of the sum of squares
+    int vpt;                      // vectors of a row per thread: ceil(hidden vectors / (CL * threads))
+    int B;                        // rows per statistics round: 1, or up to 4 when vpt == 1
 };
 
 // dt: 0 bf16, 1 fp32; wide: R > 8; allreduce: 1 = AllReduce over LL packets
-// first, 0 = the normalisation of a given AllReduce result; test: knobs.
-const void *sfar_kernel_fused(int dt, int wide, int allreduce, int test);
+// first, 0 = the normalisation of a given AllReduce result; test: knobs;
+// batch: rows per statistics round (1, or up to 4 when every thread holds one
+// vector of each row).
+const void *sfar_kernel_fused(int dt, int wide, int allreduce, int test, int batch);

@@ -66,8 +66,8 @@ struct sfar {
     int tma_tb = 0, tma_ns = 0;
     size_t tma_smem = 0;
     // fused normalisation: co-resident clusters per launch shape, queried once
-    // ([allreduce][test][cluster size][threads index], 0 = not yet known)
-    int norm_clusters[2][2][SFAR_NORM_CLMAX + 1][4] = {};
+    // ([allreduce][test][batched][cluster size][threads index], 0 = not yet known)
+    int norm_clusters[2][2][2][SFAR_NORM_CLMAX + 1][4] = {};
 };
 
 static const void *kernel_for(const sfar *h, int p, int test)
@@ -583,9 +583,9 @@ static bool norm_shape(unsigned long long VR, int *CL, int *CLmin, int *ti)
     return *CLmin <= cl;
 }
 
-static int norm_max_clusters(sfar *h, int allreduce, int test, int CL, int ti)
+static int norm_max_clusters(sfar *h, int allreduce, int test, int batch, int CL, int ti)
 {
-    int &slot = h->norm_clusters[allreduce][test][CL][ti];
+    int &slot = h->norm_clusters[allreduce][test][batch > 1 ? 1 : 0][CL][ti];
     if (slot)
         return slot;
     cudaLaunchConfig_t cfg;
@@ -600,7 +600,7 @@ static int norm_max_clusters(sfar *h, int allreduce, int test, int CL, int ti)
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, sfar_kernel_fused(h->dt, h->R > 8, allreduce, test), &cfg) !=
+    if (cudaOccupancyMaxActiveClusters(&n, sfar_kernel_fused(h->dt, h->R > 8, allreduce, test, batch), &cfg) !=
         cudaSuccess) {
         cudaGetLastError();
         return -1;
@@ -610,10 +610,12 @@ static int norm_max_clusters(sfar *h, int allreduce, int test, int CL, int ti)
 }
 
 // Launch shape of a fused call: threads per CTA, cluster size (shrunk from
-// the preferred one while R clusters cannot be resident at once) and
-// clusters per rank G (one row per cluster at a time, K = G * CL <= KMAX).
+// the preferred one while R clusters cannot be resident at once), clusters
+// per rank G (K = G * CL <= KMAX), vectors of a row per thread, and rows per
+// statistics round (up to 4 when every thread holds one vector of each row
+// and a cluster gets more than one row).
 static sfar_status norm_geometry(sfar *h, int allreduce, int test, size_t rows, unsigned long long VR, int *CL_out,
-                                 int *G_out, int *threads_out)
+                                 int *G_out, int *threads_out, int *vpt_out, int *batch_out)
 {
     int CL = 0, CLmin = 0, ti = 0;
     if (!norm_shape(VR, &CL, &CLmin, &ti))
@@ -622,9 +624,11 @@ static sfar_status norm_geometry(sfar *h, int allreduce, int test, size_t rows, 
     cudaGetDevice(&cur);
     if (cur != h->dev)
         cudaSetDevice(h->dev);
-    int maxc = -1;
+    int maxc = -1, vpt = 1, nb = 1;
     for (; CL >= CLmin; --CL) {
-        maxc = norm_max_clusters(h, allreduce, test, CL, ti);
+        vpt = (int)ceil_div(VR, (size_t)CL * kNormThreads[ti]);
+        nb = (vpt == 1 && rows > 1) ? 4 : 1;
+        maxc = norm_max_clusters(h, allreduce, test, nb, CL, ti);
         if (maxc < 0 || maxc >= h->R)
             break;
     }
@@ -641,9 +645,14 @@ static sfar_status norm_geometry(sfar *h, int allreduce, int test, size_t rows, 
         G = rows;
     if (G < 1)
         G = 1;
+    size_t B = nb;
+    if (B > ceil_div(rows, G))
+        B = ceil_div(rows, G);                    // no more rows per round than a cluster gets
     *CL_out = CL;
     *G_out = (int)G;
     *threads_out = kNormThreads[ti];
+    *vpt_out = vpt;
+    *batch_out = (int)B;
     return SFAR_OK;
 }
 
@@ -700,8 +709,8 @@ static sfar_status fused_call(sfar *h, const void *const in[], const void *const
         }
     }
     const int test = allreduce && (h->k_strag || h->k_drop || h->k_single) ? 1 : 0;
-    int CL = 0, G = 0, threads = 0;
-    const sfar_status gst = norm_geometry(h, allreduce, test, rows, VR, &CL, &G, &threads);
+    int CL = 0, G = 0, threads = 0, vpt = 1, batch = 1;
+    const sfar_status gst = norm_geometry(h, allreduce, test, rows, VR, &CL, &G, &threads, &vpt, &batch);
     if (gst != SFAR_OK)
         return gst;
     const int K = G * CL;
@@ -734,6 +743,8 @@ static sfar_status fused_call(sfar *h, const void *const in[], const void *const
     na.eps = eps;
     na.G = (int)G;
     na.CL = CL;
+    na.vpt = vpt;
+    na.B = batch;
     int c = 0;
     while (((size_t)1 << c) < hidden)
         ++c;
@@ -779,7 +790,7 @@ static sfar_status fused_call(sfar *h, const void *const in[], const void *const
     void *args[] = {&a, &na};
     if (cur != h->dev)
         cudaSetDevice(h->dev);
-    cudaError_t err = cudaLaunchKernelExC(&cfg, sfar_kernel_fused(h->dt, R > 8, allreduce, test), args);
+    cudaError_t err = cudaLaunchKernelExC(&cfg, sfar_kernel_fused(h->dt, R > 8, allreduce, test, batch), args);
     if (cur != h->dev && cur >= 0)
         cudaSetDevice(cur);
     if (err != cudaSuccess) {
@@ -797,8 +808,8 @@ sfar_status sfar_test_query_norm_launch(sfar_t *h, size_t rows, size_t hidden, i
     const unsigned long long VR = hidden * (size_t)h->es / 16;
     if (VR > 8192 || (h->R > 8 && VR > 4096))
         return SFAR_ERR_INVALID;
-    int CL = 0, G = 0, threads = 0;
-    const sfar_status st = norm_geometry(h, allreduce ? 1 : 0, 0, rows, VR, &CL, &G, &threads);
+    int CL = 0, G = 0, threads = 0, vpt = 1, batch = 1;
+    const sfar_status st = norm_geometry(h, allreduce ? 1 : 0, 0, rows, VR, &CL, &G, &threads, &vpt, &batch);
     if (st != SFAR_OK)
         return st;
     if (ctas_per_rank)
