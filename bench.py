@@ -477,6 +477,8 @@ def run_suite(args):
         # pipeline (LL AllReduce, then the normalisation kernel)
         import oracle
         for R, rows, hidden in ((8, 1, 8192), (8, 64, 7168), (4, 1, 8192), (16, 1, 8192), (8, 4, 8192)):
+            if args.suite_r and R != args.suite_r:
+                continue
             calls, eps = 32, 1e-5
             n = rows * hidden
             x = torch.stack([inputs.draw(6, c, R, n, "normal", 1.0, "bf16") for c in range(calls)])
@@ -523,7 +525,7 @@ def run_suite(args):
         import oracle
         peaks, _ = measured_peaks()
         hbm = float(peaks["hbm_gbs"])
-        R, h, layers, distinct, eps, nx = 8, 8192, 80, 4, 1e-5, 8
+        R, h, layers, distinct, eps, nx = 8, 8192, args.decode_layers, 4, 1e-5, 8
         ks = (8192 // R, 28672 // R)
         g = torch.Generator(device="cuda").manual_seed(90)
         W = [[[(torch.randn(k, h, generator=g, device="cuda") * 0.02).to(torch.bfloat16) for _ in range(R)]
@@ -603,8 +605,12 @@ def run_suite(args):
     if "atomic" in args.suite:
         # the atomic-accumulation two-shot against the flag-line protocols
         for R in (4, 8, 16):
+            if args.suite_r and R != args.suite_r:
+                continue
             h = sfar.Sfar(R, 1 << 20, "bf16")
             for b in inputs.SWEEP_BYTES:
+                if args.suite_bytes and b != args.suite_bytes:
+                    continue
                 n, calls = b // 2, 32
                 x = torch.stack([inputs.draw(5, c, R, n, "normal", 1.0, "bf16") for c in range(calls)])
                 xd = x.cuda()
@@ -814,6 +820,9 @@ def main():
     ap.add_argument("--large-r", type=int, default=8)
     ap.add_argument("--large-mb", type=int, default=64)
     ap.add_argument("--large-dtype", choices=["bf16", "fp32"], default="bf16")
+    ap.add_argument("--suite-r", type=int, default=0, help="atomic and fused suites: only this rank count")
+    ap.add_argument("--suite-bytes", type=int, default=0, help="atomic suite: only this message size per rank")
+    ap.add_argument("--decode-layers", type=int, default=80, help="decode suite: layers per token")
     ap.add_argument("--suite", default="", help="comma list of latency,bandwidth,barriers,atomic,fused,decode: sweeps as JSON lines")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
