@@ -60,7 +60,7 @@ __global__ void __launch_bounds__(SFAR_THREADS) k_db(const __grid_constant__ Sfa
     const unsigned long long v0 = (unsigned long long)k * blockDim.x + threadIdx.x;
     if (v0 * 16ull < nbytes)
         prefetch_l2((const char *)a.in[r] + v0 * 16ull);
-    const SfarEntry ent = sfar_entry(a);
+    const SfarEntry ent = sfar_entry<true>(a);     // early ticket (see sfar_entry)
     const uint4 x0 = load_vec<ES>(a.in[r], v0, nbytes);     // before the prologue's barrier
     SfarCall c;
     if (!sfar_prologue<TEST>(a, r, k, c, ent))

@@ -140,24 +140,52 @@ __device__ __forceinline__ void prefetch_l2(const void *p)
 // programmatic-launch wait returned.  Recorded only when tracing is armed.
 struct SfarEntry {
     unsigned long long t_entry, t_start;
+    unsigned long long ticket;    // serial mode, thread 0: the rank counter before this CTA's add
+    bool have_ticket;
 };
+
+__device__ __forceinline__ unsigned long long sfar_take_ticket(const SfarArgs &a, int r, int k)
+{
+    // Every CTA of rank r adds to the rank's call counter: CTA 0 adds
+    // SFAR_KMAX - K + 1, the others 1, so each call adds exactly SFAR_KMAX and
+    // every CTA of call c (counted from 0) receives a value in
+    // [c * SFAR_KMAX, (c + 1) * SFAR_KMAX) whatever the order of the atomics:
+    // all CTAs agree on the epoch c + 1, and the epoch is the same for every
+    // launch geometry.
+    const unsigned long long add = k == 0 ? (unsigned long long)(SFAR_KMAX - a.K + 1) : 1ull;
+    return atomicAdd(a.epoch + r, add);
+}
 
 // First statement of every AllReduce kernel.  In serial mode the kernel is
 // launched as a programmatic dependent of the previous kernel on the stream
 // and waits here for its predecessor to complete, so it sees exactly what
 // plain stream order would show it; the prologue then lets its own successor
 // be scheduled once every CTA holds its ticket, so the successor's launch
-// overlaps this kernel's work while at most one launched kernel waits.  In
-// overlap mode the kernel does not wait (the prologue hands off inside one
-// rank instead).
+// overlaps this kernel's work while at most one launched kernel waits.
+// With EARLY, thread 0 takes its ticket before the wait: the predecessor
+// lets this kernel launch only after every one of its CTAs has received its
+// own ticket, and nothing else touches the counters (sfar_reset clears them
+// with plain stream order), so the atomic's round trip overlaps the wait.
+// Measured on GB300 (R = 8, 16 KB): DB 4.48 -> 4.20 us, BASELINE 6.04 ->
+// 5.85, sentinel 3.21 -> 3.14, LL128 4.85 -> 4.83, but LL 3.20 -> 3.39 (its
+// successor then launches earlier, into its receive), so each kernel chooses.
+// In overlap mode the kernel does not wait (the prologue hands off inside
+// one rank instead) and the prologue takes the ticket.
+template <bool EARLY = false>
 __device__ __forceinline__ SfarEntry sfar_entry(const SfarArgs &a)
 {
-    SfarEntry t{0, 0};
+    SfarEntry t{0, 0, 0, false};
     const bool tr = a.trace != nullptr && threadIdx.x == 0;
     if (tr)
         t.t_entry = globaltimer();
-    if (!a.overlap)
+    if (!a.overlap) {
+        if (EARLY && threadIdx.x == 0) {
+            const int r = blockIdx.x / a.K;
+            t.ticket = sfar_take_ticket(a, r, blockIdx.x - r * a.K);
+            t.have_ticket = true;
+        }
         pdl_wait();
+    }
     if (tr)
         t.t_start = globaltimer();
     return t;
@@ -270,17 +298,13 @@ __device__ __forceinline__ bool sfar_prologue(const SfarArgs &a, int r, int k, S
     __shared__ int s_flags;
     c.trace = nullptr;
     if (threadIdx.x == 0) {
-        // Ticket.  Every CTA of rank r adds to the rank's call counter: CTA 0
-        // adds SFAR_KMAX - K + 1, the others 1, so each call adds exactly
-        // SFAR_KMAX and every CTA of call c (counted from 0) receives a value
-        // in [c * SFAR_KMAX, (c + 1) * SFAR_KMAX) whatever the order of the
-        // atomics: all CTAs agree on the epoch c + 1, and the epoch is the
-        // same for every launch geometry.  Calls never interleave their
-        // tickets (stream order, or in overlap mode the launch of the next
-        // call after every CTA of this one holds its ticket).  The latency
-        // overlaps the input load the caller issued just before.
-        const unsigned long long add = k == 0 ? (unsigned long long)(SFAR_KMAX - a.K + 1) : 1ull;
-        const uint32_t e = (uint32_t)(atomicAdd(a.epoch + r, add) / SFAR_KMAX) + 1u;
+        // Ticket (sfar_take_ticket).  Calls never interleave their tickets
+        // (stream order, or the launch of the next call after every CTA of
+        // this one holds its ticket).  In serial mode it was taken before the
+        // programmatic-launch wait; in overlap mode its latency overlaps the
+        // input load the caller issued just before.
+        const unsigned long long tk = t.have_ticket ? t.ticket : sfar_take_ticket(a, r, k);
+        const uint32_t e = (uint32_t)(tk / SFAR_KMAX) + 1u;
         int flags = ld_relaxed_s32(&a.ctl->status) != 0 ? 1 : 0;
         if (TEST) {
             const volatile SfarCtl *ctl = a.ctl;
