@@ -34,12 +34,13 @@
 //   1. Every rank adds each of its valid elements into the owners' lines
 //      (all R owners, itself included), fences once per warp, then adds 1 to
 //      each of those lines' counters.
-//   2. Owner r waits for counter == R on each of its lines, reads the sums,
-//      rounds them once, writes its own output and every peer's all-gather
-//      line, and clears the accumulator line (data and counter) for the next
-//      use of this parity; then fences and sets the all-gather flags to e.
-//   3. Every rank polls the all-gather flags of the other owners (all owners
-//      at once, lane j on owner j) and copies the results to its output.
+//   2. Owner r waits for counter == R on all of a warp's lines at once, then
+//      line by line reads the sums, rounds them once, writes its own output
+//      and every peer's all-gather line, and clears the accumulator line (data
+//      and counter) for the next use of this parity; then fences and sets the
+//      all-gather flags to e.
+//   3. Every rank polls the all-gather flags of every (owner, line) pair of
+//      the warp at once and copies the results to its output.
 // Reuse: a line of parity e & 1 is added to again at epoch e + 2.  A rank
 // starts epoch e + 2 only after it finished epoch e + 1, which needed every
 // owner's epoch e + 1 all-gather lines, which each owner sends only after
@@ -97,7 +98,7 @@ __device__ __forceinline__ void store_elem(void *base, unsigned long long idx, u
 }
 
 template <int DT, int RB, bool TEST>
-__global__ void __launch_bounds__(SFAR_THREADS) k_atomic(const __grid_constant__ SfarArgs a)
+__global__ void __launch_bounds__(SFAR_THREADS, 3) k_atomic(const __grid_constant__ SfarArgs a)
 {
     constexpr int ES = DT == 0 ? 2 : 4;
     const int R = a.R, K = a.K;
@@ -167,16 +168,19 @@ __global__ void __launch_bounds__(SFAR_THREADS) k_atomic(const __grid_constant__
     sfar_stamp(cl, TP_SENT);
     sfar_mid_delay<TEST>(cl);
 
-    // 2. owner: wait for all R contributions, round, all-gather send, clear
+    // 2. owner: wait for all R contributions of every line of this warp at
+    // once (lane m polls the counter of the warp's line m, m + 32, ...), then
+    // round, all-gather send and clear line by line
     bool ok = true;
-    for (unsigned long long it = it0; it < L; it += its) {
-        if (!line_valid(r, it))
-            break;
-        float *line = acc_line(r, it);
+    unsigned long long nl = 0;          // this warp's lines of owner r
+    while (line_valid(r, it0 + nl * its))
+        ++nl;
+    {
         int lok = 1;
-        if (lane == 0) {
+        for (unsigned long long m = lane; m < nl && lok; m += 32) {
+            const uint32_t *cnt = reinterpret_cast<const uint32_t *>(acc_line(r, it0 + m * its));
             SfarWaiter w;
-            while (ld_relaxed_u32(reinterpret_cast<const uint32_t *>(line)) != (uint32_t)R) {
+            while (ld_relaxed_u32(cnt) != (uint32_t)R) {
                 if (w.tick(a.ctl)) {
                     sfar_record_fault(a.ctl, r, k, -1, e, SFAR_WAIT_COUNTER);
                     lok = 0;
@@ -184,10 +188,12 @@ __global__ void __launch_bounds__(SFAR_THREADS) k_atomic(const __grid_constant__
                 }
             }
         }
-        ok = __shfl_sync(SFAR_FULL, lok, 0) != 0;
-        if (!ok)
-            break;
+        ok = __all_sync(SFAR_FULL, lok) != 0;
         fence_acq_rel_gpu();
+    }
+    for (unsigned long long m = 0; m < nl && ok; ++m) {
+        const unsigned long long it = it0 + m * its;
+        float *line = acc_line(r, it);
         const float s = lane >= 1 ? ld_relaxed_f32(line + lane) : 0.f;
         st_relaxed_u32(reinterpret_cast<uint32_t *>(line + lane), 0u);     // lane 0: the counter
         const uint32_t bits = round_elem<ES>(s);
@@ -205,17 +211,24 @@ __global__ void __launch_bounds__(SFAR_THREADS) k_atomic(const __grid_constant__
     if (ok && !cl.drop) {
         __syncwarp();
         fence_acq_rel_gpu();
-        for (unsigned long long it = it0; it < L && line_valid(r, it); it += its)
+        for (unsigned long long m = 0; m < nl; ++m)
             for (int i = lane; i < R - 1; i += 32)
-                st_relaxed_u32(ag_line(peer_of(r, i), r, it), e);
+                st_relaxed_u32(ag_line(peer_of(r, i), r, it0 + m * its), e);
     }
 
-    // 3. all-gather receive: lane j polls owner peer j's flag, then every
-    // owner's words are read in one round and copied to the output
-    for (unsigned long long it = it0; it < L && ok; it += its) {
+    // 3. all-gather receive: the warp polls the flags of every (owner, line)
+    // pair it will read at once (lane j takes pairs j, j + 32, ...), then
+    // every owner's words of each line are read in one round and copied out
+    unsigned long long na = 0;          // this warp's lines of the widest owner chunk
+    while (it0 + na * its < L)
+        ++na;
+    if (ok) {
         int lok = 1;
-        for (int i = lane; i < R - 1 && lok; i += 32) {
-            const int p = peer_of(r, i);
+        const unsigned long long pairs = na * (unsigned long long)(R - 1);
+        for (unsigned long long q = lane; q < pairs && lok; q += 32) {
+            const unsigned long long m = q / (unsigned long long)(R - 1);
+            const int p = peer_of(r, (int)(q - m * (unsigned long long)(R - 1)));
+            const unsigned long long it = it0 + m * its;
             if (!line_valid(p, it))
                 continue;
             const uint32_t *f = ag_line(r, p, it);
@@ -229,9 +242,10 @@ __global__ void __launch_bounds__(SFAR_THREADS) k_atomic(const __grid_constant__
             }
         }
         ok = __all_sync(SFAR_FULL, lok) != 0;
-        if (!ok)
-            break;
         fence_acq_rel_gpu();
+    }
+    for (unsigned long long m = 0; m < na && ok; ++m) {
+        const unsigned long long it = it0 + m * its;
         uint32_t y[RB];
 #pragma unroll
         for (int q = 0; q < RB; ++q)

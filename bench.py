@@ -389,6 +389,19 @@ def _time_chain(h, x_dev, out_dev, proto, reps=40, warm=3):
     return s.elapsed_time(e) * 1000.0 / (reps * calls)
 
 
+def _oracle_us(fn, budget_s=2.0):
+    """The oracle (CPU, one thread) timed on one call of a suite's workload:
+    µs per call, repeated while under the budget."""
+    t0 = time.perf_counter()
+    n = 0
+    while True:
+        fn()
+        n += 1
+        if time.perf_counter() - t0 > budget_s or n >= 100:
+            break
+    return round((time.perf_counter() - t0) * 1e6 / n, 1)
+
+
 def _time_calls(h, calls, steps, reps=40, warm=3):
     """One graph of `calls` iterations of the call sequence `steps` (each a
     function of the call index returning a status); µs per iteration."""
@@ -513,6 +526,8 @@ def run_suite(args):
             row["allreduce_ll_us"] = round(_time_calls(h, calls, [allreduce]), 3)
             row["norm_alone_us"] = round(_time_calls(h, calls, [norm]), 3)
             row["saved_us"] = round(row["unfused_us"] - row["fused_us"], 3)
+            xb, rb, wb = inputs.to_bits(x[0]), inputs.to_bits(res[0]), inputs.to_bits(w[None, :])[0]
+            row["oracle_us"] = _oracle_us(lambda: oracle.add_rmsnorm(xb, rb, wb, eps, hidden))
             print(json.dumps(row), flush=True)
             h.close()
             del xd, rd, od, zd, ad
@@ -537,6 +552,13 @@ def run_suite(args):
         out = [[torch.empty(h, dtype=torch.bfloat16, device="cuda") for _ in range(R)] for _ in range(calls)]
         res = [torch.randn(h, generator=g, device="cuda").to(torch.bfloat16) for _ in range(R)]
         wn = torch.randn(h, generator=g, device="cuda").to(torch.bfloat16)
+        # the oracle on one attention-output and one down projection of the
+        # workload (plus their AllReduces), per projection + AllReduce
+        xo = [np.stack([inputs.to_bits(t.cpu()) for t in X[kind][0]]) for kind in range(2)]
+        wo = [np.stack([inputs.to_bits(t.cpu()) for t in W[0][kind]]) for kind in range(2)]
+        oracle_us = round(sum(_oracle_us(lambda kind=kind: oracle.allreduce(oracle.gemv(xo[kind], wo[kind])),
+                                         budget_s=0.5) for kind in range(2)) / 2, 1)
+        del xo, wo
         hd = sfar.Sfar(R, 2 * h, "bf16")          # the AllReduces
         hg = sfar.Sfar(R, 2 * h, "bf16")          # the projections (own launch mode)
         P = lambda ts: [t.data_ptr() for t in ts]
@@ -598,7 +620,8 @@ def run_suite(args):
                                   "weight_bytes_per_token": wbytes,
                                   "weight_gbs": round(wbytes / us_token / 1e3, 1),
                                   "frac_of_measured_hbm": round(wbytes / us_token / 1e3 / hbm, 4),
-                                  "bit_exact_sample": ok}), flush=True)
+                                  "bit_exact_sample": ok,
+                                  "oracle_us_per_projection_and_allreduce": oracle_us}), flush=True)
                 del graph
         hd.close()
         hg.close()
@@ -622,6 +645,9 @@ def run_suite(args):
                                           else spot_check(od, x, [0, calls - 1]))
                 k, t = h.launch(n, "ll128_atomic")
                 row["atomic_ctas_per_rank"], row["atomic_threads"] = k, t
+                from oracle import atomic
+                xb, ob = inputs.to_bits(x[0]), inputs.to_bits(od[0, 0].cpu())
+                row["oracle_us"] = _oracle_us(lambda: atomic.check(xb, ob))   # the admissible interval of one call
                 print(json.dumps(row), flush=True)
                 del xd, od
             h.close()
