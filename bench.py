@@ -442,6 +442,11 @@ def run_suite(args):
     their AllReduces) under three launch configurations."""
     _build.build()
     l2 = torch.cuda.get_device_properties(torch.cuda.current_device()).L2_cache_size
+    # the latency floor of this box (empty graph kernel + slowest flag round
+    # trip), measured once: the roofline of the latency-bound suites
+    floor_us = floor_probe()["floor_us"] if {"atomic", "fused"} & set(args.suite.split(",")) else None
+    if floor_us is not None:
+        print(json.dumps({"suite": "floor", "floor_us": round(floor_us, 3)}), flush=True)
     if "latency" in args.suite:
         for R in (4, 8):
             h = sfar.Sfar(R, 1 << 20, "bf16")
@@ -526,6 +531,7 @@ def run_suite(args):
             row["allreduce_ll_us"] = round(_time_calls(h, calls, [allreduce]), 3)
             row["norm_alone_us"] = round(_time_calls(h, calls, [norm]), 3)
             row["saved_us"] = round(row["unfused_us"] - row["fused_us"], 3)
+            row["fused_vs_floor"] = round(row["fused_us"] / floor_us, 3)
             xb, rb, wb = inputs.to_bits(x[0]), inputs.to_bits(res[0]), inputs.to_bits(w[None, :])[0]
             row["oracle_us"] = _oracle_us(lambda: oracle.add_rmsnorm(xb, rb, wb, eps, hidden))
             print(json.dumps(row), flush=True)
@@ -645,6 +651,7 @@ def run_suite(args):
                                           else spot_check(od, x, [0, calls - 1]))
                 k, t = h.launch(n, "ll128_atomic")
                 row["atomic_ctas_per_rank"], row["atomic_threads"] = k, t
+                row["atomic_vs_floor"] = round(row["ll128_atomic"] / floor_us, 3)
                 from oracle import atomic
                 xb, ob = inputs.to_bits(x[0]), inputs.to_bits(od[0, 0].cpu())
                 row["oracle_us"] = _oracle_us(lambda: atomic.check(xb, ob))   # the admissible interval of one call
