@@ -262,3 +262,47 @@ def test_dropped_rank_times_out_and_reset_recovers():
         check(h, x, res, w, hidden, 1e-5, "after reset")
     finally:
         h.close()
+
+
+@pytest.mark.parametrize("phase", [0, 1])
+def test_fused_chain_overlap_with_straggler(phase):
+    """512 graph-chained calls in overlap mode with one rank (rotating) delayed
+    by 0-20 us before its sends (phase 0) or between its sends and receives
+    (phase 1): calls overtake one another across ranks, and the cluster
+    statistics rounds see the skew; every call stays bit-exact."""
+    R, hidden, calls, eps = 8, 8192, 512, 1e-5
+    x = torch.stack([inputs.draw(810, c, R, hidden, "normal", 1.0, "bf16") for c in range(calls)])
+    res = torch.stack([inputs.draw(811, c, R, hidden, "normal", 2.0, "bf16") for c in range(calls)])
+    w = inputs.draw(812, 0, 1, hidden, "normal", 1.0, "bf16")[0]
+    want_y, want_z = oracle.add_rmsnorm(inputs.to_bits(x.transpose(0, 1).reshape(R, calls * hidden)),
+                                        inputs.to_bits(res.transpose(0, 1).reshape(R, calls * hidden)),
+                                        inputs.to_bits(w[None, :])[0], eps, hidden)
+    h = sfar.Sfar(R, 2 * hidden, "bf16")
+    try:
+        h.set_mode("overlap")
+        xd, rd, wd = x.cuda(), res.cuda(), w.cuda()
+        od, zd = torch.empty_like(xd), torch.empty_like(xd)
+        h.allreduce_add_rmsnorm([xd[0, r] for r in range(R)], [rd[0, r] for r in range(R)], wd,
+                                [od[0, r] for r in range(R)], [zd[0, r] for r in range(R)], hidden, eps)
+        torch.cuda.synchronize()
+        g = torch.Generator().manual_seed(813)
+        delays = torch.randint(0, 20001, (calls,), generator=g).to(torch.int32).cuda()
+        assert sfar.sfar_test_set_straggler(h.h, delays.data_ptr(), calls, -1, phase) == sfar.SFAR_OK
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            for c in range(calls):
+                assert sfar.sfar_allreduce_add_rmsnorm(h.h, [xd[c, r].data_ptr() for r in range(R)],
+                                                       [rd[c, r].data_ptr() for r in range(R)], wd.data_ptr(),
+                                                       [od[c, r].data_ptr() for r in range(R)],
+                                                       [zd[c, r].data_ptr() for r in range(R)], 1, hidden,
+                                                       eps) == sfar.SFAR_OK
+        graph.replay()
+        torch.cuda.synchronize()
+        status_ok(h.h, f"straggler phase {phase}")
+        got_y = od.transpose(0, 1).reshape(R, calls * hidden)
+        got_z = zd.transpose(0, 1).reshape(R, calls * hidden)
+        for r in range(R):
+            assert_equal_nan_aware(got_z[r], want_z[r], f"straggler {phase} z rank {r}")
+            assert_equal_nan_aware(got_y[r], want_y[r], f"straggler {phase} y rank {r}")
+    finally:
+        h.close()
