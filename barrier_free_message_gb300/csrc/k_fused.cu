@@ -26,12 +26,13 @@
 //
 // Layout: a row is spread over one thread-block cluster of CL CTAs; thread t
 // of cluster CTA c holds in-row vectors c*T + t + j*CL*T (j < vpt), for B
-// rows at a time (B * vpt <= 4), whose statistics share each round.  The row
+// rows at a time (B = 1, or up to 4 when vpt = 1), whose statistics share
+// each round.  The row
 // statistics (the largest |z| as magnitude bits, then the integer S) are
 // reduced within each warp, and every warp stores its partial into its slot
 // in every cluster CTA's shared memory (st.async, distributed shared memory),
 // which completes bytes on that CTA's mbarrier; each CTA then combines the
-// slots itself.  Two such rounds per row; integer max and sum are
+// slots itself.  Two such rounds per batch of rows; integer max and sum are
 // associative, so the order does not matter.  The G clusters of a rank take
 // rows g, g + G, ...; CTA (r, k), k = g*CL + c, is blockIdx r*K + k with
 // K = G*CL, so the epoch ticket and the LL slots are those of the plain LL
