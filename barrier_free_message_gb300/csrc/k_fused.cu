@@ -335,7 +335,7 @@ __global__ void __launch_bounds__(SFAR_NORM_THREADS, 1) k_fused(const __grid_con
     bool alive = true;
     uint4 x00 = make_uint4(0, 0, 0, 0), r00 = x00, w00 = x00;
     if (AR) {
-        const SfarEntry ent = sfar_entry(a);
+        const SfarEntry ent = sfar_entry<true>(a);     // early ticket (see sfar_entry)
         if (has0)
             x00 = ld_nc_v4((const char *)a.in[r] + v00 * 16ull);
         alive = sfar_prologue<TEST>(a, r, k, c, ent);

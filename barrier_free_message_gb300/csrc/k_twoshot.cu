@@ -30,7 +30,7 @@ template <int DT, int RB, bool TEST>
 __global__ void __launch_bounds__(SFAR_THREADS) k_twoshot(const __grid_constant__ SfarArgs a)
 {
     constexpr int ES = DT == 0 ? 2 : 4;
-    const SfarEntry ent = sfar_entry(a);
+    const SfarEntry ent = sfar_entry<true>(a);     // early ticket (see sfar_entry)
     const int R = a.R, K = a.K;
     const int r = blockIdx.x / K, k = blockIdx.x - r * K;
     SfarCall c;
