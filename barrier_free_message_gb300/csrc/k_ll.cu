@@ -22,40 +22,98 @@
 // Latency: the first input vector is loaded before the prologue's barrier,
 // so its DRAM latency overlaps the epoch ticket; every poll round re-reads
 // all peers that are not ready yet at once, so one round trip covers them all.
+//
+// Half units (HALF, used for R > 8): a thread carries 8 bytes instead of 16,
+// one 16-byte LL line {w0,e,w1,e} per peer at bytes [16v, 16v + 16) of the
+// slot.  Holding R - 1 peers' packets then takes half the registers (15 peers
+// of 32 bytes each throttled the R = 16 kernel), with twice the threads.
 #include "sfar_prims.cuh"
 
-template <int RB>
+template <int RB, bool HALF>
 struct LLSlots {
-    unsigned long long w0[RB], w1[RB], w2[RB], w3[RB];
+    unsigned long long w0[RB], w1[RB], w2[HALF ? 1 : RB], w3[HALF ? 1 : RB];
     __device__ __forceinline__ void load(int q, const uint8_t *src)
     {
         ld_relaxed_v2u64(src, w0[q], w1[q]);
-        ld_relaxed_v2u64(src + 16, w2[q], w3[q]);
+        if (!HALF)
+            ld_relaxed_v2u64(src + 16, w2[HALF ? 0 : q], w3[HALF ? 0 : q]);
     }
     __device__ __forceinline__ bool ready(int q, uint32_t e) const
     {
-        return ll_ready(w0[q], w1[q], w2[q], w3[q], e);
+        if (HALF)
+            return (uint32_t)(w0[q] >> 32) == e && (uint32_t)(w1[q] >> 32) == e;
+        return ll_ready(w0[q], w1[q], w2[HALF ? 0 : q], w3[HALF ? 0 : q], e);
     }
     __device__ __forceinline__ uint4 data(int q) const
     {
-        return make_uint4((uint32_t)w0[q], (uint32_t)w1[q], (uint32_t)w2[q], (uint32_t)w3[q]);
+        if (HALF)
+            return make_uint4((uint32_t)w0[q], (uint32_t)w1[q], 0u, 0u);
+        return make_uint4((uint32_t)w0[q], (uint32_t)w1[q], (uint32_t)w2[HALF ? 0 : q], (uint32_t)w3[HALF ? 0 : q]);
     }
 };
 
-template <int DT, int RB, bool TEST>
+// 8 bytes of a rank's input as the low half of a vector (bytes past nbytes
+// read as zero, element by element), and the store of such a half.
+template <int ES>
+__device__ __forceinline__ uint4 load_half(const void *base, unsigned long long v, unsigned long long nbytes)
+{
+    const unsigned long long off = v * 8ull;
+    uint32_t w0 = 0, w1 = 0;
+    if (off + 8ull <= nbytes) {
+        asm volatile("ld.global.nc.v2.u32 {%0,%1}, [%2];" : "=r"(w0), "=r"(w1) : "l"((const char *)base + off));
+    } else if (off < nbytes) {
+        const int rem = (int)(nbytes - off);
+        if (ES == 4) {
+            w0 = *(const uint32_t *)((const char *)base + off);
+        } else {
+            const uint16_t *q = (const uint16_t *)((const char *)base + off);
+            w0 = q[0];
+            if (rem > 2) w0 |= (uint32_t)q[1] << 16;
+            if (rem > 4) w1 = q[2];
+        }
+    }
+    return make_uint4(w0, w1, 0u, 0u);
+}
+
+template <int ES>
+__device__ __forceinline__ void store_half(void *base, unsigned long long v, unsigned long long nbytes, uint4 x)
+{
+    const unsigned long long off = v * 8ull;
+    if (off + 8ull <= nbytes) {
+        st_v2u32((char *)base + off, x.x, x.y);
+        return;
+    }
+    if (off >= nbytes)
+        return;
+    const int rem = (int)(nbytes - off);
+    if (ES == 4) {
+        *(uint32_t *)((char *)base + off) = x.x;
+    } else {
+        uint16_t *q = (uint16_t *)((char *)base + off);
+        q[0] = (uint16_t)x.x;
+        if (rem > 2) q[1] = (uint16_t)(x.x >> 16);
+        if (rem > 4) q[2] = (uint16_t)x.y;
+    }
+}
+
+template <int DT, int RB, bool TEST, bool HALF>
 __global__ void __launch_bounds__(SFAR_THREADS) k_ll(const __grid_constant__ SfarArgs a)
 {
     constexpr int ES = DT == 0 ? 2 : 4;
+    constexpr unsigned long long UB = HALF ? 8ull : 16ull;      // input bytes per unit
     const int R = a.R, K = a.K;
     const int r = blockIdx.x / K, k = blockIdx.x - r * K;
     const unsigned long long nbytes = a.n * ES;
-    const unsigned long long nvec = (nbytes + 15ull) >> 4;
+    const unsigned long long nvec = (nbytes + UB - 1ull) / UB;
     const unsigned long long stride = (unsigned long long)K * blockDim.x;
     const unsigned long long v0 = (unsigned long long)k * blockDim.x + threadIdx.x;
-    if (v0 * 16ull < nbytes)
-        prefetch_l2((const char *)a.in[r] + v0 * 16ull);
+    auto load_unit = [&](unsigned long long v) {
+        return HALF ? load_half<ES>(a.in[r], v, nbytes) : load_vec<ES>(a.in[r], v, nbytes);
+    };
+    if (v0 * UB < nbytes)
+        prefetch_l2((const char *)a.in[r] + v0 * UB);
     const SfarEntry ent = sfar_entry(a);
-    const uint4 x0 = load_vec<ES>(a.in[r], v0, nbytes);     // zero past the end
+    const uint4 x0 = load_unit(v0);                         // zero past the end
     SfarCall c;
     if (!sfar_prologue<TEST>(a, r, k, c, ent))
         return;
@@ -67,15 +125,16 @@ __global__ void __launch_bounds__(SFAR_THREADS) k_ll(const __grid_constant__ Sfa
     // send: pack each input vector once, store it into every peer's slot r
     if (!c.drop) {
         for (unsigned long long v = v0; v < nvec; v += stride) {
-            const uint4 x = v == v0 ? x0 : load_vec<ES>(a.in[r], v, nbytes);
+            const uint4 x = v == v0 ? x0 : load_unit(v);
             const unsigned long long p0 = x.x | eh, p1 = x.y | eh, p2 = x.z | eh, p3 = x.w | eh;
 #pragma unroll
             for (int i = 0; i < RB - 1; ++i) {
                 if (i < R - 1) {
                     const int p = peer_of(r, i);
-                    uint8_t *dst = a.region + ((size_t)(p * 2 + c.par) * R + r) * slot + v * 32ull;
+                    uint8_t *dst = a.region + ((size_t)(p * 2 + c.par) * R + r) * slot + v * 2ull * UB;
                     st_relaxed_v2u64(dst, p0, p1);
-                    st_relaxed_v2u64(dst + 16, p2, p3);
+                    if (!HALF)
+                        st_relaxed_v2u64(dst + 16, p2, p3);
                 }
             }
         }
@@ -87,14 +146,14 @@ __global__ void __launch_bounds__(SFAR_THREADS) k_ll(const __grid_constant__ Sfa
     const uint8_t *mine = a.region + (size_t)(r * 2 + c.par) * R * slot;
     bool ok = true;
     for (unsigned long long v = v0; v < nvec && ok; v += stride) {
-        const uint4 own = v == v0 ? x0 : load_vec<ES>(a.in[r], v, nbytes);
-        LLSlots<RB> s;
+        const uint4 own = v == v0 ? x0 : load_unit(v);
+        LLSlots<RB, HALF> s;
         bool rdy[RB];
 #pragma unroll
         for (int q = 0; q < RB; ++q) {
             rdy[q] = q >= R || q == r;
             if (!rdy[q])
-                s.load(q, mine + (size_t)q * slot + v * 32ull);
+                s.load(q, mine + (size_t)q * slot + v * 2ull * UB);
         }
         SfarWaiter w;
         while (true) {
@@ -120,7 +179,7 @@ __global__ void __launch_bounds__(SFAR_THREADS) k_ll(const __grid_constant__ Sfa
 #pragma unroll
             for (int q = 0; q < RB; ++q)
                 if (!rdy[q])
-                    s.load(q, mine + (size_t)q * slot + v * 32ull);
+                    s.load(q, mine + (size_t)q * slot + v * 2ull * UB);
         }
         if (!ok)
             break;
@@ -130,18 +189,22 @@ __global__ void __launch_bounds__(SFAR_THREADS) k_ll(const __grid_constant__ Sfa
         for (int q = 1; q < RB; ++q)
             if (q < R)
                 acc.add(q == r ? own : s.data(q));
-        store_vec<ES>(a.out[r], v, nbytes, acc.get());
+        if (HALF)
+            store_half<ES>(a.out[r], v, nbytes, acc.get());
+        else
+            store_vec<ES>(a.out[r], v, nbytes, acc.get());
     }
     sfar_stamp(c, TP_RECEIVED);
     sfar_epilogue(a, r, k, e);
     sfar_stamp(c, TP_EXIT);
 }
 
+// wide (R > 8) kernels carry half units
 const void *sfar_kernel_ll(int dt, int wide, int test)
 {
 #define SFAR_PICK(D, W, T)                                   \
     if (dt == D && wide == W && test == T)                  \
-        return (const void *)k_ll<D, (W ? 16 : 8), (T != 0)>;
+        return (const void *)k_ll<D, (W ? 16 : 8), (T != 0), (W != 0)>;
     SFAR_PICK(0, 0, 0) SFAR_PICK(0, 0, 1) SFAR_PICK(0, 1, 0) SFAR_PICK(0, 1, 1)
     SFAR_PICK(1, 0, 0) SFAR_PICK(1, 0, 1) SFAR_PICK(1, 1, 0) SFAR_PICK(1, 1, 1)
 #undef SFAR_PICK
