@@ -29,44 +29,61 @@
 // of 32 bytes each throttled the R = 16 kernel), with twice the threads.
 #include "sfar_prims.cuh"
 
-template <int RB, bool HALF>
+__device__ __forceinline__ void st_relaxed_u64(unsigned long long *p, unsigned long long v)
+{
+    asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+
+// The packets of one unit from every peer: UB / 4 words {data, epoch}.
+template <int RB, int UB>
 struct LLSlots {
-    unsigned long long w0[RB], w1[RB], w2[HALF ? 1 : RB], w3[HALF ? 1 : RB];
+    static constexpr int NW = UB / 4;
+    unsigned long long w[NW][RB];
     __device__ __forceinline__ void load(int q, const uint8_t *src)
     {
-        ld_relaxed_v2u64(src, w0[q], w1[q]);
-        if (!HALF)
-            ld_relaxed_v2u64(src + 16, w2[HALF ? 0 : q], w3[HALF ? 0 : q]);
+        if (NW == 1) {
+            w[0][q] = ld_relaxed_u64(reinterpret_cast<const unsigned long long *>(src));
+        } else {
+            ld_relaxed_v2u64(src, w[0][q], w[NW > 1 ? 1 : 0][q]);
+            if (NW == 4)
+                ld_relaxed_v2u64(src + 16, w[NW > 2 ? 2 : 0][q], w[NW > 3 ? 3 : 0][q]);
+        }
     }
     __device__ __forceinline__ bool ready(int q, uint32_t e) const
     {
-        if (HALF)
-            return (uint32_t)(w0[q] >> 32) == e && (uint32_t)(w1[q] >> 32) == e;
-        return ll_ready(w0[q], w1[q], w2[HALF ? 0 : q], w3[HALF ? 0 : q], e);
+        bool r = true;
+#pragma unroll
+        for (int i = 0; i < NW; ++i)
+            r = r && (uint32_t)(w[i][q] >> 32) == e;
+        return r;
     }
     __device__ __forceinline__ uint4 data(int q) const
     {
-        if (HALF)
-            return make_uint4((uint32_t)w0[q], (uint32_t)w1[q], 0u, 0u);
-        return make_uint4((uint32_t)w0[q], (uint32_t)w1[q], (uint32_t)w2[HALF ? 0 : q], (uint32_t)w3[HALF ? 0 : q]);
+        return make_uint4((uint32_t)w[0][q], NW > 1 ? (uint32_t)w[NW > 1 ? 1 : 0][q] : 0u,
+                          NW > 2 ? (uint32_t)w[NW > 2 ? 2 : 0][q] : 0u, NW > 3 ? (uint32_t)w[NW > 3 ? 3 : 0][q] : 0u);
     }
 };
 
-// 8 bytes of a rank's input as the low half of a vector (bytes past nbytes
-// read as zero, element by element), and the store of such a half.
-template <int ES>
-__device__ __forceinline__ uint4 load_half(const void *base, unsigned long long v, unsigned long long nbytes)
+// UB (8 or 4) bytes of a rank's input as the low words of a vector (bytes
+// past nbytes read as zero, element by element), and the store of such a
+// unit.
+template <int ES, int UB>
+__device__ __forceinline__ uint4 load_part(const void *base, unsigned long long v, unsigned long long nbytes)
 {
-    const unsigned long long off = v * 8ull;
+    const unsigned long long off = v * (unsigned long long)UB;
     uint32_t w0 = 0, w1 = 0;
-    if (off + 8ull <= nbytes) {
-        asm volatile("ld.global.nc.v2.u32 {%0,%1}, [%2];" : "=r"(w0), "=r"(w1) : "l"((const char *)base + off));
+    const char *p = (const char *)base + off;
+    if (off + UB <= nbytes) {
+        if (UB == 8)
+            asm volatile("ld.global.nc.v2.u32 {%0,%1}, [%2];" : "=r"(w0), "=r"(w1) : "l"(p));
+        else
+            asm volatile("ld.global.nc.u32 %0, [%1];" : "=r"(w0) : "l"(p));
     } else if (off < nbytes) {
         const int rem = (int)(nbytes - off);
         if (ES == 4) {
-            w0 = *(const uint32_t *)((const char *)base + off);
+            w0 = *(const uint32_t *)p;
         } else {
-            const uint16_t *q = (const uint16_t *)((const char *)base + off);
+            const uint16_t *q = (const uint16_t *)p;
             w0 = q[0];
             if (rem > 2) w0 |= (uint32_t)q[1] << 16;
             if (rem > 4) w1 = q[2];
@@ -75,32 +92,35 @@ __device__ __forceinline__ uint4 load_half(const void *base, unsigned long long 
     return make_uint4(w0, w1, 0u, 0u);
 }
 
-template <int ES>
-__device__ __forceinline__ void store_half(void *base, unsigned long long v, unsigned long long nbytes, uint4 x)
+template <int ES, int UB>
+__device__ __forceinline__ void store_part(void *base, unsigned long long v, unsigned long long nbytes, uint4 x)
 {
-    const unsigned long long off = v * 8ull;
-    if (off + 8ull <= nbytes) {
-        st_v2u32((char *)base + off, x.x, x.y);
+    const unsigned long long off = v * (unsigned long long)UB;
+    char *p = (char *)base + off;
+    if (off + UB <= nbytes) {
+        if (UB == 8)
+            st_v2u32(p, x.x, x.y);
+        else
+            st_u32(p, x.x);
         return;
     }
     if (off >= nbytes)
         return;
     const int rem = (int)(nbytes - off);
     if (ES == 4) {
-        *(uint32_t *)((char *)base + off) = x.x;
+        *(uint32_t *)p = x.x;
     } else {
-        uint16_t *q = (uint16_t *)((char *)base + off);
+        uint16_t *q = (uint16_t *)p;
         q[0] = (uint16_t)x.x;
         if (rem > 2) q[1] = (uint16_t)(x.x >> 16);
         if (rem > 4) q[2] = (uint16_t)x.y;
     }
 }
 
-template <int DT, int RB, bool TEST, bool HALF>
+template <int DT, int RB, bool TEST, int UB>
 __global__ void __launch_bounds__(SFAR_THREADS) k_ll(const __grid_constant__ SfarArgs a)
 {
     constexpr int ES = DT == 0 ? 2 : 4;
-    constexpr unsigned long long UB = HALF ? 8ull : 16ull;      // input bytes per unit
     const int R = a.R, K = a.K;
     const int r = blockIdx.x / K, k = blockIdx.x - r * K;
     const unsigned long long nbytes = a.n * ES;
@@ -108,7 +128,7 @@ __global__ void __launch_bounds__(SFAR_THREADS) k_ll(const __grid_constant__ Sfa
     const unsigned long long stride = (unsigned long long)K * blockDim.x;
     const unsigned long long v0 = (unsigned long long)k * blockDim.x + threadIdx.x;
     auto load_unit = [&](unsigned long long v) {
-        return HALF ? load_half<ES>(a.in[r], v, nbytes) : load_vec<ES>(a.in[r], v, nbytes);
+        return UB == 16 ? load_vec<ES>(a.in[r], v, nbytes) : load_part<ES, UB == 16 ? 8 : UB>(a.in[r], v, nbytes);
     };
     if (v0 * UB < nbytes)
         prefetch_l2((const char *)a.in[r] + v0 * UB);
@@ -132,9 +152,13 @@ __global__ void __launch_bounds__(SFAR_THREADS) k_ll(const __grid_constant__ Sfa
                 if (i < R - 1) {
                     const int p = peer_of(r, i);
                     uint8_t *dst = a.region + ((size_t)(p * 2 + c.par) * R + r) * slot + v * 2ull * UB;
-                    st_relaxed_v2u64(dst, p0, p1);
-                    if (!HALF)
-                        st_relaxed_v2u64(dst + 16, p2, p3);
+                    if (UB == 4) {
+                        st_relaxed_u64(reinterpret_cast<unsigned long long *>(dst), p0);
+                    } else {
+                        st_relaxed_v2u64(dst, p0, p1);
+                        if (UB == 16)
+                            st_relaxed_v2u64(dst + 16, p2, p3);
+                    }
                 }
             }
         }
@@ -147,7 +171,7 @@ __global__ void __launch_bounds__(SFAR_THREADS) k_ll(const __grid_constant__ Sfa
     bool ok = true;
     for (unsigned long long v = v0; v < nvec && ok; v += stride) {
         const uint4 own = v == v0 ? x0 : load_unit(v);
-        LLSlots<RB, HALF> s;
+        LLSlots<RB, UB> s;
         bool rdy[RB];
 #pragma unroll
         for (int q = 0; q < RB; ++q) {
@@ -189,22 +213,21 @@ __global__ void __launch_bounds__(SFAR_THREADS) k_ll(const __grid_constant__ Sfa
         for (int q = 1; q < RB; ++q)
             if (q < R)
                 acc.add(q == r ? own : s.data(q));
-        if (HALF)
-            store_half<ES>(a.out[r], v, nbytes, acc.get());
-        else
+        if (UB == 16)
             store_vec<ES>(a.out[r], v, nbytes, acc.get());
+        else
+            store_part<ES, UB == 16 ? 8 : UB>(a.out[r], v, nbytes, acc.get());
     }
     sfar_stamp(c, TP_RECEIVED);
     sfar_epilogue(a, r, k, e);
     sfar_stamp(c, TP_EXIT);
 }
 
-// wide (R > 8) kernels carry half units
 const void *sfar_kernel_ll(int dt, int wide, int test)
 {
 #define SFAR_PICK(D, W, T)                                   \
     if (dt == D && wide == W && test == T)                  \
-        return (const void *)k_ll<D, (W ? 16 : 8), (T != 0), (W != 0)>;
+        return (const void *)k_ll<D, (W ? 16 : 8), (T != 0), (W ? SFAR_LL_UNIT_WIDE : SFAR_LL_UNIT_NARROW)>;
     SFAR_PICK(0, 0, 0) SFAR_PICK(0, 0, 1) SFAR_PICK(0, 1, 0) SFAR_PICK(0, 1, 1)
     SFAR_PICK(1, 0, 0) SFAR_PICK(1, 0, 1) SFAR_PICK(1, 1, 0) SFAR_PICK(1, 1, 1)
 #undef SFAR_PICK

@@ -99,16 +99,16 @@ static int thread_index(int threads)
     return -1;
 }
 
-// Work units of a call: 16-byte vectors (one-shot vector protocols; 8-byte
-// halves for LL at R > 8), 4-line groups per warp (LL128, two-shot), lines of
-// a chunk per warp (atomic path), or bytes of a chunk (TMA path).
+// Work units of a call: 16-byte vectors (one-shot vector protocols; the LL
+// kernel's unit for LL), 4-line groups per warp (LL128, two-shot), lines of a
+// chunk per warp (atomic path), or bytes of a chunk (TMA path).
 static size_t work_units(const sfar *h, int p, size_t n, size_t *chunk)
 {
     const size_t nvec = ceil_div(n * (size_t)h->es, 16);
     *chunk = 0;
     switch (p) {
     case SFAR_LL:
-        return h->R > 8 ? ceil_div(n * (size_t)h->es, 8) : nvec;     // R > 8: 8-byte half units
+        return ceil_div(n * (size_t)h->es, h->R > 8 ? SFAR_LL_UNIT_WIDE : SFAR_LL_UNIT_NARROW);
     case SFAR_LL128:
         return ceil_div(nvec, 31);
     case SFAR_TWOSHOT: {

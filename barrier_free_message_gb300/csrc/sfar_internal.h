@@ -12,6 +12,8 @@
 #define SFAR_ITER_BYTES (4 * SFAR_LL128_PAYLOAD)   // payload of the 4 lines one warp moves at once
 #define SFAR_TMA_THREADS 320                // TMA path: 8 consumer warps, a producer and a store warp
 #define SFAR_NTHREAD_OPTS 3                 // receive-buffer kernels: 64, 128 or 256 threads
+#define SFAR_LL_UNIT_NARROW 8               // LL kernel: input bytes per thread for R <= 8 (16, 8 or 4)
+#define SFAR_LL_UNIT_WIDE 8                 // and for R > 8
 
 // Device status block of one handle.  The first 32 bytes are the sticky
 // status and the fault record; the knobs follow.

@@ -112,7 +112,7 @@ sfar_status setup(int dev, cudaStream_t s, unsigned char **out)
             cudaGetLastError();
             return SFAR_ERR_CUDA;
         }
-        const int most = SFAR_NOALLOC_MAX_RANKS * (SFAR_NOALLOC_MAX_BYTES / 16 / kThreads);
+        const int most = SFAR_NOALLOC_MAX_RANKS * (SFAR_NOALLOC_MAX_BYTES / SFAR_LL_UNIT_NARROW / kThreads);
         if (nb * sms < most)
             return SFAR_ERR_UNSUPPORTED;
     }
@@ -175,8 +175,8 @@ extern "C" sfar_status sfar_allreduce_noalloc(const void *const in[], void *cons
         a.in[r] = in[r];
         a.out[r] = out[r];
     }
-    const size_t nvec = (bytes + 15) / 16;
-    const int K = (int)((nvec + kThreads - 1) / kThreads);
+    const size_t units = (bytes + SFAR_LL_UNIT_NARROW - 1) / SFAR_LL_UNIT_NARROW;     // the LL kernel's units
+    const int K = (int)((units + kThreads - 1) / kThreads);
     unsigned char *blk = base + block_offset(R);
     a.n = n;
     a.slot = kSlot;
