@@ -1,578 +1,11 @@
-// k_fused.cu -- one-shot AllReduce over LL packets fused with the residual
-// add and the RMS normalisation that follow it in a decode layer.
-//
-// "vLLM distributed inference core" (page 2), sections one and two: in the
-// decode step the normalisation runs right after the AllReduce of the
-// attention output and of the MLP down projection, on the compute stream,
-// once the AllReduce is complete.  "Every Microsecond Counts" (page 1),
-// section "Unified primitives and API design": the one-shot kernel reduces
-// the received values in registers and writes the result; here the result
-// does not go to memory but straight into the epilogue.
-//
-// What it computes per rank r and row i (h = hidden elements):
-//   a = the AllReduce result, rounded to the element type T (bit for bit the
-//       one-shot LL result);
-//   z = T(a (+) res)                    binary32 add, one rounding;
-//   ms = ldexp(float(S) (/) h, 2E - F), S = sum of z^2 in units of 2^(2E - F)
-//       with each term truncated to a whole unit: E is the exponent of the
-//       smallest power of two above every |z| of the row, F = 53 -
-//       ceil(log2 h), so S is an exact integer below 2^53 -- the same for
-//       every launch geometry and every order of the reduction; float(S) and
-//       the division round once each in binary32; NaN in the row -> NaN,
-//       else inf -> +inf;
-//   rstd = 1 (/) sqrt(ms (+) eps), y = T((z (*) rstd) (*) w), each binary32
-//       operation rounded to nearest even.
-// Outputs: out[r] = y, res_out[r] = z.
-//
-// Layout: a row is spread over one thread-block cluster of CL CTAs; thread t
-// of cluster CTA c holds in-row vectors c*T + t + j*CL*T (j < vpt), for B
-// rows at a time (B = 1, or up to 4 when vpt = 1), whose statistics share
-// each round.  The row
-// statistics (the largest |z| as magnitude bits, then the integer S) are
-// reduced within each warp, and every warp stores its partial into its slot
-// in every cluster CTA's shared memory (st.async, distributed shared memory),
-// which completes bytes on that CTA's mbarrier; each CTA then combines the
-// slots itself.  Two such rounds per batch of rows; integer max and sum are
-// associative, so the order does not matter.  The G clusters of a rank take
-// rows g, g + G, ...; CTA (r, k), k = g*CL + c, is blockIdx r*K + k with
-// K = G*CL, so the epoch ticket and the LL slots are those of the plain LL
-// kernel (receive region [receiver][parity][sender][2 * S bytes]).
-//
-// Every CTA of a cluster sends its statistics on every path: a CTA that
-// finds the handle failed, or a wait that gives up, only skips work.
-#include "sfar_fused.h"
-#include "sfar_prims.cuh"
+// k_fused.cu -- the fused AllReduce + residual add + RMS normalisation with
+// 16-byte units, and the lookup of every variant.
+#include "fused_kernel.cuh"
 
-namespace {
+SFAR_FUSED_TABLE(sfar_kernel_fused_u16, 16)
 
-__device__ __forceinline__ uint32_t mag_bits(float v) { return __float_as_uint(v) & 0x7fffffffu; }
-
-// smallest E with |v| < 2^E for the finite nonzero magnitude bits m
-__device__ __forceinline__ int exp_above(uint32_t m)
+const void *sfar_kernel_fused(int dt, int wide, int allreduce, int test, int batch, int unit)
 {
-    const uint32_t eb = m >> 23;
-    if (eb)
-        return (int)eb - 126;
-    return (31 - __clz((int)m)) - 148;
-}
-
-// floor(v^2 2^(F - 2E)) for finite v with |v| < 2^E: an integer below 2^F,
-// from the binary32 fields (v = m 2^e2), exact
-__device__ __forceinline__ unsigned long long sq_term(float v, int E, int F)
-{
-    const uint32_t b = mag_bits(v);
-    if (b == 0)
-        return 0ull;
-    const uint32_t eb = b >> 23, fr = b & 0x7fffffu;
-    const unsigned long long m = eb ? (fr | 0x800000u) : fr;
-    const int e2 = eb ? (int)eb - 150 : -149;
-    const int sh = 2 * e2 - 2 * E + F;
-    const unsigned long long m2 = m * m;
-    if (sh >= 0)
-        return m2 << sh;
-    return -sh >= 64 ? 0ull : (m2 >> (-sh));
-}
-
-__device__ __forceinline__ float mean_square(uint32_t M, unsigned long long S, unsigned long long h, int F)
-{
-    if (M > 0x7f800000u)
-        return __uint_as_float(0x7fffffffu);
-    if (M == 0x7f800000u)
-        return __uint_as_float(0x7f800000u);
-    if (M == 0)
-        return 0.f;
-    const int E = exp_above(M);
-    return ldexpf(__fdiv_rn(__ull2float_rn(S), (float)h), 2 * E - F);
-}
-
-// element lanes of a 16-byte vector as binary32
-template <int DT> struct Vec;
-template <> struct Vec<0> {
-    static constexpr int N = 8;
-    __device__ __forceinline__ static float get(const uint4 &x, int i)
-    {
-        const uint32_t w = i < 2 ? x.x : i < 4 ? x.y : i < 6 ? x.z : x.w;
-        return __uint_as_float((i & 1) ? (w & 0xffff0000u) : (w << 16));
-    }
-    __device__ __forceinline__ static uint4 pack(const float *f)
-    {
-        uint32_t w[4];
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            const uint32_t lo = __bfloat16_as_ushort(__float2bfloat16_rn(f[2 * q]));
-            const uint32_t hi = __bfloat16_as_ushort(__float2bfloat16_rn(f[2 * q + 1]));
-            w[q] = lo | (hi << 16);
-        }
-        return make_uint4(w[0], w[1], w[2], w[3]);
-    }
-};
-template <> struct Vec<1> {
-    static constexpr int N = 4;
-    __device__ __forceinline__ static float get(const uint4 &x, int i)
-    {
-        return __uint_as_float(i == 0 ? x.x : i == 1 ? x.y : i == 2 ? x.z : x.w);
-    }
-    __device__ __forceinline__ static uint4 pack(const float *f)
-    {
-        return make_uint4(__float_as_uint(f[0]), __float_as_uint(f[1]), __float_as_uint(f[2]),
-                          __float_as_uint(f[3]));
-    }
-};
-
-__device__ __forceinline__ uint4 ld_v4(const void *p)
-{
-    uint4 v;
-    asm volatile("ld.global.v4.u32 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                 : "l"(p)
-                 : "memory");
-    return v;
-}
-
-// Receive vector v from every peer's LL packets (bounded polling, all late
-// peers re-read at once) and fold in rank order with the rank's own vector.
-template <int DT, int RB>
-__device__ __forceinline__ uint4 ll_recv_fold(const SfarArgs &a, int r, int k, uint32_t e, int par,
-                                              unsigned long long v, uint4 own, bool &ok)
-{
-    const int R = a.R;
-    const uint8_t *mine = a.region + (size_t)(r * 2 + par) * R * a.slot;
-    unsigned long long w0[RB], w1[RB], w2[RB], w3[RB];
-    bool rdy[RB];
-#pragma unroll
-    for (int q = 0; q < RB; ++q) {
-        rdy[q] = q >= R || q == r;
-        if (!rdy[q]) {
-            const uint8_t *src = mine + (size_t)q * a.slot + v * 32ull;
-            ld_relaxed_v2u64(src, w0[q], w1[q]);
-            ld_relaxed_v2u64(src + 16, w2[q], w3[q]);
-        }
-    }
-    SfarWaiter w;
-    while (true) {
-        bool all = true;
-#pragma unroll
-        for (int q = 0; q < RB; ++q) {
-            if (!rdy[q])
-                rdy[q] = ll_ready(w0[q], w1[q], w2[q], w3[q], e);
-            all = all && rdy[q];
-        }
-        if (all)
-            break;
-        if (w.tick(a.ctl)) {
-            int late = -1;
-#pragma unroll
-            for (int q = RB - 1; q >= 0; --q)
-                if (!rdy[q])
-                    late = q;
-            sfar_record_fault(a.ctl, r, k, late, e, SFAR_WAIT_LL);
-            ok = false;
-            return make_uint4(0, 0, 0, 0);
-        }
-#pragma unroll
-        for (int q = 0; q < RB; ++q)
-            if (!rdy[q]) {
-                const uint8_t *src = mine + (size_t)q * a.slot + v * 32ull;
-                ld_relaxed_v2u64(src, w0[q], w1[q]);
-                ld_relaxed_v2u64(src + 16, w2[q], w3[q]);
-            }
-    }
-    auto data = [&](int q) {
-        return make_uint4((uint32_t)w0[q], (uint32_t)w1[q], (uint32_t)w2[q], (uint32_t)w3[q]);
-    };
-    SfarAcc<DT> acc;
-    acc.set(r == 0 ? own : data(0));
-#pragma unroll
-    for (int q = 1; q < RB; ++q)
-        if (q < R)
-            acc.add(q == r ? own : data(q));
-    return acc.get();
-}
-
-// ------------------------------------------- cluster exchange (DSMEM + mbarrier)
-__device__ __forceinline__ uint32_t smem_u32(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }
-// the same shared-memory offset in cluster CTA `rank`, as a shared::cluster address
-__device__ __forceinline__ uint32_t map_cta(uint32_t addr, uint32_t rank)
-{
-    uint32_t out;
-    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(out) : "r"(addr), "r"(rank));
-    return out;
-}
-__device__ __forceinline__ void mbar_init(uint32_t mb, uint32_t count)
-{
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(mb), "r"(count) : "memory");
-}
-__device__ __forceinline__ void fence_mbar_init_cluster()
-{
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-}
-__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t mb, uint32_t bytes)
-{
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(mb), "r"(bytes) : "memory");
-}
-__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t mb, uint32_t parity)
-{
-    uint32_t done;
-    asm volatile("{\n\t.reg .pred p;\n\t"
-                 "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
-                 "selp.u32 %0, 1, 0, p;\n\t}"
-                 : "=r"(done)
-                 : "r"(mb), "r"(parity)
-                 : "memory");
-    return done != 0;
-}
-__device__ __forceinline__ void st_async_u32(uint32_t raddr, uint32_t v, uint32_t rmbar)
-{
-    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];" ::"r"(raddr), "r"(v),
-                 "r"(rmbar)
-                 : "memory");
-}
-__device__ __forceinline__ void st_async_u64(uint32_t raddr, unsigned long long v, uint32_t rmbar)
-{
-    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b64 [%0], %1, [%2];" ::"r"(raddr), "l"(v),
-                 "r"(rmbar)
-                 : "memory");
-}
-__device__ __forceinline__ void st_async_v4u32(uint32_t raddr, uint4 v, uint32_t rmbar)
-{
-    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(raddr),
-                 "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w), "r"(rmbar)
-                 : "memory");
-}
-__device__ __forceinline__ void st_async_v2u64(uint32_t raddr, unsigned long long a, unsigned long long b,
-                                               uint32_t rmbar)
-{
-    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v2.b64 [%0], {%1, %2}, [%3];" ::"r"(raddr),
-                 "l"(a), "l"(b), "r"(rmbar)
-                 : "memory");
-}
-__device__ __forceinline__ void cluster_arrive_relaxed()
-{
-    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
-}
-__device__ __forceinline__ void cluster_wait()
-{
-    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-// Wait for one phase of a local mbarrier that the cluster's CTAs complete.
-// Every CTA of the cluster sends its statistics on every path, after waits
-// that are each bounded by at most twice the handle's limit, so this wait
-// does not give up when another CTA records a failure (which would let this
-// CTA exit while a peer's store into its shared memory is still coming); it
-// gives up only after 8 times the limit, records a fault and returns false.
-__device__ __forceinline__ bool cluster_mbar_wait(uint32_t mb, uint32_t parity, SfarCtl *ctl, int r, int k,
-                                                  uint32_t e)
-{
-    unsigned long long t0 = 0;
-    uint32_t it = 0;
-    while (!mbar_try_wait_cluster(mb, parity)) {
-        if ((++it & 127u) != 0)
-            continue;
-        const unsigned long long now = globaltimer();
-        if (t0 == 0) {
-            t0 = now;
-        } else if (now - t0 > (ld_relaxed_u64(&ctl->timeout_ns) << 3)) {
-            sfar_record_fault(ctl, r, k, -1, e, SFAR_WAIT_CLUSTER);
-            return false;
-        }
-    }
-    return true;
-}
-
-__device__ __forceinline__ unsigned long long warp_sum_u64(unsigned long long x)
-{
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-        const uint32_t lo = __shfl_xor_sync(SFAR_FULL, (uint32_t)x, o);
-        const uint32_t hi = __shfl_xor_sync(SFAR_FULL, (uint32_t)(x >> 32), o);
-        x += ((unsigned long long)hi << 32) | lo;
-    }
-    return x;
-}
-
-}  // namespace
-
-template <int DT, int RB, bool AR, bool TEST, int NB>
-__global__ void __launch_bounds__(SFAR_NORM_THREADS, 1) k_fused(const __grid_constant__ SfarArgs a,
-                                                             const __grid_constant__ SfarNormArgs na)
-{
-    using V = Vec<DT>;
-    constexpr int ES = DT == 0 ? 2 : 4;
-    const int R = a.R, K = a.K, CL = na.CL, G = na.G;
-    const int r = blockIdx.x / K, k = blockIdx.x - r * K;
-    const int g = k / CL, cr = k - g * CL;      // 1-D clusters of CL consecutive CTAs: the rank in the cluster
-    const int T = blockDim.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const unsigned long long h = na.hidden, rows = na.rows;
-    const unsigned long long VR = h * ES / 16ull;       // vectors per row
-    const unsigned long long ustride = (unsigned long long)CL * T;
-    const unsigned long long u0 = (unsigned long long)cr * T + tid;
-
-    // one slot per (cluster CTA, warp): every warp sends its partial straight
-    // to every cluster CTA
-    constexpr int WMAX = SFAR_NORM_THREADS / 32;
-    __shared__ __align__(16) unsigned long long s_sum[SFAR_NORM_CLMAX * WMAX][SFAR_NORM_VMAX];
-    __shared__ __align__(16) uint4 s_max[SFAR_NORM_CLMAX * WMAX];
-    __shared__ __align__(8) unsigned long long s_mbar[2];      // [0]: row maxima, [1]: row sums
-    const uint32_t mb_max = smem_u32(&s_mbar[0]), mb_sum = smem_u32(&s_mbar[1]);
-    const int W = T >> 5, nslots = CL * W, slot = cr * W + warp;
-
-    // first input vector of the first row, loaded ahead of the prologue (the
-    // L2 prefetch may precede the programmatic-launch wait, the load not)
-    const bool has0 = (unsigned long long)g < rows && u0 < VR;
-    const unsigned long long v00 = (unsigned long long)g * VR + u0;
-    if (has0) {
-        if (AR)
-            prefetch_l2((const char *)a.in[r] + v00 * 16ull);
-        prefetch_l2((const char *)na.res[r] + v00 * 16ull);
-        prefetch_l2((const char *)na.weight + u0 * 16ull);
-    }
-    SfarCall c;
-    c.e = 0;
-    c.par = 0;
-    c.drop = false;
-    c.mid_delay_ns = 0;
-    c.trace = nullptr;
-    bool alive = true;
-    uint4 x00 = make_uint4(0, 0, 0, 0), r00 = x00, w00 = x00;
-    if (AR) {
-        const SfarEntry ent = sfar_entry<true>(a);     // early ticket (see sfar_entry)
-        if (has0)
-            x00 = ld_nc_v4((const char *)a.in[r] + v00 * 16ull);
-        alive = sfar_prologue<TEST>(a, r, k, c, ent);
-    } else {
-        pdl_wait();
-    }
-    // the first row's residual and weight of vector j = 0: loaded now, so
-    // their latency overlaps the sends and the AllReduce round trip
-    if (has0) {
-        r00 = ld_v4((const char *)na.res[r] + v00 * 16ull);
-        w00 = ld_nc_v4((const char *)na.weight + u0 * 16ull);
-        if (!AR)
-            x00 = ld_nc_v4((const char *)a.in[r] + v00 * 16ull);
-    }
-    const uint32_t e = c.e;
-    bool ok = alive;
-
-    // 1. AllReduce send: every vector of every row of this cluster, as LL
-    // packets into every peer's slot r (the plain LL kernel's layout)
-    if (AR && ok && !c.drop) {
-        const unsigned long long eh = (unsigned long long)e << 32;
-        for (unsigned long long i = g; i < rows; i += G) {
-#pragma unroll
-            for (int j = 0; j < SFAR_NORM_VMAX; ++j) {
-                const unsigned long long u = u0 + j * ustride;
-                if (u < VR) {
-                    const unsigned long long v = i * VR + u;
-                    const uint4 x = (i == (unsigned long long)g && j == 0) ? x00
-                                                                            : ld_nc_v4((const char *)a.in[r] + v * 16ull);
-                    const unsigned long long p0 = x.x | eh, p1 = x.y | eh, p2 = x.z | eh, p3 = x.w | eh;
-#pragma unroll
-                    for (int q = 0; q < RB - 1; ++q) {
-                        if (q < R - 1) {
-                            const int p = peer_of(r, q);
-                            uint8_t *dst = a.region + ((size_t)(p * 2 + c.par) * R + r) * a.slot + v * 32ull;
-                            st_relaxed_v2u64(dst, p0, p1);
-                            st_relaxed_v2u64(dst + 16, p2, p3);
-                        }
-                    }
-                }
-            }
-        }
-    }
-    if (AR) {
-        sfar_stamp(c, TP_SENT);
-        sfar_mid_delay<TEST>(c);
-    }
-
-    // Row statistics travel between the cluster's CTAs as st.async stores
-    // into each other's shared memory, each completing bytes on the
-    // receiver's mbarrier.  The mbarriers must be initialised before any peer
-    // signals them: init, fence, cluster arrive here (after the sends,
-    // which are more urgent); the matching wait comes
-    // just before the first store to a peer.
-    if (tid == 0) {
-        mbar_init(mb_max, 1);
-        mbar_init(mb_sum, 1);
-        fence_mbar_init_cluster();
-    }
-    __syncthreads();
-    cluster_arrive_relaxed();
-    bool cluster_ready = false;
-    uint32_t phase = 0;
-
-
-    // 2. rows in batches of B: the AllReduce result, z, then the row
-    // statistics of the whole batch in two cluster rounds (each warp sends its
-    // B maxima, then its B sums), then y.  NB = 1: one row, slot q of a thread
-    // is its vector q of the row; NB = 4 (one vector per row and thread): slot
-    // q is row i0 + q*G.
-    const int vpt = na.vpt, B = na.B;
-    for (unsigned long long i0 = g; i0 < rows; i0 += (unsigned long long)G * B) {
-        uint4 zv[SFAR_NORM_VMAX], wv[SFAR_NORM_VMAX], rv[SFAR_NORM_VMAX], xv[SFAR_NORM_VMAX];
-        bool valid[SFAR_NORM_VMAX];
-        unsigned long long vq[SFAR_NORM_VMAX];
-        // independent loads first: residual, weight and own input of every slot
-#pragma unroll
-        for (int q = 0; q < SFAR_NORM_VMAX; ++q) {
-            const int bq = NB == 1 ? 0 : q, j = NB == 1 ? q : 0;
-            const unsigned long long i = i0 + (unsigned long long)bq * G, u = u0 + j * ustride;
-            zv[q] = wv[q] = rv[q] = xv[q] = make_uint4(0, 0, 0, 0);
-            valid[q] = bq < B && j < vpt && i < rows && u < VR;
-            vq[q] = i * VR + u;
-            if (valid[q]) {
-                if (i == (unsigned long long)g && j == 0) {
-                    rv[q] = r00;
-                    wv[q] = w00;
-                    xv[q] = x00;
-                } else {
-                    rv[q] = ld_v4((const char *)na.res[r] + vq[q] * 16ull);
-                    wv[q] = ld_nc_v4((const char *)na.weight + u * 16ull);
-                    xv[q] = ld_nc_v4((const char *)a.in[r] + vq[q] * 16ull);
-                }
-            }
-        }
-        uint32_t lmax[NB];                                        // per row of the batch
-#pragma unroll
-        for (int bb = 0; bb < NB; ++bb)
-            lmax[bb] = 0u;
-#pragma unroll
-        for (int q = 0; q < SFAR_NORM_VMAX; ++q) {
-            if (valid[q] && ok) {
-                const uint4 av = AR ? ll_recv_fold<DT, RB>(a, r, k, e, c.par, vq[q], xv[q], ok) : xv[q];
-                float zf[V::N];
-#pragma unroll
-                for (int t = 0; t < V::N; ++t)
-                    zf[t] = __fadd_rn(V::get(av, t), V::get(rv[q], t));
-                zv[q] = V::pack(zf);
-                uint32_t m = 0;
-#pragma unroll
-                for (int t = 0; t < V::N; ++t)
-                    m = max(m, mag_bits(V::get(zv[q], t)));
-                lmax[NB == 1 ? 0 : q] = max(lmax[NB == 1 ? 0 : q], m);
-            }
-        }
-        if (i0 == (unsigned long long)g)
-            sfar_stamp(c, TP_INPUT);          // first batch: AllReduce result and z in registers
-        // row maxima of the magnitude bits: each warp's B maxima go to its slot
-        // in every cluster CTA
-#pragma unroll
-        for (int bb = 0; bb < NB; ++bb)
-            if (bb < B)
-                lmax[bb] = __reduce_max_sync(SFAR_FULL, lmax[bb]);
-        if (!cluster_ready) {
-            cluster_wait();                    // every peer's mbarriers are initialised
-            cluster_ready = true;
-        }
-        if (tid == 0)
-            mbar_arrive_expect_tx(mb_max, (uint32_t)nslots * (NB == 1 ? 4u : 16u));
-        if (lane < CL) {
-            if (NB == 1)
-                st_async_u32(map_cta(smem_u32(&s_max[slot]), lane), lmax[0], map_cta(mb_max, lane));
-            else
-                st_async_v4u32(map_cta(smem_u32(&s_max[slot]), lane),
-                               make_uint4(lmax[0], lmax[NB > 1 ? 1 : 0], lmax[NB > 2 ? 2 : 0], lmax[NB > 3 ? 3 : 0]),
-                               map_cta(mb_max, lane));
-        }
-        if (!cluster_mbar_wait(mb_max, phase, a.ctl, r, k, e))
-            ok = false;
-        uint32_t M[NB];
-#pragma unroll
-        for (int bb = 0; bb < NB; ++bb)
-            M[bb] = 0u;
-        for (int qs = 0; qs < nslots; ++qs) {
-            const uint4 m4 = s_max[qs];
-            M[0] = max(M[0], m4.x);
-            if (NB > 1) {
-                M[NB > 1 ? 1 : 0] = max(M[NB > 1 ? 1 : 0], m4.y);
-                M[NB > 2 ? 2 : 0] = max(M[NB > 2 ? 2 : 0], m4.z);
-                M[NB > 3 ? 3 : 0] = max(M[NB > 3 ? 3 : 0], m4.w);
-            }
-        }
-        // the truncated squares of each row, summed as integers
-        unsigned long long lsum[NB];
-#pragma unroll
-        for (int bb = 0; bb < NB; ++bb)
-            lsum[bb] = 0ull;
-#pragma unroll
-        for (int q = 0; q < SFAR_NORM_VMAX; ++q) {
-            const int bq = NB == 1 ? 0 : q;
-            if (valid[q] && M[bq] != 0 && M[bq] < 0x7f800000u) {
-                const int E = exp_above(M[bq]);
-#pragma unroll
-                for (int t = 0; t < V::N; ++t)
-                    lsum[bq] += sq_term(V::get(zv[q], t), E, na.F);
-            }
-        }
-#pragma unroll
-        for (int bb = 0; bb < NB; ++bb)
-            if (bb < B)
-                lsum[bb] = warp_sum_u64(lsum[bb]);
-        if (tid == 0)
-            mbar_arrive_expect_tx(mb_sum, (uint32_t)nslots * (NB == 1 ? 8u : 32u));
-        if (lane < CL) {
-            if (NB == 1) {
-                st_async_u64(map_cta(smem_u32(&s_sum[slot][0]), lane), lsum[0], map_cta(mb_sum, lane));
-            } else {
-                st_async_v2u64(map_cta(smem_u32(&s_sum[slot][0]), lane), lsum[0], lsum[NB > 1 ? 1 : 0],
-                               map_cta(mb_sum, lane));
-                st_async_v2u64(map_cta(smem_u32(&s_sum[slot][2]), lane), lsum[NB > 2 ? 2 : 0], lsum[NB > 3 ? 3 : 0],
-                               map_cta(mb_sum, lane));
-            }
-        }
-        if (!cluster_mbar_wait(mb_sum, phase, a.ctl, r, k, e))
-            ok = false;
-        phase ^= 1u;
-        float rstd[NB];
-#pragma unroll
-        for (int bb = 0; bb < NB; ++bb) {
-            rstd[bb] = 0.f;
-            if (bb >= B)
-                continue;
-            unsigned long long S = 0;
-            for (int qs = 0; qs < nslots; ++qs)
-                S += s_sum[qs][bb];
-            const float ms = mean_square(M[bb], S, h, na.F);
-            rstd[bb] = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(ms, na.eps)));
-        }
-        if (i0 == (unsigned long long)g)
-            sfar_stamp(c, TP_RECEIVED);       // first batch: both cluster rounds done
-#pragma unroll
-        for (int q = 0; q < SFAR_NORM_VMAX; ++q) {
-            if (valid[q] && ok) {
-                const float rs = rstd[NB == 1 ? 0 : q];
-                float yf[V::N];
-#pragma unroll
-                for (int t = 0; t < V::N; ++t)
-                    yf[t] = __fmul_rn(__fmul_rn(V::get(zv[q], t), rs), V::get(wv[q], t));
-                st_v4((char *)na.res_out[r] + vq[q] * 16ull, zv[q]);
-                st_v4((char *)a.out[r] + vq[q] * 16ull, V::pack(yf));
-            }
-        }
-    }
-    // A CTA leaves only after its last statistics wait, so every store that a
-    // peer makes into its shared memory has landed (the mbarrier counts the
-    // bytes); the cluster barrier opened at the start is closed first.
-    if (!cluster_ready)
-        cluster_wait();
-    if (AR && alive) {
-        sfar_epilogue(a, r, k, e);
-        sfar_stamp(c, TP_EXIT);
-    }
-}
-
-const void *sfar_kernel_fused(int dt, int wide, int allreduce, int test, int batch)
-{
-    if (!allreduce)
-        wide = test = 0;            // the normalisation alone neither receives nor reads knobs
-    const int nb = batch > 1 ? 4 : 1;
-#define SFAR_PICK(D, W, A, T, N)                                                       \
-    if (dt == D && wide == W && allreduce == A && test == T && nb == N)               \
-        return (const void *)k_fused<D, (W ? 16 : 8), (A != 0), (T != 0), N>;
-#define SFAR_PICK_NB(D, W, A, T) SFAR_PICK(D, W, A, T, 1) SFAR_PICK(D, W, A, T, 4)
-    SFAR_PICK_NB(0, 0, 1, 0) SFAR_PICK_NB(0, 0, 1, 1) SFAR_PICK_NB(0, 1, 1, 0) SFAR_PICK_NB(0, 1, 1, 1)
-    SFAR_PICK_NB(1, 0, 1, 0) SFAR_PICK_NB(1, 0, 1, 1) SFAR_PICK_NB(1, 1, 1, 0) SFAR_PICK_NB(1, 1, 1, 1)
-    SFAR_PICK_NB(0, 0, 0, 0) SFAR_PICK_NB(1, 0, 0, 0)
-#undef SFAR_PICK_NB
-#undef SFAR_PICK
-    return nullptr;
+    return unit == 8 ? sfar_kernel_fused_u8(dt, wide, allreduce, test, batch)
+                     : sfar_kernel_fused_u16(dt, wide, allreduce, test, batch);
 }

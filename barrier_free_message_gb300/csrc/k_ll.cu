@@ -23,16 +23,12 @@
 // so its DRAM latency overlaps the epoch ticket; every poll round re-reads
 // all peers that are not ready yet at once, so one round trip covers them all.
 //
-// Half units (HALF, used for R > 8): a thread carries 8 bytes instead of 16,
-// one 16-byte LL line {w0,e,w1,e} per peer at bytes [16v, 16v + 16) of the
-// slot.  Holding R - 1 peers' packets then takes half the registers (15 peers
-// of 32 bytes each throttled the R = 16 kernel), with twice the threads.
-#include "sfar_prims.cuh"
-
-__device__ __forceinline__ void st_relaxed_u64(unsigned long long *p, unsigned long long v)
-{
-    asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
-}
+// Units (UB, 8 bytes for every rank count): a thread carries UB bytes of
+// input, one 16-byte LL line {w0,e,w1,e} per peer at bytes [16v, 16v + 16)
+// of the slot for UB = 8 (two lines for UB = 16, one 8-byte word {w0,e} for
+// UB = 4).  Holding R - 1 peers' packets then takes half the registers of
+// 16-byte units, with twice the threads.
+#include "sfar_units.cuh"
 
 // The packets of one unit from every peer: UB / 4 words {data, epoch}.
 template <int RB, int UB>
@@ -64,59 +60,6 @@ struct LLSlots {
     }
 };
 
-// UB (8 or 4) bytes of a rank's input as the low words of a vector (bytes
-// past nbytes read as zero, element by element), and the store of such a
-// unit.
-template <int ES, int UB>
-__device__ __forceinline__ uint4 load_part(const void *base, unsigned long long v, unsigned long long nbytes)
-{
-    const unsigned long long off = v * (unsigned long long)UB;
-    uint32_t w0 = 0, w1 = 0;
-    const char *p = (const char *)base + off;
-    if (off + UB <= nbytes) {
-        if (UB == 8)
-            asm volatile("ld.global.nc.v2.u32 {%0,%1}, [%2];" : "=r"(w0), "=r"(w1) : "l"(p));
-        else
-            asm volatile("ld.global.nc.u32 %0, [%1];" : "=r"(w0) : "l"(p));
-    } else if (off < nbytes) {
-        const int rem = (int)(nbytes - off);
-        if (ES == 4) {
-            w0 = *(const uint32_t *)p;
-        } else {
-            const uint16_t *q = (const uint16_t *)p;
-            w0 = q[0];
-            if (rem > 2) w0 |= (uint32_t)q[1] << 16;
-            if (rem > 4) w1 = q[2];
-        }
-    }
-    return make_uint4(w0, w1, 0u, 0u);
-}
-
-template <int ES, int UB>
-__device__ __forceinline__ void store_part(void *base, unsigned long long v, unsigned long long nbytes, uint4 x)
-{
-    const unsigned long long off = v * (unsigned long long)UB;
-    char *p = (char *)base + off;
-    if (off + UB <= nbytes) {
-        if (UB == 8)
-            st_v2u32(p, x.x, x.y);
-        else
-            st_u32(p, x.x);
-        return;
-    }
-    if (off >= nbytes)
-        return;
-    const int rem = (int)(nbytes - off);
-    if (ES == 4) {
-        *(uint32_t *)p = x.x;
-    } else {
-        uint16_t *q = (uint16_t *)p;
-        q[0] = (uint16_t)x.x;
-        if (rem > 2) q[1] = (uint16_t)(x.x >> 16);
-        if (rem > 4) q[2] = (uint16_t)x.y;
-    }
-}
-
 template <int DT, int RB, bool TEST, int UB>
 __global__ void __launch_bounds__(SFAR_THREADS) k_ll(const __grid_constant__ SfarArgs a)
 {
@@ -127,13 +70,11 @@ __global__ void __launch_bounds__(SFAR_THREADS) k_ll(const __grid_constant__ Sfa
     const unsigned long long nvec = (nbytes + UB - 1ull) / UB;
     const unsigned long long stride = (unsigned long long)K * blockDim.x;
     const unsigned long long v0 = (unsigned long long)k * blockDim.x + threadIdx.x;
-    auto load_unit = [&](unsigned long long v) {
-        return UB == 16 ? load_vec<ES>(a.in[r], v, nbytes) : load_part<ES, UB == 16 ? 8 : UB>(a.in[r], v, nbytes);
-    };
+    auto load_in = [&](unsigned long long v) { return load_unit<ES, UB>(a.in[r], v, nbytes); };
     if (v0 * UB < nbytes)
         prefetch_l2((const char *)a.in[r] + v0 * UB);
     const SfarEntry ent = sfar_entry(a);
-    const uint4 x0 = load_unit(v0);                         // zero past the end
+    const uint4 x0 = load_in(v0);                         // zero past the end
     SfarCall c;
     if (!sfar_prologue<TEST>(a, r, k, c, ent))
         return;
@@ -145,7 +86,7 @@ __global__ void __launch_bounds__(SFAR_THREADS) k_ll(const __grid_constant__ Sfa
     // send: pack each input vector once, store it into every peer's slot r
     if (!c.drop) {
         for (unsigned long long v = v0; v < nvec; v += stride) {
-            const uint4 x = v == v0 ? x0 : load_unit(v);
+            const uint4 x = v == v0 ? x0 : load_in(v);
             const unsigned long long p0 = x.x | eh, p1 = x.y | eh, p2 = x.z | eh, p3 = x.w | eh;
 #pragma unroll
             for (int i = 0; i < RB - 1; ++i) {
@@ -153,7 +94,7 @@ __global__ void __launch_bounds__(SFAR_THREADS) k_ll(const __grid_constant__ Sfa
                     const int p = peer_of(r, i);
                     uint8_t *dst = a.region + ((size_t)(p * 2 + c.par) * R + r) * slot + v * 2ull * UB;
                     if (UB == 4) {
-                        st_relaxed_u64(reinterpret_cast<unsigned long long *>(dst), p0);
+                        st_relaxed_u64(dst, p0);
                     } else {
                         st_relaxed_v2u64(dst, p0, p1);
                         if (UB == 16)
@@ -170,7 +111,7 @@ __global__ void __launch_bounds__(SFAR_THREADS) k_ll(const __grid_constant__ Sfa
     const uint8_t *mine = a.region + (size_t)(r * 2 + c.par) * R * slot;
     bool ok = true;
     for (unsigned long long v = v0; v < nvec && ok; v += stride) {
-        const uint4 own = v == v0 ? x0 : load_unit(v);
+        const uint4 own = v == v0 ? x0 : load_in(v);
         LLSlots<RB, UB> s;
         bool rdy[RB];
 #pragma unroll
@@ -213,10 +154,7 @@ __global__ void __launch_bounds__(SFAR_THREADS) k_ll(const __grid_constant__ Sfa
         for (int q = 1; q < RB; ++q)
             if (q < R)
                 acc.add(q == r ? own : s.data(q));
-        if (UB == 16)
-            store_vec<ES>(a.out[r], v, nbytes, acc.get());
-        else
-            store_part<ES, UB == 16 ? 8 : UB>(a.out[r], v, nbytes, acc.get());
+        store_unit<ES, UB>(a.out[r], v, nbytes, acc.get());
     }
     sfar_stamp(c, TP_RECEIVED);
     sfar_epilogue(a, r, k, e);

@@ -23,5 +23,7 @@ struct SfarNormArgs {
 // dt: 0 bf16, 1 fp32; wide: R > 8; allreduce: 1 = AllReduce over LL packets
 // first, 0 = the normalisation of a given AllReduce result; test: knobs;
 // batch: rows per statistics round (1, or up to 4 when every thread holds one
-// vector of each row).
-const void *sfar_kernel_fused(int dt, int wide, int allreduce, int test, int batch);
+// unit of each row); unit: bytes per unit, 16 or 8.
+const void *sfar_kernel_fused(int dt, int wide, int allreduce, int test, int batch, int unit);
+const void *sfar_kernel_fused_u16(int dt, int wide, int allreduce, int test, int batch);
+const void *sfar_kernel_fused_u8(int dt, int wide, int allreduce, int test, int batch);

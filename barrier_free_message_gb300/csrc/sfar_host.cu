@@ -66,8 +66,8 @@ struct sfar {
     int tma_tb = 0, tma_ns = 0;
     size_t tma_smem = 0;
     // fused normalisation: co-resident clusters per launch shape, queried once
-    // ([allreduce][test][batched][cluster size][threads index], 0 = not yet known)
-    int norm_clusters[2][2][2][SFAR_NORM_CLMAX + 1][4] = {};
+    // ([allreduce][test][batched][8-byte units][cluster size][threads index], 0 = not yet known)
+    int norm_clusters[2][2][2][2][SFAR_NORM_CLMAX + 1][4] = {};
 };
 
 static const void *kernel_for(const sfar *h, int p, int test)
@@ -109,6 +109,8 @@ static size_t work_units(const sfar *h, int p, size_t n, size_t *chunk)
     switch (p) {
     case SFAR_LL:
         return ceil_div(n * (size_t)h->es, h->R > 8 ? SFAR_LL_UNIT_WIDE : SFAR_LL_UNIT_NARROW);
+    case SFAR_SENTINEL:
+        return ceil_div(n * (size_t)h->es, SFAR_SENT_UNIT);
     case SFAR_LL128:
         return ceil_div(nvec, 31);
     case SFAR_TWOSHOT: {
@@ -563,19 +565,20 @@ sfar_status sfar_allreduce(sfar_t *h, const void *const in[], void *const out[],
 // ------------------------------------------------- fused AllReduce + RMSNorm
 static const int kNormThreads[4] = {32, 64, 128, 256};
 
-// Cluster size and threads for a row of VR vectors: 128 threads per CTA up
-// to 4096 vectors (256 beyond, up to 8192), preferably one vector per thread
-// over a cluster of up to 8 CTAs (*CL); *CLmin is the smallest cluster that
-// still gives every thread at most SFAR_NORM_VMAX vectors.  Rows of up to
-// 128 vectors take one CTA.
-static bool norm_shape(unsigned long long VR, int *CL, int *CLmin, int *ti)
+// Cluster size and threads for a row of VR units: one unit per thread over
+// a cluster of up to 8 CTAs where it fits (*CL) -- 128 threads per CTA up to
+// 1024 units, 256 threads beyond for 8-byte units; for 16-byte units 128
+// threads up to 4096 units, 256 beyond (up to 8192).  *CLmin is the smallest
+// cluster that still gives every thread at most SFAR_NORM_VMAX units.  Rows
+// of up to 128 units take one CTA.
+static bool norm_shape(unsigned long long VR, int unit, int *CL, int *CLmin, int *ti)
 {
     if (VR <= 128) {
         *CL = *CLmin = 1;
         *ti = VR <= 32 ? 0 : VR <= 64 ? 1 : 2;
         return true;
     }
-    const int t = VR <= 4096 ? 128 : 256;
+    const int t = VR <= (unit == 8 ? 1024u : 4096u) ? 128 : 256;
     *ti = t == 128 ? 2 : 3;
     int cl = (int)ceil_div(VR, (size_t)t);
     if (cl > SFAR_NORM_CLMAX)
@@ -585,9 +588,9 @@ static bool norm_shape(unsigned long long VR, int *CL, int *CLmin, int *ti)
     return *CLmin <= cl;
 }
 
-static int norm_max_clusters(sfar *h, int allreduce, int test, int batch, int CL, int ti)
+static int norm_max_clusters(sfar *h, int allreduce, int test, int batch, int unit, int CL, int ti)
 {
-    int &slot = h->norm_clusters[allreduce][test][batch > 1 ? 1 : 0][CL][ti];
+    int &slot = h->norm_clusters[allreduce][test][batch > 1 ? 1 : 0][unit == 8 ? 1 : 0][CL][ti];
     if (slot)
         return slot;
     cudaLaunchConfig_t cfg;
@@ -602,7 +605,7 @@ static int norm_max_clusters(sfar *h, int allreduce, int test, int batch, int CL
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, sfar_kernel_fused(h->dt, h->R > 8, allreduce, test, batch), &cfg) !=
+    if (cudaOccupancyMaxActiveClusters(&n, sfar_kernel_fused(h->dt, h->R > 8, allreduce, test, batch, unit), &cfg) !=
         cudaSuccess) {
         cudaGetLastError();
         return -1;
@@ -616,11 +619,11 @@ static int norm_max_clusters(sfar *h, int allreduce, int test, int batch, int CL
 // per rank G (K = G * CL <= KMAX), vectors of a row per thread, and rows per
 // statistics round (up to 4 when every thread holds one vector of each row
 // and a cluster gets more than one row).
-static sfar_status norm_geometry(sfar *h, int allreduce, int test, size_t rows, unsigned long long VR, int *CL_out,
-                                 int *G_out, int *threads_out, int *vpt_out, int *batch_out)
+static sfar_status norm_geometry(sfar *h, int allreduce, int test, size_t rows, unsigned long long VR, int unit,
+                                 int *CL_out, int *G_out, int *threads_out, int *vpt_out, int *batch_out)
 {
     int CL = 0, CLmin = 0, ti = 0;
-    if (!norm_shape(VR, &CL, &CLmin, &ti))
+    if (!norm_shape(VR, unit, &CL, &CLmin, &ti))
         return SFAR_ERR_INVALID;
     int cur = -1;
     cudaGetDevice(&cur);
@@ -630,7 +633,7 @@ static sfar_status norm_geometry(sfar *h, int allreduce, int test, size_t rows, 
     for (; CL >= CLmin; --CL) {
         vpt = (int)ceil_div(VR, (size_t)CL * kNormThreads[ti]);
         nb = (vpt == 1 && rows > 1) ? 4 : 1;
-        maxc = norm_max_clusters(h, allreduce, test, nb, CL, ti);
+        maxc = norm_max_clusters(h, allreduce, test, nb, unit, CL, ti);
         if (maxc < 0 || maxc >= h->R)
             break;
     }
@@ -658,6 +661,26 @@ static sfar_status norm_geometry(sfar *h, int allreduce, int test, size_t rows, 
     return SFAR_OK;
 }
 
+// The launch plan of a fused call.  8-byte units (one LL line per peer and
+// thread, as the plain LL kernel) serve an AllReduce of rows of at most
+// 16 KB when every cluster still gets at most one row: they double the
+// threads of a row, so a rank gets about half as many clusters, which costs
+// more than the shorter receive once a cluster has several rows.  16-byte
+// units otherwise, and always for the normalisation alone (no receive).
+static sfar_status norm_plan(sfar *h, int allreduce, int test, size_t rows, size_t row_bytes, int *unit, int *CL,
+                             int *G, int *threads, int *vpt, int *batch)
+{
+    if (allreduce && row_bytes <= 16384) {
+        const sfar_status st = norm_geometry(h, allreduce, test, rows, row_bytes / 8, 8, CL, G, threads, vpt, batch);
+        if (st == SFAR_OK && (size_t)*G >= rows) {
+            *unit = 8;
+            return SFAR_OK;
+        }
+    }
+    *unit = 16;
+    return norm_geometry(h, allreduce, test, rows, row_bytes / 16, 16, CL, G, threads, vpt, batch);
+}
+
 static bool ranges_overlap(const void *a, const void *b, size_t bytes)
 {
     const uintptr_t a0 = (uintptr_t)a, b0 = (uintptr_t)b;
@@ -683,8 +706,8 @@ static sfar_status fused_call(sfar *h, const void *const in[], const void *const
     const size_t bytes = rows * hidden * es;
     if (allreduce && bytes > h->rb)
         return SFAR_ERR_INVALID;
-    const unsigned long long VR = hidden * es / 16;
-    if (VR > 8192 || (R > 8 && VR > 4096))
+    // rows of at most 128 KiB (64 KiB for R > 8)
+    if (hidden * es > 131072 || (R > 8 && hidden * es > 65536))
         return SFAR_ERR_INVALID;
     for (int r = 0; r < R; ++r)
         if (!in[r] || !residual[r] || !out[r] || !residual_out[r] || ((uintptr_t)in[r] & 15u) ||
@@ -711,10 +734,11 @@ static sfar_status fused_call(sfar *h, const void *const in[], const void *const
         }
     }
     const int test = allreduce && (h->k_strag || h->k_drop || h->k_single) ? 1 : 0;
-    int CL = 0, G = 0, threads = 0, vpt = 1, batch = 1;
-    const sfar_status gst = norm_geometry(h, allreduce, test, rows, VR, &CL, &G, &threads, &vpt, &batch);
+    int unit = 16, CL = 0, G = 0, threads = 0, vpt = 1, batch = 1;
+    const sfar_status gst = norm_plan(h, allreduce, test, rows, hidden * es, &unit, &CL, &G, &threads, &vpt, &batch);
     if (gst != SFAR_OK)
         return gst;
+    const unsigned long long VR = hidden * es / (size_t)unit;
     const int K = G * CL;
     int cur = -1;
     cudaGetDevice(&cur);
@@ -753,8 +777,9 @@ static sfar_status fused_call(sfar *h, const void *const in[], const void *const
     na.F = 53 - c;
     a.overlap = 0;
     if (allreduce && h->mode == SFAR_LAUNCH_OVERLAP) {
-        // the vector -> CTA mapping depends on the cluster shape and the row
-        // length too, so all of them are part of the overlap key
+        // the unit -> CTA mapping depends on the cluster shape, the row
+        // length and the unit size too, so all of them are part of the
+        // overlap key
         cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
         unsigned long long cap = 0;
         if (cudaStreamGetCaptureInfo((cudaStream_t)s, &cs, &cap) != cudaSuccess) {
@@ -763,8 +788,8 @@ static sfar_status fused_call(sfar *h, const void *const in[], const void *const
         }
         if (cs != cudaStreamCaptureStatusActive)
             cap = 0;
-        const long long key = (31ll << 40) | ((long long)CL << 36) | ((long long)K << 27) |
-                              ((long long)threads << 16) | (long long)VR;
+        const long long key = ((long long)(unit == 8) << 45) | (31ll << 40) | ((long long)CL << 36) |
+                              ((long long)K << 27) | ((long long)threads << 16) | (long long)VR;
         a.overlap = (key == h->last_key && s == h->last_stream && cap == h->last_capture) ? 1 : 0;
         h->last_key = key;
         h->last_stream = s;
@@ -792,7 +817,7 @@ static sfar_status fused_call(sfar *h, const void *const in[], const void *const
     void *args[] = {&a, &na};
     if (cur != h->dev)
         cudaSetDevice(h->dev);
-    cudaError_t err = cudaLaunchKernelExC(&cfg, sfar_kernel_fused(h->dt, R > 8, allreduce, test, batch), args);
+    cudaError_t err = cudaLaunchKernelExC(&cfg, sfar_kernel_fused(h->dt, R > 8, allreduce, test, batch, unit), args);
     if (cur != h->dev && cur >= 0)
         cudaSetDevice(cur);
     if (err != cudaSuccess) {
@@ -807,11 +832,11 @@ sfar_status sfar_test_query_norm_launch(sfar_t *h, size_t rows, size_t hidden, i
 {
     if (!h || hidden == 0 || rows == 0 || (hidden * (size_t)h->es) % 16)
         return SFAR_ERR_INVALID;
-    const unsigned long long VR = hidden * (size_t)h->es / 16;
-    if (VR > 8192 || (h->R > 8 && VR > 4096))
+    const size_t row = hidden * (size_t)h->es;
+    if (row > 131072 || (h->R > 8 && row > 65536))
         return SFAR_ERR_INVALID;
-    int CL = 0, G = 0, threads = 0, vpt = 1, batch = 1;
-    const sfar_status st = norm_geometry(h, allreduce ? 1 : 0, 0, rows, VR, &CL, &G, &threads, &vpt, &batch);
+    int unit = 16, CL = 0, G = 0, threads = 0, vpt = 1, batch = 1;
+    const sfar_status st = norm_plan(h, allreduce ? 1 : 0, 0, rows, row, &unit, &CL, &G, &threads, &vpt, &batch);
     if (st != SFAR_OK)
         return st;
     if (ctas_per_rank)

@@ -14,6 +14,7 @@
 #define SFAR_NTHREAD_OPTS 3                 // receive-buffer kernels: 64, 128 or 256 threads
 #define SFAR_LL_UNIT_NARROW 8               // LL kernel: input bytes per thread for R <= 8 (16, 8 or 4)
 #define SFAR_LL_UNIT_WIDE 8                 // and for R > 8
+#define SFAR_SENT_UNIT 8                    // sentinel kernel: input bytes per thread (16 or 8)
 
 // Device status block of one handle.  The first 32 bytes are the sticky
 // status and the fault record; the knobs follow.

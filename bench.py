@@ -145,15 +145,16 @@ def measured_peaks():
         return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}, "fallback"
 
 
-KERNEL_SOURCES = {"k_ll": "k_ll.cu", "k_sentinel": "k_sentinel.cu", "k_db": "k_db.cu", "k_baseline": "k_db.cu",
-                  "k_ll128": "k_ll128.cu", "k_tma": "k_tma.cu"}
+KERNEL_SOURCES = {"k_ll": ("k_ll.cu", "sfar_units.cuh"), "k_sentinel": ("k_sentinel.cu", "sfar_units.cuh"),
+                  "k_db": ("k_db.cu",), "k_baseline": ("k_db.cu",), "k_ll128": ("k_ll128.cu",),
+                  "k_tma": ("k_tma.cu",)}
 
 
 def kernel_sources_hash(kernel: str) -> str:
-    """Hash of the files that make up one kernel (its .cu and the shared headers)."""
+    """Hash of the files that make up one kernel (its own sources and the shared headers)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "barrier_free_message_gb300", "csrc")
-    for name in (KERNEL_SOURCES.get(kernel, ""), "sfar_prims.cuh", "sfar_internal.h"):
+    for name in (*KERNEL_SOURCES.get(kernel, ()), "sfar_prims.cuh", "sfar_internal.h"):
         p = os.path.join(csrc, name)
         if os.path.isfile(p):
             with open(p, "rb") as f:
