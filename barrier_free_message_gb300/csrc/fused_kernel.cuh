@@ -341,9 +341,12 @@ __device__ __forceinline__ unsigned long long warp_sum_u64(unsigned long long x)
 
 }  // namespace
 
+// Two CTAs per SM for 8-byte units and R <= 8 (at most 128 registers; the
+// batched variant spills 12 bytes): twice the clusters per rank, so more rows
+// take 8-byte units.  The wide variant keeps one (it would spill 290 bytes).
 template <int DT, int RB, bool AR, bool TEST, int NB, int UB>
-__global__ void __launch_bounds__(SFAR_NORM_THREADS, 1) k_fused(const __grid_constant__ SfarArgs a,
-                                                             const __grid_constant__ SfarNormArgs na)
+__global__ void __launch_bounds__(SFAR_NORM_THREADS, UB == 8 && RB <= 8 ? 2 : 1)
+    k_fused(const __grid_constant__ SfarArgs a, const __grid_constant__ SfarNormArgs na)
 {
     using V = Vec<DT>;
     constexpr int ES = DT == 0 ? 2 : 4;
