@@ -27,3 +27,6 @@ struct SfarNormArgs {
 const void *sfar_kernel_fused(int dt, int wide, int allreduce, int test, int batch, int unit);
 const void *sfar_kernel_fused_u16(int dt, int wide, int allreduce, int test, int batch);
 const void *sfar_kernel_fused_u8(int dt, int wide, int allreduce, int test, int batch);
+// The two-shot fused kernel (rows of at most 32 KB, one 16-byte unit per
+// thread): dt, wide and test as above.
+const void *sfar_kernel_fused_ts(int dt, int wide, int test);

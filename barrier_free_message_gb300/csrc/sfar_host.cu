@@ -68,6 +68,9 @@ struct sfar {
     // fused normalisation: co-resident clusters per launch shape, queried once
     // ([allreduce][test][batched][8-byte units][cluster size][threads index], 0 = not yet known)
     int norm_clusters[2][2][2][2][SFAR_NORM_CLMAX + 1][4] = {};
+    // two-shot fused kernel: co-resident clusters ([test][cluster size][threads index])
+    int ts_clusters[2][SFAR_NORM_CLMAX + 1][4] = {};
+    int fused_path = 0;                 // test knob: 0 by shape, 1 one-shot LL, 2 two-shot
 };
 
 static const void *kernel_for(const sfar *h, int p, int test)
@@ -661,15 +664,83 @@ static sfar_status norm_geometry(sfar *h, int allreduce, int test, size_t rows, 
     return SFAR_OK;
 }
 
+// Two-shot fused call: a row over one cluster of CL CTAs with one 16-byte
+// unit per thread (32-128 threads for rows of up to 128 units, 128 up to
+// 1024, 256 up to 2048: rows of at most 32 KB), and G clusters per rank: as
+// many as the rows need, all of the grid resident at once (its CTAs wait on
+// one another).
+static sfar_status ts_geometry(sfar *h, int test, size_t rows, unsigned long long VR, int *CL_out, int *G_out,
+                               int *threads_out)
+{
+    const int ti = VR <= 32 ? 0 : VR <= 64 ? 1 : VR <= 1024 ? 2 : 3;
+    const size_t CL = ceil_div(VR, (size_t)kNormThreads[ti]);
+    if (CL > SFAR_NORM_CLMAX)
+        return SFAR_ERR_UNSUPPORTED;
+    int &slot = h->ts_clusters[test][CL][ti];
+    if (!slot) {
+        cudaLaunchConfig_t cfg;
+        memset(&cfg, 0, sizeof cfg);
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = (unsigned)CL;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.gridDim = dim3((unsigned)CL);
+        cfg.blockDim = dim3((unsigned)kNormThreads[ti]);
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        int cur = -1, n = 0;
+        cudaGetDevice(&cur);
+        if (cur != h->dev)
+            cudaSetDevice(h->dev);
+        const cudaError_t err =
+            cudaOccupancyMaxActiveClusters(&n, sfar_kernel_fused_ts(h->dt, h->R > 8, test), &cfg);
+        if (cur != h->dev && cur >= 0)
+            cudaSetDevice(cur);
+        if (err != cudaSuccess) {
+            cudaGetLastError();
+            return SFAR_ERR_CUDA;
+        }
+        slot = n > 0 ? n : -1;
+    }
+    if (slot < h->R)
+        return SFAR_ERR_UNSUPPORTED;
+    size_t G = (size_t)slot / (size_t)h->R;
+    if (G > (size_t)SFAR_KMAX / CL)
+        G = (size_t)SFAR_KMAX / CL;
+    if (G > ceil_div(rows, (size_t)h->R))
+        G = ceil_div(rows, (size_t)h->R);
+    *CL_out = (int)CL;
+    *G_out = (int)(G < 1 ? 1 : G);
+    *threads_out = kNormThreads[ti];
+    return SFAR_OK;
+}
+
 // The launch plan of a fused call.  8-byte units (one LL line per peer and
 // thread, as the plain LL kernel) serve an AllReduce of rows of at most
 // 16 KB when every cluster still gets at most one row: they double the
 // threads of a row, so a rank gets about half as many clusters, which costs
 // more than the shorter receive once a cluster has several rows.  16-byte
 // units otherwise, and always for the normalisation alone (no receive).
-static sfar_status norm_plan(sfar *h, int allreduce, int test, size_t rows, size_t row_bytes, int *unit, int *CL,
-                             int *G, int *threads, int *vpt, int *batch)
+//
+// Path 2, the two-shot fused kernel, serves an AllReduce whose rows (at most
+// 32 KB) the one-shot plan would stack several to a cluster: there every
+// rank would receive every row from every peer through LL packets, while the
+// two-shot owner of a row reads each rank's row once.  Path 1 is the one-shot
+// kernel over LL packets; it also takes the shapes whose two-shot grid
+// cannot be resident at once.
+static sfar_status norm_plan(sfar *h, int allreduce, int test, size_t rows, size_t row_bytes, int *path, int *unit,
+                             int *CL, int *G, int *threads, int *vpt, int *batch)
 {
+    const bool ts_fits = allreduce && row_bytes <= 32768;
+    *vpt = 1;
+    *batch = 1;
+    if (ts_fits && h->fused_path == 2 && ts_geometry(h, test, rows, row_bytes / 16, CL, G, threads) == SFAR_OK) {
+        *path = 2;
+        *unit = 16;
+        return SFAR_OK;
+    }
+    *path = 1;
     if (allreduce && row_bytes <= 16384) {
         const sfar_status st = norm_geometry(h, allreduce, test, rows, row_bytes / 8, 8, CL, G, threads, vpt, batch);
         if (st == SFAR_OK && (size_t)*G >= rows) {
@@ -678,7 +749,20 @@ static sfar_status norm_plan(sfar *h, int allreduce, int test, size_t rows, size
         }
     }
     *unit = 16;
-    return norm_geometry(h, allreduce, test, rows, row_bytes / 16, 16, CL, G, threads, vpt, batch);
+    const sfar_status st = norm_geometry(h, allreduce, test, rows, row_bytes / 16, 16, CL, G, threads, vpt, batch);
+    if (ts_fits && h->fused_path == 0 && (st != SFAR_OK || (size_t)*G < rows)) {
+        int tCL = 0, tG = 0, tT = 0;
+        if (ts_geometry(h, test, rows, row_bytes / 16, &tCL, &tG, &tT) == SFAR_OK) {
+            *path = 2;
+            *CL = tCL;
+            *G = tG;
+            *threads = tT;
+            *vpt = 1;
+            *batch = 1;
+            return SFAR_OK;
+        }
+    }
+    return st;
 }
 
 static bool ranges_overlap(const void *a, const void *b, size_t bytes)
@@ -734,8 +818,9 @@ static sfar_status fused_call(sfar *h, const void *const in[], const void *const
         }
     }
     const int test = allreduce && (h->k_strag || h->k_drop || h->k_single) ? 1 : 0;
-    int unit = 16, CL = 0, G = 0, threads = 0, vpt = 1, batch = 1;
-    const sfar_status gst = norm_plan(h, allreduce, test, rows, hidden * es, &unit, &CL, &G, &threads, &vpt, &batch);
+    int path = 1, unit = 16, CL = 0, G = 0, threads = 0, vpt = 1, batch = 1;
+    const sfar_status gst =
+        norm_plan(h, allreduce, test, rows, hidden * es, &path, &unit, &CL, &G, &threads, &vpt, &batch);
     if (gst != SFAR_OK)
         return gst;
     const unsigned long long VR = hidden * es / (size_t)unit;
@@ -759,8 +844,10 @@ static sfar_status fused_call(sfar *h, const void *const in[], const void *const
     a.ctl = h->ctl;
     a.R = R;
     a.K = K;
-    a.region = h->r_ll;
-    a.slot = h->s_ll;
+    a.region = path == 1 ? h->r_ll : nullptr;
+    a.slot = path == 1 ? h->s_ll : 0;
+    a.fa = path == 2 ? h->fc : nullptr;       // arrival flags [R][KMAX]
+    a.fb = path == 2 ? h->fd : nullptr;       // completion flags [R][R][KMAX]
     a.trace = allreduce ? h->trace : nullptr;
     a.trace_calls = allreduce ? h->trace_calls : 0;
     na.weight = weight;
@@ -776,7 +863,11 @@ static sfar_status fused_call(sfar *h, const void *const in[], const void *const
         ++c;
     na.F = 53 - c;
     a.overlap = 0;
-    if (allreduce && h->mode == SFAR_LAUNCH_OVERLAP) {
+    if (path == 2) {
+        // the two-shot kernel never overtakes a call, and the call after it
+        // does not overtake it: it starts with serial semantics
+        h->last_key = -1;
+    } else if (allreduce && h->mode == SFAR_LAUNCH_OVERLAP) {
         // the unit -> CTA mapping depends on the cluster shape, the row
         // length and the unit size too, so all of them are part of the
         // overlap key
@@ -817,7 +908,9 @@ static sfar_status fused_call(sfar *h, const void *const in[], const void *const
     void *args[] = {&a, &na};
     if (cur != h->dev)
         cudaSetDevice(h->dev);
-    cudaError_t err = cudaLaunchKernelExC(&cfg, sfar_kernel_fused(h->dt, R > 8, allreduce, test, batch, unit), args);
+    const void *kern = path == 2 ? sfar_kernel_fused_ts(h->dt, R > 8, test)
+                                 : sfar_kernel_fused(h->dt, R > 8, allreduce, test, batch, unit);
+    cudaError_t err = cudaLaunchKernelExC(&cfg, kern, args);
     if (cur != h->dev && cur >= 0)
         cudaSetDevice(cur);
     if (err != cudaSuccess) {
@@ -835,8 +928,9 @@ sfar_status sfar_test_query_norm_launch(sfar_t *h, size_t rows, size_t hidden, i
     const size_t row = hidden * (size_t)h->es;
     if (row > 131072 || (h->R > 8 && row > 65536))
         return SFAR_ERR_INVALID;
-    int unit = 16, CL = 0, G = 0, threads = 0, vpt = 1, batch = 1;
-    const sfar_status st = norm_plan(h, allreduce ? 1 : 0, 0, rows, row, &unit, &CL, &G, &threads, &vpt, &batch);
+    int path = 1, unit = 16, CL = 0, G = 0, threads = 0, vpt = 1, batch = 1;
+    const sfar_status st =
+        norm_plan(h, allreduce ? 1 : 0, 0, rows, row, &path, &unit, &CL, &G, &threads, &vpt, &batch);
     if (st != SFAR_OK)
         return st;
     if (ctas_per_rank)
@@ -1044,6 +1138,25 @@ sfar_status sfar_test_set_geometry(sfar_t *h, int ctas_per_rank, int threads_per
     h->ctas_override = ctas_per_rank;
     h->threads_override = threads_per_cta;
     return SFAR_OK;
+}
+
+sfar_status sfar_test_set_fused_path(sfar_t *h, int path)
+{
+    if (!h || path < 0 || path > 2)
+        return SFAR_ERR_INVALID;
+    h->fused_path = path;
+    return SFAR_OK;
+}
+
+sfar_status sfar_test_query_fused_path(sfar_t *h, size_t rows, size_t hidden, int *path)
+{
+    if (!h || !path || hidden == 0 || rows == 0 || (hidden * (size_t)h->es) % 16)
+        return SFAR_ERR_INVALID;
+    const size_t row = hidden * (size_t)h->es;
+    if (row > 131072 || (h->R > 8 && row > 65536))
+        return SFAR_ERR_INVALID;
+    int unit = 16, CL = 0, G = 0, threads = 0, vpt = 1, batch = 1;
+    return norm_plan(h, 1, 0, rows, row, path, &unit, &CL, &G, &threads, &vpt, &batch);
 }
 
 sfar_status sfar_probe_empty(sfar_stream_t s)

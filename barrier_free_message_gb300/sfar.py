@@ -77,6 +77,9 @@ _SIGS = [
     ("sfar_test_query_norm_launch", ctypes.c_int, [ctypes.c_void_p, ctypes.c_size_t, ctypes.c_size_t, ctypes.c_int,
                                                    ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_int),
                                                    ctypes.POINTER(ctypes.c_int)]),
+    ("sfar_test_set_fused_path", ctypes.c_int, [ctypes.c_void_p, ctypes.c_int]),
+    ("sfar_test_query_fused_path", ctypes.c_int, [ctypes.c_void_p, ctypes.c_size_t, ctypes.c_size_t,
+                                                  ctypes.POINTER(ctypes.c_int)]),
     ("sfar_probe_empty", ctypes.c_int, [ctypes.c_void_p]),
     ("sfar_probe_pingpong", ctypes.c_int, [ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                            ctypes.c_void_p, ctypes.c_void_p]),
@@ -163,6 +166,20 @@ def sfar_test_query_norm_launch(h, rows: int, hidden: int, allreduce: bool = Tru
     code = lib().sfar_test_query_norm_launch(h, rows, hidden, 1 if allreduce else 0, ctypes.byref(k),
                                              ctypes.byref(cl), ctypes.byref(t))
     return code, k.value, cl.value, t.value
+
+
+FUSED_PATHS = {"auto": 0, "oneshot": 1, "twoshot": 2}
+
+
+def sfar_test_set_fused_path(h, path="auto") -> int:
+    return lib().sfar_test_set_fused_path(h, FUSED_PATHS[path] if isinstance(path, str) else int(path))
+
+
+def sfar_test_query_fused_path(h, rows: int, hidden: int):
+    """(status, path) of sfar_allreduce_add_rmsnorm: 1 one-shot, 2 two-shot."""
+    p = ctypes.c_int(0)
+    code = lib().sfar_test_query_fused_path(h, rows, hidden, ctypes.byref(p))
+    return code, p.value
 
 
 def sfar_allreduce_noalloc(in_ptrs, out_ptrs, R: int, n: int, dtype="bf16", stream=None) -> int:

@@ -495,7 +495,8 @@ def run_suite(args):
         # AllReduce + residual add + RMSNorm in one kernel against the two-kernel
         # pipeline (LL AllReduce, then the normalisation kernel)
         import oracle
-        for R, rows, hidden in ((8, 1, 8192), (8, 64, 7168), (4, 1, 8192), (16, 1, 8192), (8, 4, 8192)):
+        for R, rows, hidden in ((8, 1, 8192), (8, 64, 7168), (4, 1, 8192), (16, 1, 8192), (8, 4, 8192),
+                                (8, 8, 8192), (8, 16, 7168), (16, 64, 7168)):
             if args.suite_r and R != args.suite_r:
                 continue
             calls, eps = 32, 1e-5
@@ -520,6 +521,12 @@ def run_suite(args):
                                              hidden, eps)
 
             row = {"suite": "fused", "R": R, "rows": rows, "hidden": hidden, "bytes_per_rank": 2 * n}
+            row["fused_path"] = {1: "oneshot", 2: "twoshot"}[sfar.sfar_test_query_fused_path(h.h, rows, hidden)[1]]
+            for path in ("oneshot", "twoshot"):          # each kernel forced, where the shape allows it
+                sfar.sfar_test_set_fused_path(h.h, path)
+                if sfar.sfar_test_query_fused_path(h.h, rows, hidden) == (sfar.SFAR_OK, 1 if path == "oneshot" else 2):
+                    row[f"fused_{path}_us"] = round(_time_calls(h, calls, [fused]), 3)
+            sfar.sfar_test_set_fused_path(h.h, "auto")
             row["fused_us"] = round(_time_calls(h, calls, [fused]), 3)
             ok = True
             for c in (0, calls - 1):

@@ -95,8 +95,8 @@ typedef int sfar_status;
 #define SFAR_WAIT_LL128 6     /* LL128 line flag (one-shot)                            */
 #define SFAR_WAIT_RS 7        /* two-shot reduce-scatter line flag                     */
 #define SFAR_WAIT_AG 8        /* two-shot all-gather line flag                         */
-#define SFAR_WAIT_ARRIVE 9    /* TMA path: peer arrival (top barrier)                  */
-#define SFAR_WAIT_COMPLETE 10 /* TMA path: owner completion flags                      */
+#define SFAR_WAIT_ARRIVE 9    /* TMA / two-shot fused: peer arrival (top barrier)      */
+#define SFAR_WAIT_COMPLETE 10 /* TMA / two-shot fused: owner completion flags          */
 #define SFAR_WAIT_COPY 11     /* TMA path: bulk copy completion                        */
 #define SFAR_WAIT_COUNTER 12  /* atomic path: a line's arrival counter stayed below R  */
 #define SFAR_WAIT_CLUSTER 13  /* fused normalisation: a cluster peer's row statistics
@@ -212,7 +212,12 @@ size_t sfar_max_bytes(const sfar_t *h, sfar_proto p);
  * residual_out[r] may be residual[r] (in place); otherwise no output may
  * overlap an input, the weight or another output.  rows == 0 is a no-op.
  * One kernel on stream s (thread-block clusters, one cluster per row at a
- * time); capturable; errors as for sfar_allreduce.
+ * time); capturable; errors as for sfar_allreduce.  The kernel depends on
+ * the shape, the result does not: the one-shot kernel over LL packets, or,
+ * when that kernel would stack several rows on a cluster and rows are at
+ * most 32 KB, a two-shot kernel ("SiFAR" (page 3), "Limits of existing
+ * algorithms") in which the owner of a row reads it from every rank once and
+ * writes every rank's z and y.
  */
 sfar_status sfar_allreduce_add_rmsnorm(sfar_t *h, const void *const in[], const void *const residual[],
                                        const void *weight, void *const out[], void *const residual_out[],

@@ -94,6 +94,19 @@ sfar_status sfar_test_set_geometry(sfar_t *h, int ctas_per_rank, int threads_per
 sfar_status sfar_test_query_norm_launch(sfar_t *h, size_t rows, size_t hidden, int allreduce, int *ctas_per_rank,
                                         int *cluster_size, int *threads_per_cta);
 
+/* Kernel of every later sfar_allreduce_add_rmsnorm call: path 0 = chosen by
+ * shape (default), 1 = the one-shot kernel over LL packets, 2 = the two-shot
+ * kernel (each row reduced once by an owner cluster that normalises it for
+ * every rank; rows of at most 32 KB whose grid can be resident at once,
+ * other shapes keep path 1).
+ * SFAR_ERR_INVALID for another value.  Host-side; no launch. */
+sfar_status sfar_test_set_fused_path(sfar_t *h, int path);
+
+/* Which kernel sfar_allreduce_add_rmsnorm would launch for rows x hidden
+ * under the current setting: *path = 1 (one-shot) or 2 (two-shot).  Returns
+ * what the call would return for the shape, without launching anything. */
+sfar_status sfar_test_query_fused_path(sfar_t *h, size_t rows, size_t hidden, int *path);
+
 /*
  * Latency floor probes.
  * sfar_probe_empty: enqueue one empty kernel (1 CTA, 32 threads) on s.

@@ -80,12 +80,14 @@ SHAPES = {"bf16": [(1, 8192), (3, 7168), (5, 64), (2, 8), (1, 24), (4, 1000), (2
           "fp32": [(1, 8192), (3, 7168), (5, 64), (2, 4), (1, 20), (4, 1000), (1, 32768), (32, 4096)]}
 
 
+@pytest.mark.parametrize("path", ["auto", "oneshot"])
 @pytest.mark.parametrize("dtype", ["bf16", "fp32"])
 @pytest.mark.parametrize("R", [2, 3, 8, 16])
-def test_fused_parity(R, dtype):
+def test_fused_parity(R, dtype, path):
     h = sfar.Sfar(R, 1 << 20, dtype)
     es = 2 if dtype == "bf16" else 4
     try:
+        assert sfar.sfar_test_set_fused_path(h.h, path) == sfar.SFAR_OK
         for rows, hidden in SHAPES[dtype]:
             code, k, cl, t = sfar.sfar_test_query_norm_launch(h.h, rows, hidden)
             if R > 8 and hidden * es > 65536:
@@ -93,7 +95,8 @@ def test_fused_parity(R, dtype):
                 continue
             assert code == sfar.SFAR_OK and k % cl == 0 and 1 <= cl <= 8 and t in (32, 64, 128, 256)
             x, res, w = draw_case(500 + R + rows, R, rows, hidden, dtype)
-            check(h, x, res, w, hidden, 1e-5, f"R={R} {rows}x{hidden} {dtype} ({k} CTAs/rank, cluster {cl}, {t})")
+            check(h, x, res, w, hidden, 1e-5,
+                  f"{path} R={R} {rows}x{hidden} {dtype} ({k} CTAs/rank, cluster {cl}, {t})")
     finally:
         h.close()
 
@@ -244,6 +247,7 @@ def test_dropped_rank_times_out_and_reset_recovers():
     R, rows, hidden = 4, 2, 4096
     h = sfar.Sfar(R, 1 << 16, "bf16")
     try:
+        assert sfar.sfar_test_set_fused_path(h.h, "oneshot") == sfar.SFAR_OK
         x, res, w = draw_case(960, R, rows, hidden, "bf16")
         check(h, x, res, w, hidden, 1e-5, "before")
         assert sfar.sfar_test_set_timeout(h.h, 2_000_000) == sfar.SFAR_OK
@@ -304,5 +308,197 @@ def test_fused_chain_overlap_with_straggler(phase):
         for r in range(R):
             assert_equal_nan_aware(got_z[r], want_z[r], f"straggler {phase} z rank {r}")
             assert_equal_nan_aware(got_y[r], want_y[r], f"straggler {phase} y rank {r}")
+    finally:
+        h.close()
+
+
+# ------------------------------------------------------- two-shot fused kernel
+def force_two_shot(h, rows, hidden):
+    code, path = sfar.sfar_test_query_fused_path(h.h, rows, hidden)
+    assert code == sfar.SFAR_OK and path == 2, (code, path)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp32"])
+@pytest.mark.parametrize("R", [2, 3, 8, 16])
+def test_two_shot_parity(R, dtype):
+    """Every shape whose rows fit the two-shot kernel (at most 32 KB), with
+    the kernel forced: the same bits as the oracle on every rank."""
+    h = sfar.Sfar(R, 1 << 20, dtype)
+    es = 2 if dtype == "bf16" else 4
+    try:
+        assert sfar.sfar_test_set_fused_path(h.h, "twoshot") == sfar.SFAR_OK
+        for rows, hidden in SHAPES[dtype] + [(7, 2048 // es), (R + 1, 4096 // es)]:
+            code, path = sfar.sfar_test_query_fused_path(h.h, rows, hidden)
+            if hidden * es > 32768:
+                assert code != sfar.SFAR_OK or path == 1              # rows above 32 KB keep the one-shot kernel
+                continue
+            if path == 1:
+                # the two-shot grid cannot be resident at once: R = 16 with rows above 16 KB (clusters of
+                # up to 8 CTAs of 256 threads, one CTA per SM)
+                assert R == 16 and hidden * es > 16384, (R, rows, hidden, dtype)
+                continue
+            force_two_shot(h, rows, hidden)
+            x, res, w = draw_case(1000 + R + rows, R, rows, hidden, dtype)
+            check(h, x, res, w, hidden, 1e-5, f"two-shot R={R} {rows}x{hidden} {dtype}")
+    finally:
+        h.close()
+
+
+def test_two_shot_in_place_and_special_rows():
+    R, hidden = 4, 1024
+    h = sfar.Sfar(R, 1 << 20, "fp32")
+    try:
+        assert sfar.sfar_test_set_fused_path(h.h, "twoshot") == sfar.SFAR_OK
+        force_two_shot(h, 6, hidden)
+        x, res, w = draw_case(1101, R, 6, hidden, "fp32")
+        res[:, :hidden] = 0.0
+        x[:, :hidden] = 0.0                          # row 0: all zero
+        x[1, hidden + 7] = float("nan")              # row 1: NaN
+        res[2, 2 * hidden + 9] = float("inf")        # row 2: an infinity on rank 2 only
+        x[:, 3 * hidden:4 * hidden] *= 2.0 ** 60     # row 3: large
+        x[:, 4 * hidden:5 * hidden] *= 2.0 ** -70    # row 4: tiny (subnormal squares)
+        res[:, 4 * hidden:5 * hidden] *= 2.0 ** -70
+        check(h, x, res, w, hidden, 1e-6, "two-shot special rows")
+        check(h, x, res, w, hidden, 1e-6, "two-shot in place", in_place=True)
+    finally:
+        h.close()
+
+
+def test_shape_chooses_the_kernel():
+    R = 8
+    h = sfar.Sfar(R, 2 << 20, "bf16")
+    try:
+        assert sfar.sfar_test_query_fused_path(h.h, 1, 8192) == (sfar.SFAR_OK, 1)
+        assert sfar.sfar_test_query_fused_path(h.h, 64, 7168) == (sfar.SFAR_OK, 2)
+        assert sfar.sfar_test_query_fused_path(h.h, 8, 32768)[1] == 1          # 64 KB rows: one-shot only
+        assert sfar.sfar_test_set_fused_path(h.h, "oneshot") == sfar.SFAR_OK
+        assert sfar.sfar_test_query_fused_path(h.h, 64, 7168) == (sfar.SFAR_OK, 1)
+        assert sfar.sfar_test_set_fused_path(h.h, 3) == sfar.SFAR_ERR_INVALID
+    finally:
+        h.close()
+
+
+@pytest.mark.parametrize("mode", ["serial", "overlap"])
+def test_two_shot_chain_with_other_calls(mode):
+    """256 graph-chained calls that cycle through the two-shot fused kernel
+    (4 rows), the one-shot fused kernel (1 row), the two-shot TMA AllReduce
+    (which shares the arrival and completion flags) and the LL AllReduce,
+    each with its own inputs: every result bit for bit.  Each fused call has
+    its kernel forced."""
+    R, hidden, calls, eps = 8, 8192, 256, 1e-5
+    rows_of = lambda c: 4 if c % 4 == 0 else 1
+    x = torch.stack([inputs.draw(1200, c, R, 4 * hidden, "normal", 1.0, "bf16") for c in range(calls)])
+    res = torch.stack([inputs.draw(1201, c, R, 4 * hidden, "normal", 2.0, "bf16") for c in range(calls)])
+    w = inputs.draw(1202, 0, 1, hidden, "normal", 1.0, "bf16")[0]
+    h = sfar.Sfar(R, 8 * hidden, "bf16")
+    try:
+        h.set_mode(mode)
+        xd, rd, wd = x.cuda(), res.cuda(), w.cuda()
+        od, zd = torch.empty_like(xd), torch.empty_like(xd)
+        P = lambda t, c: [t[c, r].data_ptr() for r in range(R)]
+
+        def call(c):
+            kind = c % 4
+            if kind in (0, 1):
+                # the kernel is chosen when the call is enqueued (here: captured)
+                assert sfar.sfar_test_set_fused_path(h.h, "twoshot" if kind == 0 else "oneshot") == sfar.SFAR_OK
+                assert sfar.sfar_test_query_fused_path(h.h, rows_of(c), hidden) == (sfar.SFAR_OK, 2 - kind)
+                return sfar.sfar_allreduce_add_rmsnorm(h.h, P(xd, c), P(rd, c), wd.data_ptr(), P(od, c), P(zd, c),
+                                                       rows_of(c), hidden, eps)
+            return sfar.sfar_allreduce(h.h, P(xd, c), P(od, c), 4 * hidden, "twoshot_tma" if kind == 2 else "ll")
+
+        assert call(0) == sfar.SFAR_OK
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            for c in range(calls):
+                assert call(c) == sfar.SFAR_OK
+        od.view(torch.int16).fill_(-1)
+        graph.replay()
+        torch.cuda.synchronize()
+        status_ok(h.h, f"mixed chain {mode}")
+        wb = inputs.to_bits(w[None, :])[0]
+        for c in range(calls):
+            n = rows_of(c) * hidden
+            xb = inputs.to_bits(x[c, :, :n]) if c % 4 in (0, 1) else inputs.to_bits(x[c])
+            if c % 4 in (0, 1):
+                want_y, want_z = oracle.add_rmsnorm(xb, inputs.to_bits(res[c, :, :n]), wb, eps, hidden)
+                for r in range(R):
+                    assert_equal_nan_aware(zd[c, r, :n], want_z[r], f"{mode} call {c} z rank {r}")
+                    assert_equal_nan_aware(od[c, r, :n], want_y[r], f"{mode} call {c} y rank {r}")
+            else:
+                want = oracle.allreduce(xb)
+                for r in range(R):
+                    assert np.array_equal(inputs.to_bits(od[c, r].cpu()), want[r]), f"{mode} call {c} rank {r}"
+    finally:
+        h.close()
+
+
+@pytest.mark.parametrize("phase", [0, 1])
+def test_two_shot_chain_with_straggler(phase):
+    """256 graph-chained two-shot calls (8 rows of 7168 bf16, R = 8) in
+    overlap mode with one rank (rotating) delayed by 0-20 us before its
+    arrival (phase 0) or between its arrival and its reads (phase 1)."""
+    R, rows, hidden, calls, eps = 8, 8, 7168, 256, 1e-5
+    n = rows * hidden
+    x = torch.stack([inputs.draw(1300, c, R, n, "normal", 1.0, "bf16") for c in range(calls)])
+    res = torch.stack([inputs.draw(1301, c, R, n, "normal", 2.0, "bf16") for c in range(calls)])
+    w = inputs.draw(1302, 0, 1, hidden, "normal", 1.0, "bf16")[0]
+    h = sfar.Sfar(R, 2 * n, "bf16")
+    try:
+        h.set_mode("overlap")
+        assert sfar.sfar_test_set_fused_path(h.h, "twoshot") == sfar.SFAR_OK
+        force_two_shot(h, rows, hidden)
+        xd, rd, wd = x.cuda(), res.cuda(), w.cuda()
+        od, zd = torch.empty_like(xd), torch.empty_like(xd)
+        P = lambda t, c: [t[c, r].data_ptr() for r in range(R)]
+        g = torch.Generator().manual_seed(1303)
+        delays = torch.randint(0, 20001, (calls,), generator=g).to(torch.int32).cuda()
+        assert sfar.sfar_allreduce_add_rmsnorm(h.h, P(xd, 0), P(rd, 0), wd.data_ptr(), P(od, 0), P(zd, 0), rows,
+                                               hidden, eps) == sfar.SFAR_OK
+        torch.cuda.synchronize()
+        assert sfar.sfar_test_set_straggler(h.h, delays.data_ptr(), calls, -1, phase) == sfar.SFAR_OK
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            for c in range(calls):
+                assert sfar.sfar_allreduce_add_rmsnorm(h.h, P(xd, c), P(rd, c), wd.data_ptr(), P(od, c), P(zd, c),
+                                                       rows, hidden, eps) == sfar.SFAR_OK
+        graph.replay()
+        torch.cuda.synchronize()
+        status_ok(h.h, f"two-shot straggler phase {phase}")
+        want_y, want_z = oracle.add_rmsnorm(inputs.to_bits(x.transpose(0, 1).reshape(R, calls * n)),
+                                            inputs.to_bits(res.transpose(0, 1).reshape(R, calls * n)),
+                                            inputs.to_bits(w[None, :])[0], eps, hidden)
+        got_y = od.transpose(0, 1).reshape(R, calls * n)
+        got_z = zd.transpose(0, 1).reshape(R, calls * n)
+        for r in range(R):
+            assert_equal_nan_aware(got_z[r], want_z[r], f"two-shot straggler {phase} z rank {r}")
+            assert_equal_nan_aware(got_y[r], want_y[r], f"two-shot straggler {phase} y rank {r}")
+    finally:
+        h.close()
+
+
+def test_two_shot_dropped_rank_times_out_and_reset_recovers():
+    R, rows, hidden = 4, 8, 4096
+    h = sfar.Sfar(R, 1 << 17, "bf16")
+    try:
+        assert sfar.sfar_test_set_fused_path(h.h, "twoshot") == sfar.SFAR_OK
+        force_two_shot(h, rows, hidden)
+        x, res, w = draw_case(1400, R, rows, hidden, "bf16")
+        check(h, x, res, w, hidden, 1e-5, "two-shot before")
+        assert sfar.sfar_test_set_timeout(h.h, 2_000_000) == sfar.SFAR_OK
+        assert sfar.sfar_test_drop_rank(h.h, 1) == sfar.SFAR_OK
+        ins = [t.cuda() for t in x]
+        rs = [t.cuda() for t in res]
+        outs = [torch.empty_like(t) for t in ins]
+        zs = [torch.empty_like(t) for t in ins]
+        h.allreduce_add_rmsnorm(ins, rs, w.cuda(), outs, zs, hidden, 1e-5)
+        torch.cuda.synchronize()
+        code, f = sfar.sfar_status_get(h.h)
+        assert code == sfar.SFAR_ERR_TIMEOUT and sfar.WAIT_NAMES[f.where] in ("arrive", "complete")
+        h.reset()
+        assert sfar.sfar_test_drop_rank(h.h, -1) == sfar.SFAR_OK
+        torch.cuda.synchronize()
+        check(h, x, res, w, hidden, 1e-5, "two-shot after reset")
     finally:
         h.close()
