@@ -497,7 +497,7 @@ def run_suite(args):
         import oracle
         for R, rows, hidden in ((8, 1, 8192), (8, 64, 7168), (4, 1, 8192), (16, 1, 8192), (8, 4, 8192),
                                 (8, 8, 8192), (8, 16, 7168), (16, 64, 7168)):
-            if args.suite_r and R != args.suite_r:
+            if (args.suite_r and R != args.suite_r) or (args.suite_rows and rows != args.suite_rows):
                 continue
             calls, eps = 32, 1e-5
             n = rows * hidden
@@ -862,6 +862,7 @@ def main():
     ap.add_argument("--large-mb", type=int, default=64)
     ap.add_argument("--large-dtype", choices=["bf16", "fp32"], default="bf16")
     ap.add_argument("--suite-r", type=int, default=0, help="atomic and fused suites: only this rank count")
+    ap.add_argument("--suite-rows", type=int, default=0, help="fused suite: only this row count")
     ap.add_argument("--suite-bytes", type=int, default=0, help="atomic suite: only this message size per rank")
     ap.add_argument("--decode-layers", type=int, default=80, help="decode suite: layers per token")
     ap.add_argument("--suite", default="", help="comma list of latency,bandwidth,barriers,atomic,fused,decode: sweeps as JSON lines")
