@@ -38,6 +38,31 @@ __device__ __forceinline__ unsigned long long sq_term(float v, int E, int F)
     return -sh >= 64 ? 0ull : (m2 >> (-sh));
 }
 
+// The same truncated square for values of at most 8 significant bits (bf16
+// elements), in binary32: v is scaled by 2^k, k = floor(F/2) - E, in two
+// exact steps (each factor within 2^-55 .. 2^87), so |v 2^k| < 2^26 and its
+// square has at most 16 significant bits: exact whenever it is normal, and
+// below 1 (truncating to 0 either way) when it is not.  The square, doubled
+// when F is odd (exact), truncated to an integer is floor(v^2 2^(F - 2E)).
+struct SqScale {
+    float s1, s2;
+    bool odd;
+};
+__device__ __forceinline__ SqScale sq_scale(int E, int F)
+{
+    const int k = (F >> 1) - E;
+    const int k1 = k >> 1, k2 = k - k1;
+    return {__int_as_float((127 + k1) << 23), __int_as_float((127 + k2) << 23), (F & 1) != 0};
+}
+__device__ __forceinline__ unsigned long long sq_term_narrow(float v, const SqScale &s)
+{
+    const float vs = __fmul_rn(__fmul_rn(v, s.s1), s.s2);
+    float t = __fmul_rn(vs, vs);
+    if (s.odd)
+        t = __fmul_rn(t, 2.0f);
+    return __float2ull_rz(t);
+}
+
 __device__ __forceinline__ float mean_square(uint32_t M, unsigned long long S, unsigned long long h, int F)
 {
     if (M > 0x7f800000u)

@@ -331,9 +331,16 @@ __global__ void __launch_bounds__(SFAR_NORM_THREADS, UB == 8 && RB <= 8 ? 2 : 1)
             const int bq = NB == 1 ? 0 : q;
             if (valid[q] && M[bq] != 0 && M[bq] < 0x7f800000u) {
                 const int E = exp_above(M[bq]);
+                if (DT == 0) {
+                    const SqScale sc = sq_scale(E, na.F);
 #pragma unroll
-                for (int t = 0; t < NE; ++t)
-                    lsum[bq] += sq_term(V::get(zv[q], t), E, na.F);
+                    for (int t = 0; t < NE; ++t)
+                        lsum[bq] += sq_term_narrow(V::get(zv[q], t), sc);
+                } else {
+#pragma unroll
+                    for (int t = 0; t < NE; ++t)
+                        lsum[bq] += sq_term(V::get(zv[q], t), E, na.F);
+                }
             }
         }
 #pragma unroll

@@ -26,11 +26,14 @@
 //   2. forms z_p for every rank p and the largest |z_p| (R maxima per warp,
 //      round 1 of the cluster exchange), then the truncated squares of every
 //      z_p summed as integers (R sums per warp, round 2);
-//   3. writes z_p and y_p into rank p's buffers.
+//   3. writes z_p into rank p's residual output as soon as it is formed, and
+//      y_p into rank p's output after the statistics.
 // The exchange is the one of the one-shot fused kernel: every warp stores its
 // partials into its slot in every cluster CTA's shared memory (st.async,
 // counted in bytes by that CTA's mbarrier); lane p of each warp then combines
-// rank p's slots and hands the result to the warp by shuffle.
+// rank p's slots and hands the result to the warp by shuffle.  The R sums of
+// a warp are reduced transposed (warp_sums_transposed), so the exchange costs
+// a handful of shuffles rather than R full warp reductions.
 //
 // Synchronisation between simulated ranks (as the two-shot TMA kernel: the
 // pages' counters reaching N, page 1 section "Four barrier-free mechanisms",
@@ -60,6 +63,43 @@ __device__ __forceinline__ uint32_t unit_max(const uint4 &z)
     return m;
 }
 
+__device__ __forceinline__ unsigned long long shfl_xor_u64(unsigned long long x, int m)
+{
+    const uint32_t lo = __shfl_xor_sync(SFAR_FULL, (uint32_t)x, m);
+    const uint32_t hi = __shfl_xor_sync(SFAR_FULL, (uint32_t)(x >> 32), m);
+    return ((unsigned long long)hi << 32) | lo;
+}
+
+// Warp sums of the RB (8 or 16) values of every lane, transposed: each xor
+// step from 16 down keeps half of a lane's values and adds its partner's copy
+// of them, until one value is left, and the last steps add it over the
+// remaining lanes.  Lane l ends with the warp sum of value
+// (l >> (5 - log2 RB)) & (RB - 1): log2(RB) + 1 ... 5 exchanges instead of
+// RB * 5.
+template <int RB>
+__device__ __forceinline__ unsigned long long warp_sums_transposed(unsigned long long (&v)[RB], int lane)
+{
+    constexpr int LOG = RB == 16 ? 4 : 3;
+#pragma unroll
+    for (int s = 0; s < LOG; ++s) {
+        const int n = RB >> (s + 1);
+        const int off = 16 >> s;
+        const bool up = (lane & off) != 0;
+#pragma unroll
+        for (int j = 0; j < RB / 2; ++j) {
+            if (j < n) {
+                const unsigned long long keep = up ? v[j + n] : v[j];
+                const unsigned long long give = up ? v[j] : v[j + n];
+                v[j] = keep + shfl_xor_u64(give, off);
+            }
+        }
+    }
+#pragma unroll
+    for (int off = 16 >> LOG; off > 0; off >>= 1)
+        v[0] += shfl_xor_u64(v[0], off);
+    return v[0];
+}
+
 template <int DT, int RB, bool TEST>
 __global__ void __launch_bounds__(SFAR_NORM_THREADS, RB <= 8 ? 2 : 1)
     k_fused_ts(const __grid_constant__ SfarArgs a, const __grid_constant__ SfarNormArgs na)
@@ -84,7 +124,7 @@ __global__ void __launch_bounds__(SFAR_NORM_THREADS, RB <= 8 ? 2 : 1)
     __shared__ int s_ok;
     const uint32_t mb_max = smem_u32(&s_mbar[0]), mb_sum = smem_u32(&s_mbar[1]);
     const int W = T >> 5, nslots = CL * W, slot = cr * W + warp;
-    const int R4 = (R + 3) >> 2, R2 = (R + 1) >> 1;               // 16-byte stores per slot and round
+    const int R4 = (R + 3) >> 2;                  // 16-byte stores per slot in round 1
 
     const bool works = has_u && i0 < rows;
     if (works)
@@ -180,6 +220,7 @@ __global__ void __launch_bounds__(SFAR_NORM_THREADS, RB <= 8 ? 2 : 1)
                         zf[t] = __fadd_rn(V::get(av, t), V::get(zs[p], t));
                     zs[p] = V::pack(zf);
                     lmax[p] = unit_max<DT>(zs[p]);
+                    st_v4((char *)na.res_out[p] + off, zs[p]);     // z is final: stored now
                 }
             }
         }
@@ -224,24 +265,28 @@ __global__ void __launch_bounds__(SFAR_NORM_THREADS, RB <= 8 ? 2 : 1)
             lsum[p] = 0ull;
             if (p < R && M[p] != 0 && M[p] < 0x7f800000u) {
                 const int E = exp_above(M[p]);
+                if (DT == 0) {
+                    const SqScale sc = sq_scale(E, na.F);
 #pragma unroll
-                for (int t = 0; t < V::N; ++t)
-                    lsum[p] += sq_term(V::get(zs[p], t), E, na.F);
+                    for (int t = 0; t < V::N; ++t)
+                        lsum[p] += sq_term_narrow(V::get(zs[p], t), sc);
+                } else {
+#pragma unroll
+                    for (int t = 0; t < V::N; ++t)
+                        lsum[p] += sq_term(V::get(zs[p], t), E, na.F);
+                }
             }
         }
-#pragma unroll
-        for (int p = 0; p < RB; ++p)
-            if (p < R)
-                lsum[p] = warp_sum_u64(lsum[p]);
+        // lane l holds the warp sum of rank (l >> SH) & (RB - 1); the 2^SH lanes
+        // holding rank p's sum send it to cluster CTAs c, c + 2^SH, ...
+        constexpr int SH = RB == 16 ? 1 : 2;
+        const unsigned long long wsum = warp_sums_transposed<RB>(lsum, lane);
+        const int psum = (lane >> SH) & (RB - 1);
         if (tid == 0)
-            mbar_arrive_expect_tx(mb_sum, (uint32_t)(nslots * R2 * 16));
-        if (lane < CL) {
-#pragma unroll
-            for (int b = 0; b < RB / 2; ++b)
-                if (b < R2)
-                    st_async_v2u64(map_cta(smem_u32(&s_sum[slot][2 * b]), lane), lsum[2 * b], lsum[2 * b + 1],
-                                   map_cta(mb_sum, lane));
-        }
+            mbar_arrive_expect_tx(mb_sum, (uint32_t)(nslots * R * 8));
+        if (psum < R)
+            for (int dst = lane & ((1 << SH) - 1); dst < CL; dst += 1 << SH)
+                st_async_u64(map_cta(smem_u32(&s_sum[slot][psum]), dst), wsum, map_cta(mb_sum, dst));
         if (!cluster_mbar_wait(mb_sum, phase, a.ctl, r, k, e))
             ok = false;
         phase ^= 1u;
@@ -265,7 +310,6 @@ __global__ void __launch_bounds__(SFAR_NORM_THREADS, RB <= 8 ? 2 : 1)
 #pragma unroll
                 for (int t = 0; t < V::N; ++t)
                     yf[t] = __fmul_rn(__fmul_rn(V::get(zs[p], t), rs), V::get(wv, t));
-                st_v4((char *)na.res_out[p] + off, zs[p]);
                 st_v4((char *)a.out[p] + off, V::pack(yf));
             }
         }

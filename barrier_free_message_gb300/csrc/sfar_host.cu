@@ -617,13 +617,26 @@ static int norm_max_clusters(sfar *h, int allreduce, int test, int batch, int un
     return slot;
 }
 
+// A fused AllReduce grid whose clusters take more than three quarters of
+// `maxc` (the co-resident clusters that the occupancy query reports for an
+// idle device) runs solo: launched without programmatic overlap, it starts on
+// an idle device and lets no successor launch before it ends.  Every CTA of
+// such a grid waits on others, and a large cluster grid launched early, while
+// its predecessor still held the device, did not always get all of its
+// clusters placed: R = 8, eight rows of 8192 bf16, 32 of 36 clusters of 8
+// CTAs, timed out on its last rank in 12 of 40 graph replays of 32 calls with
+// overlap and in none without.  Grids at 70% and 79% of `maxc` ran thousands
+// of overlapped calls without a stall.
+static bool solo_grid(int clusters, int maxc) { return 4 * clusters > 3 * maxc; }
+
 // Launch shape of a fused call: threads per CTA, cluster size (shrunk from
 // the preferred one while R clusters cannot be resident at once), clusters
 // per rank G (K = G * CL <= KMAX), vectors of a row per thread, and rows per
 // statistics round (up to 4 when every thread holds one vector of each row
 // and a cluster gets more than one row).
 static sfar_status norm_geometry(sfar *h, int allreduce, int test, size_t rows, unsigned long long VR, int unit,
-                                 int *CL_out, int *G_out, int *threads_out, int *vpt_out, int *batch_out)
+                                 int *CL_out, int *G_out, int *threads_out, int *vpt_out, int *batch_out,
+                                 int *maxc_out)
 {
     int CL = 0, CLmin = 0, ti = 0;
     if (!norm_shape(VR, unit, &CL, &CLmin, &ti))
@@ -658,6 +671,7 @@ static sfar_status norm_geometry(sfar *h, int allreduce, int test, size_t rows, 
         B = ceil_div(rows, G);                    // no more rows per round than a cluster gets
     *CL_out = CL;
     *G_out = (int)G;
+    *maxc_out = maxc;
     *threads_out = kNormThreads[ti];
     *vpt_out = vpt;
     *batch_out = (int)B;
@@ -670,7 +684,7 @@ static sfar_status norm_geometry(sfar *h, int allreduce, int test, size_t rows, 
 // many as the rows need, all of the grid resident at once (its CTAs wait on
 // one another).
 static sfar_status ts_geometry(sfar *h, int test, size_t rows, unsigned long long VR, int *CL_out, int *G_out,
-                               int *threads_out)
+                               int *threads_out, int *maxc_out)
 {
     const int ti = VR <= 32 ? 0 : VR <= 64 ? 1 : VR <= 1024 ? 2 : 3;
     const size_t CL = ceil_div(VR, (size_t)kNormThreads[ti]);
@@ -713,6 +727,7 @@ static sfar_status ts_geometry(sfar *h, int test, size_t rows, unsigned long lon
     *CL_out = (int)CL;
     *G_out = (int)(G < 1 ? 1 : G);
     *threads_out = kNormThreads[ti];
+    *maxc_out = slot;
     return SFAR_OK;
 }
 
@@ -730,33 +745,37 @@ static sfar_status ts_geometry(sfar *h, int test, size_t rows, unsigned long lon
 // kernel over LL packets; it also takes the shapes whose two-shot grid
 // cannot be resident at once.
 static sfar_status norm_plan(sfar *h, int allreduce, int test, size_t rows, size_t row_bytes, int *path, int *unit,
-                             int *CL, int *G, int *threads, int *vpt, int *batch)
+                             int *CL, int *G, int *threads, int *vpt, int *batch, int *maxc)
 {
     const bool ts_fits = allreduce && row_bytes <= 32768;
     *vpt = 1;
     *batch = 1;
-    if (ts_fits && h->fused_path == 2 && ts_geometry(h, test, rows, row_bytes / 16, CL, G, threads) == SFAR_OK) {
+    if (ts_fits && h->fused_path == 2 &&
+        ts_geometry(h, test, rows, row_bytes / 16, CL, G, threads, maxc) == SFAR_OK) {
         *path = 2;
         *unit = 16;
         return SFAR_OK;
     }
     *path = 1;
     if (allreduce && row_bytes <= 16384) {
-        const sfar_status st = norm_geometry(h, allreduce, test, rows, row_bytes / 8, 8, CL, G, threads, vpt, batch);
+        const sfar_status st =
+            norm_geometry(h, allreduce, test, rows, row_bytes / 8, 8, CL, G, threads, vpt, batch, maxc);
         if (st == SFAR_OK && (size_t)*G >= rows) {
             *unit = 8;
             return SFAR_OK;
         }
     }
     *unit = 16;
-    const sfar_status st = norm_geometry(h, allreduce, test, rows, row_bytes / 16, 16, CL, G, threads, vpt, batch);
+    const sfar_status st =
+        norm_geometry(h, allreduce, test, rows, row_bytes / 16, 16, CL, G, threads, vpt, batch, maxc);
     if (ts_fits && h->fused_path == 0 && (st != SFAR_OK || (size_t)*G < rows)) {
-        int tCL = 0, tG = 0, tT = 0;
-        if (ts_geometry(h, test, rows, row_bytes / 16, &tCL, &tG, &tT) == SFAR_OK) {
+        int tCL = 0, tG = 0, tT = 0, tmax = 0;
+        if (ts_geometry(h, test, rows, row_bytes / 16, &tCL, &tG, &tT, &tmax) == SFAR_OK) {
             *path = 2;
             *CL = tCL;
             *G = tG;
             *threads = tT;
+            *maxc = tmax;
             *vpt = 1;
             *batch = 1;
             return SFAR_OK;
@@ -818,9 +837,9 @@ static sfar_status fused_call(sfar *h, const void *const in[], const void *const
         }
     }
     const int test = allreduce && (h->k_strag || h->k_drop || h->k_single) ? 1 : 0;
-    int path = 1, unit = 16, CL = 0, G = 0, threads = 0, vpt = 1, batch = 1;
+    int path = 1, unit = 16, CL = 0, G = 0, threads = 0, vpt = 1, batch = 1, maxc = 0;
     const sfar_status gst =
-        norm_plan(h, allreduce, test, rows, hidden * es, &path, &unit, &CL, &G, &threads, &vpt, &batch);
+        norm_plan(h, allreduce, test, rows, hidden * es, &path, &unit, &CL, &G, &threads, &vpt, &batch, &maxc);
     if (gst != SFAR_OK)
         return gst;
     const unsigned long long VR = hidden * es / (size_t)unit;
@@ -863,9 +882,11 @@ static sfar_status fused_call(sfar *h, const void *const in[], const void *const
         ++c;
     na.F = 53 - c;
     a.overlap = 0;
-    if (path == 2) {
-        // the two-shot kernel never overtakes a call, and the call after it
-        // does not overtake it: it starts with serial semantics
+    const bool solo = allreduce && solo_grid(R * G, maxc);
+    a.solo = solo ? 1 : 0;
+    if (path == 2 || solo) {
+        // the two-shot kernel and a solo grid never overtake a call, and the
+        // call after them does not overtake them: serial semantics
         h->last_key = -1;
     } else if (allreduce && h->mode == SFAR_LAUNCH_OVERLAP) {
         // the unit -> CTA mapping depends on the cluster shape, the row
@@ -898,7 +919,7 @@ static sfar_status fused_call(sfar *h, const void *const in[], const void *const
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     int na_attr = 1;
-    if (h->mode != SFAR_LAUNCH_PLAIN) {
+    if (h->mode != SFAR_LAUNCH_PLAIN && !solo) {
         attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
         attr[1].val.programmaticStreamSerializationAllowed = 1;
         na_attr = 2;
@@ -928,9 +949,9 @@ sfar_status sfar_test_query_norm_launch(sfar_t *h, size_t rows, size_t hidden, i
     const size_t row = hidden * (size_t)h->es;
     if (row > 131072 || (h->R > 8 && row > 65536))
         return SFAR_ERR_INVALID;
-    int path = 1, unit = 16, CL = 0, G = 0, threads = 0, vpt = 1, batch = 1;
+    int path = 1, unit = 16, CL = 0, G = 0, threads = 0, vpt = 1, batch = 1, maxc = 0;
     const sfar_status st =
-        norm_plan(h, allreduce ? 1 : 0, 0, rows, row, &path, &unit, &CL, &G, &threads, &vpt, &batch);
+        norm_plan(h, allreduce ? 1 : 0, 0, rows, row, &path, &unit, &CL, &G, &threads, &vpt, &batch, &maxc);
     if (st != SFAR_OK)
         return st;
     if (ctas_per_rank)
@@ -1155,8 +1176,8 @@ sfar_status sfar_test_query_fused_path(sfar_t *h, size_t rows, size_t hidden, in
     const size_t row = hidden * (size_t)h->es;
     if (row > 131072 || (h->R > 8 && row > 65536))
         return SFAR_ERR_INVALID;
-    int unit = 16, CL = 0, G = 0, threads = 0, vpt = 1, batch = 1;
-    return norm_plan(h, 1, 0, rows, row, path, &unit, &CL, &G, &threads, &vpt, &batch);
+    int unit = 16, CL = 0, G = 0, threads = 0, vpt = 1, batch = 1, maxc = 0;
+    return norm_plan(h, 1, 0, rows, row, path, &unit, &CL, &G, &threads, &vpt, &batch, &maxc);
 }
 
 sfar_status sfar_probe_empty(sfar_stream_t s)

@@ -54,6 +54,7 @@ struct SfarArgs {
     int R, K, overlap, tile_bytes, stages;
     unsigned long long *trace;    // NULL, or a ring of trace_calls entries per CTA (see sfar_test.h)
     uint32_t trace_calls;
+    int solo;                     // 1: launched without overlap, and lets no successor launch early
 };
 
 // Kernel lookup, one function per translation unit.  dt: 0 bf16, 1 fp32.

@@ -327,7 +327,8 @@ __device__ __forceinline__ bool sfar_prologue(const SfarArgs &a, int r, int k, S
     const int flags = s_flags;
     // The successor may take its tickets only after all of ours are taken
     // (a successor in overlap mode does not wait for this kernel to end).
-    if (!a.overlap || (flags & 1))
+    // A solo grid (one that fills the GPU) lets it launch only at its end.
+    if ((!a.overlap || (flags & 1)) && !a.solo)
         pdl_launch_dependents();
     if (flags & 1)
         return false;

@@ -223,7 +223,7 @@ def check_status(h, what):
     code, f = sfar.sfar_status_get(h.h)
     if code != sfar.SFAR_OK:
         raise RuntimeError(f"{what}: device status {sfar.strerror(code)} (rank {f.rank} cta {f.cta} peer {f.peer} "
-                           f"where {sfar.WAIT_NAMES.get(f.where, f.where)})")
+                           f"epoch {f.epoch} where {sfar.WAIT_NAMES.get(f.where, f.where)})")
 
 
 def floor_probe():

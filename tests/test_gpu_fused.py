@@ -502,3 +502,48 @@ def test_two_shot_dropped_rank_times_out_and_reset_recovers():
         check(h, x, res, w, hidden, 1e-5, "two-shot after reset")
     finally:
         h.close()
+
+
+def test_large_grid_chain_does_not_stall():
+    """A one-shot grid that fills most of the device (R = 8, eight rows of
+    8192 bf16: 32 clusters of 8 CTAs) chained in a graph in serial mode:
+    launched as a programmatic dependent it sometimes had a cluster that
+    never started (its peers timed out); such grids now run solo.  Twenty
+    replays of 32 calls with a 50 ms wait limit, then the last call against
+    the oracle."""
+    R, rows, hidden, calls, eps = 8, 8, 8192, 32, 1e-5
+    n = rows * hidden
+    x = torch.stack([inputs.draw(1500, c, R, n, "normal", 1.0, "bf16") for c in range(calls)])
+    res = torch.stack([inputs.draw(1501, c, R, n, "normal", 2.0, "bf16") for c in range(calls)])
+    w = inputs.draw(1502, 0, 1, hidden, "normal", 1.0, "bf16")[0]
+    h = sfar.Sfar(R, 2 * n, "bf16")
+    try:
+        h.set_mode("serial")
+        assert sfar.sfar_test_set_fused_path(h.h, "oneshot") == sfar.SFAR_OK
+        code, k, cl, t = sfar.sfar_test_query_norm_launch(h.h, rows, hidden)
+        assert code == sfar.SFAR_OK and k * R // cl >= 24, (k, cl)          # a grid of most of the device
+        assert sfar.sfar_test_set_timeout(h.h, 50_000_000) == sfar.SFAR_OK
+        xd, rd, wd = x.cuda(), res.cuda(), w.cuda()
+        od, zd = torch.empty_like(xd), torch.empty_like(xd)
+        P = lambda t, c: [t[c, r].data_ptr() for r in range(R)]
+        f = lambda c: sfar.sfar_allreduce_add_rmsnorm(h.h, P(xd, c), P(rd, c), wd.data_ptr(), P(od, c), P(zd, c),
+                                                       rows, hidden, eps)
+        assert f(0) == sfar.SFAR_OK
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            for c in range(calls):
+                assert f(c) == sfar.SFAR_OK
+        for rep in range(20):
+            for _ in range(32):
+                graph.replay()
+            torch.cuda.synchronize()
+            status_ok(h.h, f"large grid replay batch {rep}")
+        c = calls - 1
+        want_y, want_z = oracle.add_rmsnorm(inputs.to_bits(x[c]), inputs.to_bits(res[c]),
+                                            inputs.to_bits(w[None, :])[0], eps, hidden)
+        for r in range(R):
+            assert_equal_nan_aware(zd[c, r], want_z[r], f"large grid z rank {r}")
+            assert_equal_nan_aware(od[c, r], want_y[r], f"large grid y rank {r}")
+    finally:
+        h.close()
