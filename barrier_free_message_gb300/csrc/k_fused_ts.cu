@@ -50,8 +50,7 @@
 // path: a CTA whose handle failed, or whose wait gave up, only skips work.
 #include "fused_common.cuh"
 
-// Largest magnitude and integer sum of truncated squares of the elements of
-// one unit.
+// Largest magnitude (as binary32 magnitude bits) of the elements of one unit.
 template <int DT>
 __device__ __forceinline__ uint32_t unit_max(const uint4 &z)
 {

@@ -58,7 +58,10 @@ sfar_status sfar_test_force_single_buffer(sfar_t *h, int on, sfar_stream_t s);
  * rank, not across ranks).  Calls may then overtake one another across
  * ranks, which is what double buffering has to survive.  Use OVERLAP only
  * for chains of calls whose inputs do not depend on the previous call's
- * outputs.
+ * outputs.  In every mode, a fused AllReduce + RMSNorm call whose grid takes
+ * more than three quarters of the device's co-resident clusters, and every
+ * two-shot fused call, runs with serial semantics; the first of those also
+ * without programmatic launch, and lets no successor launch before it ends.
  */
 #define SFAR_LAUNCH_SERIAL 0
 #define SFAR_LAUNCH_OVERLAP 1
