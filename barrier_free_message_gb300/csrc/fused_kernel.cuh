@@ -24,7 +24,8 @@
 //       else inf -> +inf;
 //   rstd = 1 (/) sqrt(ms (+) eps), y = T((z (*) rstd) (*) w), each binary32
 //       operation rounded to nearest even.
-// Outputs: out[r] = y, res_out[r] = z.
+// Outputs: out[r] = y, res_out[r] = z (z is stored as soon as it is formed,
+// before the row statistics).
 //
 // Units: a thread carries UB bytes of a row per unit: 16, or 8 (one LL line
 // per peer instead of two, as the plain LL kernel) for an AllReduce of rows
@@ -282,6 +283,8 @@ __global__ void __launch_bounds__(SFAR_NORM_THREADS, UB == 8 && RB <= 8 ? 2 : 1)
                 for (int t = 0; t < NE; ++t)
                     m = max(m, mag_bits(V::get(zv[q], t)));
                 lmax[NB == 1 ? 0 : q] = max(lmax[NB == 1 ? 0 : q], m);
+                if (ok)
+                    st_unit<UB>((char *)na.res_out[r] + vq[q] * UB, zv[q]);    // z is final: stored now
             }
         }
         if (i0 == (unsigned long long)g)
@@ -384,7 +387,6 @@ __global__ void __launch_bounds__(SFAR_NORM_THREADS, UB == 8 && RB <= 8 ? 2 : 1)
 #pragma unroll
                 for (int t = 0; t < V::N; ++t)
                     yf[t] = t < NE ? __fmul_rn(__fmul_rn(V::get(zv[q], t), rs), V::get(wv[q], t)) : 0.f;
-                st_unit<UB>((char *)na.res_out[r] + vq[q] * UB, zv[q]);
                 st_unit<UB>((char *)a.out[r] + vq[q] * UB, V::pack(yf));
             }
         }
