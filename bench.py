@@ -343,14 +343,16 @@ def large_message_roofline(peak_gbs, R=8, mb=64, dtype="bf16", iters=10):
             "traffic": profiled_traffic("k_tma"), "bit_exact_sample": ok}
 
 
-def oracle_cpu_time(x_host, budget_s=10.0, calls_per_step=None):
-    """The oracle as it stands, single-threaded, on a bounded sample of calls."""
+def oracle_cpu_time(x_host, budget_s=10.0, calls_per_step=None, threads=1):
+    """The oracle as it stands on a bounded sample of calls: single-threaded,
+    or with each call's elements split over `threads` threads (its
+    multithreaded variant, the same bits)."""
     import oracle
     xs = [inputs.to_bits(x_host[c]) for c in range(min(len(x_host), 2048))]
-    oracle.allreduce(xs[0])
+    oracle.allreduce(xs[0], threads=threads)
     done, t0 = 0, time.perf_counter()
     while True:
-        oracle.allreduce(xs[done % len(xs)])
+        oracle.allreduce(xs[done % len(xs)], threads=threads)
         done += 1
         if calls_per_step is not None:
             if done >= calls_per_step:
@@ -807,6 +809,13 @@ def run_ours(args, world, rank):
         cpu_us, cpu_calls, cpu_s = oracle_cpu_time(x_host, budget_s=args.cpu_seconds)
         cpu = {"value": round(cpu_us, 3), "unit": "us/call", "cores": 1, "kind": "oracle",
                "sample": f"{cpu_calls} calls of R=8 x 8192 bf16 (tp-decode), {cpu_s:.1f} s, single thread"}
+        # the same with every host thread splitting each call (a call is short at
+        # 16 KB per rank, so thread start-up takes much of what the split saves)
+        nthr = os.cpu_count() or 1
+        if nthr > 1:
+            mt_us, mt_calls, mt_s = oracle_cpu_time(x_host, budget_s=min(3.0, args.cpu_seconds), threads=nthr)
+            cpu["threaded"] = {"value": round(mt_us, 3), "unit": "us/call", "cores": nthr,
+                               "sample": f"{mt_calls} calls, {mt_s:.1f} s, each split over {nthr} threads"}
 
     if rank != 0:
         return
