@@ -547,3 +547,55 @@ def test_large_grid_chain_does_not_stall():
             assert_equal_nan_aware(od[c, r], want_y[r], f"large grid y rank {r}")
     finally:
         h.close()
+
+
+def test_solo_grid_between_overlapped_calls():
+    """Overlap mode: LL calls, a fused call whose grid runs solo (8 rows of
+    8192 bf16, one-shot forced) and more LL calls, all on one handle and in
+    one graph; the calls around the solo grid must not overtake it.  Every
+    result bit for bit."""
+    R, rows, hidden, eps = 8, 8, 8192, 1e-5
+    n = rows * hidden
+    seq = ["ll", "ll", "fused", "ll", "ll", "fused", "fused", "ll"] * 8
+    x = torch.stack([inputs.draw(1600, c, R, n, "normal", 1.0, "bf16") for c in range(len(seq))])
+    res = torch.stack([inputs.draw(1601, c, R, n, "normal", 2.0, "bf16") for c in range(len(seq))])
+    w = inputs.draw(1602, 0, 1, hidden, "normal", 1.0, "bf16")[0]
+    h = sfar.Sfar(R, 2 * n, "bf16")
+    try:
+        h.set_mode("overlap")
+        assert sfar.sfar_test_set_fused_path(h.h, "oneshot") == sfar.SFAR_OK
+        xd, rd, wd = x.cuda(), res.cuda(), w.cuda()
+        od, zd = torch.empty_like(xd), torch.empty_like(xd)
+        P = lambda t, c: [t[c, r].data_ptr() for r in range(R)]
+
+        def call(c):
+            if seq[c] == "ll":
+                return sfar.sfar_allreduce(h.h, P(xd, c), P(od, c), n, "ll")
+            return sfar.sfar_allreduce_add_rmsnorm(h.h, P(xd, c), P(rd, c), wd.data_ptr(), P(od, c), P(zd, c),
+                                                   rows, hidden, eps)
+
+        assert call(0) == sfar.SFAR_OK
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            for c in range(len(seq)):
+                assert call(c) == sfar.SFAR_OK
+        for rep in range(4):
+            od.view(torch.int16).fill_(-1)
+            graph.replay()
+            torch.cuda.synchronize()
+            status_ok(h.h, f"solo between overlapped calls, replay {rep}")
+        wb = inputs.to_bits(w[None, :])[0]
+        for c in range(len(seq)):
+            xb = inputs.to_bits(x[c])
+            if seq[c] == "ll":
+                want = oracle.allreduce(xb)
+                for r in range(R):
+                    assert np.array_equal(inputs.to_bits(od[c, r].cpu()), want[r]), f"call {c} rank {r}"
+            else:
+                want_y, want_z = oracle.add_rmsnorm(xb, inputs.to_bits(res[c]), wb, eps, hidden)
+                for r in range(R):
+                    assert_equal_nan_aware(zd[c, r], want_z[r], f"call {c} z rank {r}")
+                    assert_equal_nan_aware(od[c, r], want_y[r], f"call {c} y rank {r}")
+    finally:
+        h.close()
