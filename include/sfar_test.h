@@ -92,8 +92,10 @@ sfar_status sfar_test_set_geometry(sfar_t *h, int ctas_per_rank, int threads_per
 /* Launch shape of sfar_allreduce_add_rmsnorm (allreduce = 1) or
  * sfar_add_rmsnorm (allreduce = 0) for rows x hidden: CTAs per rank, CTAs per
  * thread-block cluster (a row is spread over one cluster) and threads per
- * CTA.  Returns what the call itself would return for the shape
- * (SFAR_ERR_INVALID, SFAR_ERR_UNSUPPORTED) without launching anything. */
+ * CTA, of whichever kernel the call would launch (see
+ * sfar_test_query_fused_path).  Returns what the call itself would return
+ * for the shape (SFAR_ERR_INVALID, SFAR_ERR_UNSUPPORTED) without launching
+ * anything. */
 sfar_status sfar_test_query_norm_launch(sfar_t *h, size_t rows, size_t hidden, int allreduce, int *ctas_per_rank,
                                         int *cluster_size, int *threads_per_cta);
 
