@@ -24,8 +24,8 @@
 //   1. reads its unit from every rank's input and folds them (R loads in
 //      flight, with every rank's residual unit too for R <= 8);
 //   2. forms z_p for every rank p and the largest |z_p| (R maxima per warp,
-//      round 1 of the cluster exchange), then the truncated squares of every
-//      z_p summed as integers (R sums per warp, round 2);
+//      the first cluster exchange), then the truncated squares of every
+//      z_p summed as integers (R sums per warp, the second exchange);
 //   3. writes z_p into rank p's residual output as soon as it is formed, and
 //      y_p into rank p's output after the statistics.
 // The exchange is the one of the one-shot fused kernel: every warp stores its
@@ -123,7 +123,7 @@ __global__ void __launch_bounds__(SFAR_NORM_THREADS, RB <= 8 ? 2 : 1)
     __shared__ int s_ok;
     const uint32_t mb_max = smem_u32(&s_mbar[0]), mb_sum = smem_u32(&s_mbar[1]);
     const int W = T >> 5, nslots = CL * W, slot = cr * W + warp;
-    const int R4 = (R + 3) >> 2;                  // 16-byte stores per slot in round 1
+    const int R4 = (R + 3) >> 2;                  // 16-byte stores per slot in the first exchange
 
     const bool works = has_u && i0 < rows;
     if (works)
@@ -226,7 +226,7 @@ __global__ void __launch_bounds__(SFAR_NORM_THREADS, RB <= 8 ? 2 : 1)
         if (i == i0)
             sfar_stamp(c, TP_INPUT);          // first row: AllReduce result and z in registers
 
-        // round 1: every warp's R maxima to its slot in every cluster CTA
+        // first exchange: every warp's R maxima to its slot in every cluster CTA
 #pragma unroll
         for (int p = 0; p < RB; ++p)
             if (p < R)
@@ -257,7 +257,7 @@ __global__ void __launch_bounds__(SFAR_NORM_THREADS, RB <= 8 ? 2 : 1)
         for (int p = 0; p < RB; ++p)
             M[p] = __shfl_sync(SFAR_FULL, mine, p);
 
-        // round 2: the truncated squares of every rank's row, summed as integers
+        // second exchange: the truncated squares of every rank's row, summed as integers
         unsigned long long lsum[RB];
 #pragma unroll
         for (int p = 0; p < RB; ++p) {
