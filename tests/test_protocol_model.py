@@ -1,0 +1,223 @@
+"""Race checks of the synchronisation protocols by exhaustive-ish random
+interleaving, on the CPU (compute-sanitizer is not available, and a GPU run
+shows one schedule at a time).
+
+Each (rank, call) of a chain is a process of small atomic steps: stores,
+polls that block until a condition holds, reads.  A scheduler runs a random
+runnable process one step at a time, over many seeds.  A process of call e
+starts, in serial mode, once every rank has finished call e - 1 (the kernel
+boundary), in overlap mode once its own rank has finished call e - 1 (the
+hand-off of CTA (r, k) to CTA (r, k) of the next call).  Found:
+
+* a race: a store over a slot whose previous message was not read yet, or a
+  read of an input or output of the wrong call;
+* a deadlock: nothing can run before every process has finished.
+
+Models (one CTA index; the protocols are per CTA index):
+
+* LL: epoch-tagged packets into recv[receiver][e & 1][sender]; the reader
+  polls until the slot carries epoch e ("Every Microsecond Counts", page 1,
+  section "Four barrier-free mechanisms", parts 1 and 3).
+* sentinel: raw values into the same slots; the reader polls until the slot
+  is not the sentinel, reads, and refills it with the sentinel (part 2).
+* two-shot pull (the TMA AllReduce and the two-shot fused normalisation):
+  rank q publishes its input for call e and stores arrive[q] = e; owner j
+  reads every rank's input once arrive[q] >= e and writes its share of every
+  rank's output, then stores cmpl[p][j] = e; rank p finishes only once every
+  owner's cmpl[p][j] >= e ("SiFAR", page 3, "Limits of existing algorithms";
+  page 1 part 4: counters reaching N, kept as flags).
+
+Each model also runs with a planted mistake (a single buffer, no refill, no
+completion wait, no arrival wait) that the search must catch, so the checker
+itself is shown to see races.
+"""
+import random
+
+import pytest
+
+
+class Race(AssertionError):
+    pass
+
+
+class Deadlock(AssertionError):
+    pass
+
+
+def run(procs_of, R, calls, overlap, seed, max_steps=200000):
+    """procs_of(r, e, state) -> generator; yields a callable (block until it
+    returns True) or None (a step boundary)."""
+    rng = random.Random(seed)
+    state = {"done": [0] * R}
+    live = {}            # (r, e) -> [generator, pending condition]
+    started = set()
+
+    def can_start(r, e):
+        if overlap:
+            return state["done"][r] >= e - 1
+        return all(d >= e - 1 for d in state["done"])
+
+    for _ in range(max_steps):
+        for r in range(R):
+            e = state["done"][r] + 1
+            while (r, e) in started:
+                e += 1
+            if e <= calls and (r, e) not in started and can_start(r, e) and \
+                    all((r, f) not in live for f in range(1, e)):
+                live[(r, e)] = [procs_of(r, e, state), None]
+                started.add((r, e))
+        runnable = [key for key, (g, cond) in live.items() if cond is None or cond()]
+        if not runnable:
+            if not live and all(d == calls for d in state["done"]):
+                return
+            raise Deadlock(f"seed {seed}: nothing can run; waiting: {sorted(live)}")
+        key = rng.choice(runnable)
+        g = live[key][0]
+        try:
+            live[key][1] = next(g)
+        except StopIteration:
+            r, e = key
+            state["done"][r] = e
+            del live[key]
+    raise AssertionError("step limit")
+
+
+# ------------------------------------------------------------------ LL
+def ll_model(R, single_buffer=False):
+    def procs_of(r, e, st):
+        slots = st.setdefault("slots", {})
+        par = 0 if single_buffer else e & 1
+        peers = [q for q in range(R) if q != r]
+        for p in peers:                                   # sends
+            s = slots.setdefault((p, par, r), {"epoch": 0, "unread": False})
+            if s["unread"]:
+                raise Race(f"rank {r} call {e} overwrote rank {p}'s unread epoch {s['epoch']}")
+            s.update(epoch=e, unread=True)
+            yield None
+        for q in random.Random(r * 1000 + e).sample(peers, len(peers)):      # receives, any order
+            key = (r, par, q)
+            yield (lambda key=key: slots.get(key, {}).get("epoch") == e)
+            s = slots[key]
+            if s["epoch"] != e:
+                raise Race(f"rank {r} call {e} read epoch {s['epoch']} from {q}")
+            s["unread"] = False
+    return procs_of
+
+
+# ------------------------------------------------------------ sentinel
+SENT = None
+
+
+def sentinel_model(R, refill=True):
+    def procs_of(r, e, st):
+        slots = st.setdefault("slots", {})
+        par = e & 1
+        peers = [q for q in range(R) if q != r]
+        for p in peers:
+            key = (p, par, r)
+            if slots.get(key, SENT) is not SENT:
+                raise Race(f"rank {r} call {e} stored over {slots[key]} (not yet read or refilled)")
+            slots[key] = (r, e)
+            yield None
+        for q in random.Random(r * 7919 + e).sample(peers, len(peers)):
+            key = (r, par, q)
+            yield (lambda key=key: slots.get(key, SENT) is not SENT)
+            if slots[key] != (q, e):
+                raise Race(f"rank {r} call {e} read {slots[key]} from {q}")
+            yield None
+            if refill:
+                slots[key] = SENT
+            else:
+                slots[key] = ("stale", q, e)      # a reader that forgets the refill
+    return procs_of
+
+
+# ------------------------------------------------------------ two-shot pull
+def pull_model(R, completion_wait=True, arrival_wait=True):
+    def procs_of(r, e, st):
+        inp = st.setdefault("input", [0] * R)
+        out = st.setdefault("out", [[0] * R for _ in range(R)])      # out[p][owner share] = call written
+        arrive = st.setdefault("arrive", [0] * R)
+        cmpl = st.setdefault("cmpl", [[0] * R for _ in range(R)])
+        # rank r's stream: the previous call's output is consumed, then this
+        # call's input produced
+        if e > 1 and any(v != e - 1 for v in out[r]):
+            raise Race(f"rank {r} consumed call {e - 1}'s output while it held {out[r]}")
+        inp[r] = e
+        yield None
+        arrive[r] = e
+        yield None
+        order = random.Random(r * 104729 + e).sample(range(R), R)
+        for q in order:                                   # owner r reads share r of every rank
+            if arrival_wait:
+                yield (lambda q=q: arrive[q] >= e)
+            if inp[q] != e:
+                raise Race(f"owner {r} call {e} read rank {q}'s input of call {inp[q]}")
+            yield None
+        for p in order:                                   # and writes share r of every rank's output
+            out[p][r] = e
+            yield None
+        for p in range(R):
+            cmpl[p][r] = e
+        yield None
+        if completion_wait:
+            for q in range(R):
+                yield (lambda q=q: cmpl[r][q] >= e)
+    return procs_of
+
+
+SEEDS = range(300)
+
+
+@pytest.mark.parametrize("overlap", [False, True])
+@pytest.mark.parametrize("R", [2, 3, 4])
+def test_ll_double_buffer_has_no_race(R, overlap):
+    for seed in SEEDS:
+        run(ll_model(R), R, calls=6, overlap=overlap, seed=seed)
+
+
+def test_ll_single_buffer_races_under_overlap():
+    """The forced single buffer: safe with kernel boundaries, a race once
+    calls overlap (the GPU test of the same knob sees a timeout or a wrong
+    value)."""
+    for seed in SEEDS:
+        run(ll_model(3, single_buffer=True), 3, calls=6, overlap=False, seed=seed)
+    caught = 0
+    for seed in SEEDS:
+        try:
+            run(ll_model(3, single_buffer=True), 3, calls=6, overlap=True, seed=seed)
+        except (Race, Deadlock):
+            caught += 1
+    assert caught > 0
+
+
+@pytest.mark.parametrize("overlap", [False, True])
+@pytest.mark.parametrize("R", [2, 3, 4])
+def test_sentinel_refill_has_no_race(R, overlap):
+    for seed in SEEDS:
+        run(sentinel_model(R), R, calls=6, overlap=overlap, seed=seed)
+
+
+def test_sentinel_without_refill_is_caught():
+    with pytest.raises(Race):
+        for seed in SEEDS:
+            run(sentinel_model(3, refill=False), 3, calls=6, overlap=False, seed=seed)
+
+
+@pytest.mark.parametrize("overlap", [False, True])
+@pytest.mark.parametrize("R", [2, 3, 4])
+def test_two_shot_pull_has_no_race(R, overlap):
+    for seed in SEEDS:
+        run(pull_model(R), R, calls=6, overlap=overlap, seed=seed)
+
+
+@pytest.mark.parametrize("planted", ["no completion wait", "no arrival wait"])
+def test_two_shot_pull_planted_mistakes_are_caught(planted):
+    kw = {"completion_wait": planted != "no completion wait", "arrival_wait": planted != "no arrival wait"}
+    caught = 0
+    for seed in SEEDS:
+        try:
+            run(pull_model(3, **kw), 3, calls=6, overlap=True, seed=seed)
+        except Race:
+            caught += 1
+    assert caught > 0, planted
