@@ -27,9 +27,17 @@ Models (one CTA index; the protocols are per CTA index):
   owner's cmpl[p][j] >= e ("SiFAR", page 3, "Limits of existing algorithms";
   page 1 part 4: counters reaching N, kept as flags).
 
-Each model also runs with a planted mistake (a single buffer, no refill, no
-completion wait, no arrival wait) that the search must catch, so the checker
-itself is shown to see races.
+* DB and BASELINE: raw data, then a top barrier of epoch flags (DB, two
+  buffers) or one buffer with a top and a bottom barrier (BASELINE).
+* two-shot over flagged lines: reduce-scatter into the owner's lines, then an
+  all-gather into every rank's lines, both epoch-tagged.
+* atomic accumulation: every rank adds into the owner's line and bumps its
+  counter; the owner reads at counter = R, clears the line, all-gathers.
+
+Each model also runs with a planted mistake (a single buffer under overlap,
+no refill, no bottom barrier on one buffer, no completion wait, no arrival
+wait, no all-gather wait, no clear) that the search must catch, so the
+checker itself is shown to see races.
 """
 import random
 
@@ -221,3 +229,184 @@ def test_two_shot_pull_planted_mistakes_are_caught(planted):
         except Race:
             caught += 1
     assert caught > 0, planted
+
+
+# ------------------------------------------------------------ DB / BASELINE
+def flag_model(R, double_buffer=True, bottom=False):
+    """Raw data into recv[receiver][parity][sender], then a top barrier of
+    epoch flags (DB: ready flags after the data; "SiFAR", page 3, Technique
+    1), and for BASELINE one buffer and a bottom barrier after the reads
+    (page 1, "Global memory barriers")."""
+    def procs_of(r, e, st):
+        slots = st.setdefault("slots", {})
+        top = st.setdefault("top", {})
+        bot = st.setdefault("bot", {})
+        par = e & 1 if double_buffer else 0
+        peers = [q for q in range(R) if q != r]
+        for p in peers:
+            s = slots.setdefault((p, par, r), {"call": 0, "unread": False})
+            if s["unread"]:
+                raise Race(f"rank {r} call {e} overwrote rank {p}'s unread call {s['call']}")
+            s.update(call=e, unread=True)
+            yield None
+        for p in peers:
+            top[(p, r)] = e
+        yield None
+        for q in peers:
+            yield (lambda q=q: top.get((r, q), 0) >= e)
+        for q in peers:
+            s = slots[(r, par, q)]
+            if s["call"] != e:
+                raise Race(f"rank {r} call {e} read call {s['call']} from {q}")
+            s["unread"] = False
+            yield None
+        if bottom:
+            for p in peers:
+                bot[(p, r)] = e
+            yield None
+            for q in peers:
+                yield (lambda q=q: bot.get((r, q), 0) >= e)
+    return procs_of
+
+
+@pytest.mark.parametrize("overlap", [False, True])
+@pytest.mark.parametrize("R", [2, 3, 4])
+@pytest.mark.parametrize("proto", ["db", "baseline"])
+def test_flag_protocols_have_no_race(proto, R, overlap):
+    kw = {"double_buffer": True, "bottom": False} if proto == "db" else {"double_buffer": False, "bottom": True}
+    for seed in SEEDS:
+        run(flag_model(R, **kw), R, calls=6, overlap=overlap, seed=seed)
+
+
+def test_one_buffer_without_bottom_barrier_is_caught():
+    caught = 0
+    for seed in SEEDS:
+        try:
+            run(flag_model(3, double_buffer=False, bottom=False), 3, calls=6, overlap=True, seed=seed)
+        except Race:
+            caught += 1
+    assert caught > 0
+
+
+# ------------------------------------------------ two-shot over flagged lines
+def twoshot_model(R, double_buffer=True, ag_wait=True):
+    """Reduce-scatter: rank q sends share j to owner j's slot rs[j][par][q]
+    (epoch-tagged lines); the owner polls all R - 1, folds, and all-gathers
+    the result into ag[p][par][j] for every rank p, which polls all owners."""
+    def procs_of(r, e, st):
+        rs = st.setdefault("rs", {})
+        ag = st.setdefault("ag", {})
+        par = e & 1 if double_buffer else 0
+        peers = [q for q in range(R) if q != r]
+
+        def put(region, key):
+            s = region.setdefault(key, {"epoch": 0, "unread": False})
+            if s["unread"]:
+                raise Race(f"rank {r} call {e} overwrote unread epoch {s['epoch']} at {key}")
+            s.update(epoch=e, unread=True)
+
+        def take(region, key):
+            s = region[key]
+            if s["epoch"] != e:
+                raise Race(f"rank {r} call {e} read epoch {s['epoch']} at {key}")
+            s["unread"] = False
+
+        for j in peers:
+            put(rs, (j, par, r))
+            yield None
+        for q in peers:
+            yield (lambda q=q: rs.get((r, par, q), {}).get("epoch") == e)
+            take(rs, (r, par, q))
+        for p in peers:
+            put(ag, (p, par, r))
+            yield None
+        for j in peers:
+            if ag_wait:
+                yield (lambda j=j: ag.get((r, par, j), {}).get("epoch") == e)
+                take(ag, (r, par, j))
+    return procs_of
+
+
+@pytest.mark.parametrize("overlap", [False, True])
+@pytest.mark.parametrize("R", [2, 3, 4])
+def test_twoshot_lines_have_no_race(R, overlap):
+    for seed in SEEDS:
+        run(twoshot_model(R), R, calls=6, overlap=overlap, seed=seed)
+
+
+def test_twoshot_phases_order_slot_reuse():
+    """Finding: the two phases alone order every slot's reuse (a rank starts
+    call e + 1 only after every owner's all-gather of call e, which the owner
+    sends only after reading that rank's reduce-scatter lines of call e), so
+    even one buffer is race-free in this model; the kernel double-buffers
+    anyway.  A rank that skips the all-gather wait is caught."""
+    for seed in SEEDS:
+        run(twoshot_model(3, double_buffer=False), 3, calls=6, overlap=True, seed=seed)
+    caught = 0
+    for seed in SEEDS:
+        try:
+            run(twoshot_model(3, double_buffer=False, ag_wait=False), 3, calls=6, overlap=True, seed=seed)
+        except (Race, Deadlock):
+            caught += 1
+    assert caught > 0
+
+
+# ------------------------------------------------------- atomic accumulation
+def atomic_model(R, clear=True, double_buffer=True):
+    """LL128 atomic (page 1, part 4): every rank adds its part into owner j's
+    accumulator line acc[j][par] and bumps its counter; the owner waits for
+    counter == R, reads the sum, clears the line (data and counter) and
+    all-gathers with epoch flags."""
+    def procs_of(r, e, st):
+        acc = st.setdefault("acc", {})
+        ag = st.setdefault("ag", {})
+        par = e & 1 if double_buffer else 0
+        peers = [q for q in range(R) if q != r]
+        for j in range(R):                                # adds, own line included
+            line = acc.setdefault((j, par), {"parts": [], "count": 0})
+            if any(c != e for _, c in line["parts"]):
+                raise Race(f"rank {r} call {e} added into owner {j}'s line holding {line['parts']}")
+            line["parts"].append((r, e))
+            line["count"] += 1
+            yield None
+        line = acc[(r, par)]
+        yield (lambda line=line: line["count"] >= R)
+        if sorted(line["parts"]) != [(q, e) for q in range(R)]:
+            raise Race(f"owner {r} call {e} read {sorted(line['parts'])}")
+        if clear:
+            line["parts"], line["count"] = [], 0
+        else:
+            line["count"] = 0                             # a reader that forgets the data
+        yield None
+        for p in peers:
+            ag[(p, par, r)] = e
+        yield None
+        for j in peers:
+            yield (lambda j=j: ag.get((r, par, j), 0) == e)
+    return procs_of
+
+
+@pytest.mark.parametrize("overlap", [False, True])
+@pytest.mark.parametrize("R", [2, 3, 4])
+def test_atomic_lines_have_no_race(R, overlap):
+    for seed in SEEDS:
+        run(atomic_model(R), R, calls=6, overlap=overlap, seed=seed)
+
+
+def test_atomic_missing_clear_is_caught():
+    caught = 0
+    for seed in SEEDS:
+        try:
+            run(atomic_model(3, clear=False), 3, calls=6, overlap=True, seed=seed)
+        except (Race, Deadlock):
+            caught += 1
+    assert caught > 0
+
+
+def test_atomic_all_gather_orders_line_reuse():
+    """Finding, as for the two-shot lines: the all-gather already orders the
+    reuse of an accumulator line (the owner clears it before its all-gather,
+    and every adder waits for that all-gather before its next call), so one
+    buffer is race-free in this model too."""
+    for seed in SEEDS:
+        run(atomic_model(3, double_buffer=False), 3, calls=6, overlap=True, seed=seed)
