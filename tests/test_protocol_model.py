@@ -410,3 +410,86 @@ def test_atomic_all_gather_orders_line_reuse():
     buffer is race-free in this model too."""
     for seed in SEEDS:
         run(atomic_model(3, double_buffer=False), 3, calls=6, overlap=True, seed=seed)
+
+
+# ------------------------------------------- overlap hand-off and geometry
+def run_ctas(R, Ks, units, overlap, cross_geometry, seed, max_steps=400000):
+    """LL over CTAs: call e (epoch e) runs Ks[e - 1] CTAs per rank; CTA k of
+    every rank handles units u with u % K == k.  In overlap mode CTA (r, k)
+    of call e starts once CTA (r, k) of call e - 1 is done, but only when
+    the two calls have the same geometry (the host's overlap key); otherwise
+    (or in serial mode) it starts once every CTA of every earlier call is done.
+    cross_geometry=True plants the mistake of overlapping across a change."""
+    rng = random.Random(seed)
+    calls = len(Ks)
+    done = {}                       # (r, k) -> last epoch finished by that CTA index
+    finished = set()                # (r, k, e)
+    slots = {}
+    live, started = {}, set()
+
+    def all_done_before(e):
+        return all((r, k, f) in finished for f in range(1, e) for r in range(R) for k in range(Ks[f - 1]))
+
+    def can_start(r, k, e):
+        if e > 1 and overlap and (Ks[e - 1] == Ks[e - 2] or cross_geometry):
+            return k < Ks[e - 2] and (r, k, e - 1) in finished or (k >= Ks[e - 2] and all_done_before(e))
+        return all_done_before(e)
+
+    def proc(r, k, e):
+        K = Ks[e - 1]
+        par = e & 1
+        mine = [u for u in range(units) if u % K == k]
+        peers = [q for q in range(R) if q != r]
+        for u in mine:
+            for p in peers:
+                s = slots.setdefault((p, par, r, u), {"epoch": 0, "unread": False})
+                if s["unread"]:
+                    raise Race(f"CTA ({r},{k}) call {e} overwrote unread epoch {s['epoch']} of unit {u} at rank {p}")
+                s.update(epoch=e, unread=True)
+                yield None
+        for u in mine:
+            for q in peers:
+                key = (r, par, q, u)
+                yield (lambda key=key: slots.get(key, {}).get("epoch") == e)
+                slots[key]["unread"] = False
+
+    for _ in range(max_steps):
+        for e in range(1, calls + 1):
+            for r in range(R):
+                for k in range(Ks[e - 1]):
+                    if (r, k, e) not in started and can_start(r, k, e):
+                        live[(r, k, e)] = [proc(r, k, e), None]
+                        started.add((r, k, e))
+        runnable = [key for key, (g, cond) in live.items() if cond is None or cond()]
+        if not runnable:
+            if len(finished) == sum(R * K for K in Ks):
+                return
+            raise Deadlock(f"seed {seed}: waiting {sorted(live)}")
+        key = rng.choice(runnable)
+        try:
+            live[key][1] = next(live[key][0])
+        except StopIteration:
+            finished.add(key)
+            done[key[:2]] = key[2]
+            del live[key]
+    raise AssertionError("step limit")
+
+
+GEOMETRIES = [[2, 2, 1, 1, 2, 2, 2, 1], [1, 2, 2, 1, 2, 1, 1, 2], [2, 2, 2, 2, 2, 2, 2, 2]]
+
+
+@pytest.mark.parametrize("Ks", GEOMETRIES)
+def test_overlap_hand_off_only_within_one_geometry_is_safe(Ks):
+    for seed in range(150):
+        run_ctas(3, Ks, units=4, overlap=True, cross_geometry=False, seed=seed)
+        run_ctas(3, Ks, units=4, overlap=False, cross_geometry=False, seed=seed)
+
+
+def test_overlap_across_a_geometry_change_is_caught():
+    caught = 0
+    for seed in range(150):
+        try:
+            run_ctas(3, GEOMETRIES[0], units=4, overlap=True, cross_geometry=True, seed=seed)
+        except (Race, Deadlock):
+            caught += 1
+    assert caught > 0
