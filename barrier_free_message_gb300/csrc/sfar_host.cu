@@ -537,8 +537,7 @@ sfar_status sfar_allreduce(sfar_t *h, const void *const in[], void *const out[],
     }
     const int test = (h->k_strag || h->k_drop || h->k_single) ? 1 : 0;
 
-    cudaLaunchConfig_t cfg;
-    memset(&cfg, 0, sizeof cfg);
+    cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3((unsigned)(R * K));
     cfg.blockDim = dim3((unsigned)threads);
     cfg.dynamicSmemBytes = smem_for(h, p);
@@ -596,8 +595,7 @@ static int norm_max_clusters(sfar *h, int allreduce, int test, int batch, int un
     int &slot = h->norm_clusters[allreduce][test][batch > 1 ? 1 : 0][unit == 8 ? 1 : 0][CL][ti];
     if (slot)
         return slot;
-    cudaLaunchConfig_t cfg;
-    memset(&cfg, 0, sizeof cfg);
+    cudaLaunchConfig_t cfg{};
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = (unsigned)CL;
@@ -695,8 +693,7 @@ static sfar_status ts_geometry(sfar *h, int test, size_t rows, unsigned long lon
         return SFAR_ERR_UNSUPPORTED;
     int &slot = h->ts_clusters[test][CL][ti];
     if (!slot) {
-        cudaLaunchConfig_t cfg;
-        memset(&cfg, 0, sizeof cfg);
+        cudaLaunchConfig_t cfg{};
         cudaLaunchAttribute attr[1];
         attr[0].id = cudaLaunchAttributeClusterDimension;
         attr[0].val.clusterDim.x = (unsigned)CL;
@@ -911,8 +908,7 @@ static sfar_status fused_call(sfar *h, const void *const in[], const void *const
         h->last_capture = cap;
     }
 
-    cudaLaunchConfig_t cfg;
-    memset(&cfg, 0, sizeof cfg);
+    cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3((unsigned)(R * K));
     cfg.blockDim = dim3((unsigned)threads);
     cfg.stream = (cudaStream_t)s;
@@ -1018,8 +1014,7 @@ sfar_status sfar_rowpar_gemv(sfar_t *h, const void *const x[], const void *const
     g.prefetch = prefetch_rows < g.seg ? prefetch_rows : g.seg;
     g.tiles = (int)ceil_div(hidden, SFAR_GEMV_COLS);
 
-    cudaLaunchConfig_t cfg;
-    memset(&cfg, 0, sizeof cfg);
+    cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3((unsigned)(R * g.tiles));
     cfg.blockDim = dim3(SFAR_GEMV_SEGMENTS * 32);
     cfg.stream = (cudaStream_t)s;

@@ -188,8 +188,7 @@ extern "C" sfar_status sfar_allreduce_noalloc(const void *const in[], void *cons
     a.K = K;
     a.overlap = 0;
 
-    cudaLaunchConfig_t cfg;
-    memset(&cfg, 0, sizeof cfg);
+    cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3((unsigned)(R * K));
     cfg.blockDim = dim3(kThreads);
     cfg.stream = (cudaStream_t)s;
