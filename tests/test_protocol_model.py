@@ -493,3 +493,71 @@ def test_overlap_across_a_geometry_change_is_caught():
         except (Race, Deadlock):
             caught += 1
     assert caught > 0
+
+
+# --------------------------------------------- cluster statistics exchange
+def run_cluster(CL, rows, seed, early_exit=False, max_steps=200000):
+    """The row statistics exchange of the fused kernels: per row, every CTA of
+    a cluster stores its partial into a slot of every cluster CTA (st.async),
+    counted by the target's mbarrier of that round, waits for its own
+    mbarrier, reads the slots; two rounds (maxima, sums) per row, one
+    mbarrier each, whose phase advances once per row.  Checked: a store for
+    row j reaches a CTA only after that CTA has read its row j - 1 slots of
+    the round (else it would overwrite them or count in the wrong phase),
+    and never after the CTA has exited.  early_exit plants a CTA that leaves
+    without its last wait."""
+    rng = random.Random(seed)
+    ctas = [{"read": [0, 0], "count": [dict(), dict()], "slot": [dict(), dict()], "exited": False}
+            for _ in range(CL)]
+
+    def proc(c):
+        for row in range(rows):
+            for rnd in (0, 1):
+                for d in rng.sample(range(CL), CL):
+                    dst = ctas[d]
+                    if dst["exited"]:
+                        raise Race(f"CTA {c} stored row {row} round {rnd} into exited CTA {d}")
+                    if dst["read"][rnd] < row:
+                        raise Race(f"CTA {c} stored row {row} round {rnd} before CTA {d} read row {row - 1}")
+                    dst["slot"][rnd][c] = row
+                    dst["count"][rnd][row] = dst["count"][rnd].get(row, 0) + 1
+                    yield None
+                me = ctas[c]
+                if early_exit and c == 0 and row == rows - 1 and rnd == 1:
+                    break
+                yield (lambda me=me, rnd=rnd, row=row: me["count"][rnd].get(row, 0) == CL)
+                if any(v != row for v in me["slot"][rnd].values()):
+                    raise Race(f"CTA {c} row {row} round {rnd} read {me['slot'][rnd]}")
+                me["read"][rnd] = row + 1
+                yield None
+        ctas[c]["exited"] = True
+
+    live = {c: [proc(c), None] for c in range(CL)}
+    for _ in range(max_steps):
+        runnable = [c for c, (g, cond) in live.items() if cond is None or cond()]
+        if not runnable:
+            if not live:
+                return
+            raise Deadlock(f"seed {seed}: {sorted(live)}")
+        c = rng.choice(runnable)
+        try:
+            live[c][1] = next(live[c][0])
+        except StopIteration:
+            del live[c]
+    raise AssertionError("step limit")
+
+
+@pytest.mark.parametrize("CL", [1, 2, 4, 8])
+def test_cluster_exchange_has_no_race(CL):
+    for seed in range(300):
+        run_cluster(CL, rows=4, seed=seed)
+
+
+def test_cluster_exchange_early_exit_is_caught():
+    caught = 0
+    for seed in range(300):
+        try:
+            run_cluster(4, rows=3, seed=seed, early_exit=True)
+        except (Race, Deadlock):
+            caught += 1
+    assert caught > 0
