@@ -17,7 +17,7 @@ INCLUDE = os.path.join(ROOT, "include")
 OUT_DIR = os.path.join(PKG, "_build")
 LIB = os.path.join(OUT_DIR, "libsfar.so")
 
-SOURCES = ["sfar_host.cu", "k_ll.cu", "k_ll128.cu", "k_sentinel.cu", "k_db.cu", "k_twoshot.cu", "k_tma.cu",
+SOURCES = ["sfar_host.cu", "k_ll.cu", "k_ll128.cu", "k_sentinel.cu", "k_db.cu", "k_twoshot.cu", "k_twoshot_sent.cu", "k_tma.cu",
            "k_atomic.cu", "k_fused.cu", "k_fused8.cu", "k_fused_ts.cu", "k_gemv.cu",
            "k_misc.cu", "sfar_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

@@ -10,9 +10,13 @@
 //
 // Line: word 0 = flag (epoch), words 1..31 = 124 bytes of payload.  A warp
 // moves 4 lines (496 payload bytes = 31 input vectors) per iteration; lane
-// l holds 16 bytes of line l / 8.  The writer stores the payload, then
-// (after __syncwarp and one fence.acq_rel.gpu for all its lines) the flags;
-// the reader polls the flag, fences, then reads the payload.  The sum is
+// l holds 16 bytes of line l / 8.  The writer stores the payload of all its
+// lines, then __syncwarp (the warp barrier orders every lane's payload
+// stores before what each lane does next), then the flag lanes store the
+// epoch with st.release.gpu: the release covers the payload the flag lane
+// has observed through the barrier.  The reader polls its flag with
+// ld.acquire.gpu, then __syncwarp passes each lane's acquisition on to the
+// lanes that read the other peers' payload of the same line.  The sum is
 // folded in line layout (the reduction is element-wise and lines keep 4-byte
 // words intact) and unpacked to vector layout for the output store.
 //
@@ -43,7 +47,7 @@ __global__ void __launch_bounds__(SFAR_THREADS) k_ll128(const __grid_constant__ 
     const size_t slot = a.slot;
     sfar_stamp_after(c, TP_INPUT, x0.x);
 
-    // send: payload of every line to every peer, then one fence, then the flags
+    // send: payload of every line to every peer, a warp barrier, then the flags
     if (!c.drop) {
         for (unsigned long long it = it0; it < nit; it += its) {
             const uint4 x = it == it0 ? x0 : (lane < 31 ? load_vec<ES>(a.in[r], it * 31ull + lane, nbytes) : zero);
@@ -58,11 +62,10 @@ __global__ void __launch_bounds__(SFAR_THREADS) k_ll128(const __grid_constant__ 
             }
         }
         __syncwarp();
-        fence_acq_rel_gpu();
         for (unsigned long long it = it0; it < nit; it += its)
             for (int i = m; i < R - 1; i += 8) {
                 const int p = peer_of(r, i);
-                st_relaxed_u32((uint32_t *)(a.region + ((size_t)(p * 2 + c.par) * R + r) * slot +
+                st_release_u32((uint32_t *)(a.region + ((size_t)(p * 2 + c.par) * R + r) * slot +
                                             (it * 4ull + g) * 128ull),
                                e);
             }
@@ -81,7 +84,7 @@ __global__ void __launch_bounds__(SFAR_THREADS) k_ll128(const __grid_constant__ 
             const int q = peer_of(r, i);
             const uint32_t *f = (const uint32_t *)(mine + (size_t)q * slot + loff);
             SfarWaiter w;
-            while (ld_relaxed_u32(f) != e) {
+            while (ld_acquire_u32(f) != e) {
                 if (w.tick(a.ctl)) {
                     sfar_record_fault(a.ctl, r, k, q, e, SFAR_WAIT_LL128);
                     lok = 0;
@@ -92,7 +95,7 @@ __global__ void __launch_bounds__(SFAR_THREADS) k_ll128(const __grid_constant__ 
         ok = __all_sync(SFAR_FULL, lok) != 0;
         if (!ok)
             break;
-        fence_acq_rel_gpu();
+        __syncwarp();
         const uint4 x = it == it0 ? x0 : (lane < 31 ? load_vec<ES>(a.in[r], it * 31ull + lane, nbytes) : zero);
         const uint4 own = ll128_pack(x, lane);
         uint4 y[RB];

@@ -114,7 +114,10 @@ __global__ void __launch_bounds__(SFAR_TMA_THREADS, 1) k_tma(const __grid_consta
 {
     constexpr int ES = DT == 0 ? 2 : 4;
     constexpr int NB = TMA_OUT_BUFS;
-    const SfarEntry ent = sfar_entry(a);
+    // Early ticket (see sfar_entry): the epoch atomic overlaps the wait for the
+    // predecessor.  A successor cannot start on this kernel's SMs anyway (its
+    // shared memory fills them), so launching it earlier costs nothing here.
+    const SfarEntry ent = sfar_entry<true>(a);
     const int R = a.R, K = a.K;
     const int r = blockIdx.x / K, k = blockIdx.x - r * K;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -294,6 +297,7 @@ __global__ void __launch_bounds__(SFAR_TMA_THREADS, 1) k_tma(const __grid_consta
         }
     }
     __syncthreads();
+    sfar_stamp(c, TP_INPUT);        // this path: the CTA's tiles are folded and stored
     // completion: tell every rank this owner's part of its output is written
     if (tid < 32) {
         fence_acq_rel_gpu();

@@ -30,7 +30,9 @@ thread_local sfar_status g_last_error = SFAR_OK;
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 size_t ceil_div(size_t x, size_t a) { return (x + a - 1) / a; }
 
-const size_t kTmaMinBytesPerCta = 32u << 10;
+// TMA path: each CTA takes at least this many bytes of a chunk, so from
+// about 150 KB per chunk every SM streams (one CTA per SM).
+const size_t kTmaMinBytesPerCta = 8u << 10;
 
 }  // namespace
 
@@ -49,8 +51,9 @@ struct sfar {
     SfarCtl *ctl = nullptr;
     uint8_t *r_raw = nullptr, *r_ll = nullptr, *r_ll128 = nullptr, *r_sent = nullptr;
     uint8_t *r_rs = nullptr, *r_ag = nullptr;
+    uint8_t *r_srs = nullptr, *r_sag = nullptr;   // sentinel two-shot: RS and AG regions (sentinel-prefilled)
     uint8_t *r_acc = nullptr, *r_agx = nullptr;   // atomic path: accumulator and all-gather lines
-    size_t s_raw = 0, s_ll = 0, s_ll128 = 0, s_2s = 0, s_at = 0, sent_bytes = 0;
+    size_t s_raw = 0, s_ll = 0, s_ll128 = 0, s_2s = 0, s_at = 0, s_ts = 0, sent_bytes = 0;
     int mode = SFAR_LAUNCH_SERIAL;
     int ctas_override = 0, threads_override = 0;
     long long last_key = -1;            // overlap mode: geometry of the previous call
@@ -83,6 +86,7 @@ static const void *kernel_for(const sfar *h, int p, int test)
     case SFAR_LL128: return sfar_kernel_ll128(h->dt, wide, test);
     case SFAR_SENTINEL: return sfar_kernel_sentinel(h->dt, wide, test);
     case SFAR_TWOSHOT: return sfar_kernel_twoshot(h->dt, wide, test);
+    case SFAR_TWOSHOT_SENTINEL: return sfar_kernel_twoshot_sent(h->dt, wide, test);
     case SFAR_TWOSHOT_TMA: return sfar_kernel_tma(h->dt, test);
     case SFAR_LL128_ATOMIC: return sfar_kernel_atomic(h->dt, wide, test);
     default: return nullptr;
@@ -124,6 +128,9 @@ static size_t work_units(const sfar *h, int p, size_t n, size_t *chunk)
     case SFAR_TWOSHOT_TMA:
         *chunk = align_up(ceil_div(n, (size_t)h->R), 16 / (size_t)h->es);
         return *chunk * (size_t)h->es;
+    case SFAR_TWOSHOT_SENTINEL:                                // 8-byte units of a chunk
+        *chunk = align_up(ceil_div(n, (size_t)h->R), 16 / (size_t)h->es);
+        return *chunk * (size_t)h->es / 8;
     case SFAR_LL128_ATOMIC:
         *chunk = align_up(ceil_div(n, (size_t)h->R), 31);
         return *chunk / 31;
@@ -267,6 +274,8 @@ sfar_t *sfar_create(int R, size_t max_bytes, sfar_dtype dt)
         h->s_2s = align_up(c / epi * 512, 256);
         // atomic path: 128-byte lines of 31 elements per (owner, parity)
         h->s_at = align_up(ceil_div(ceil_div(nmax, (size_t)R), 31) * 128, 256);
+        // sentinel two-shot: one chunk of raw bytes per (owner or receiver, parity, peer)
+        h->s_ts = align_up(align_up(ceil_div(nmax, (size_t)R), 16 / (size_t)h->es) * (size_t)h->es, 256);
     }
     const size_t RR2 = (size_t)R * 2 * R;
     size_t off = 0;
@@ -288,10 +297,12 @@ sfar_t *sfar_create(int R, size_t max_bytes, sfar_dtype dt)
     const size_t o_ll128 = carve(RR2 * h->s_ll128);
     const size_t o_rs = carve(RR2 * h->s_2s);
     const size_t o_ag = carve(RR2 * h->s_2s);
-    const size_t o_sent = carve(RR2 * h->s_raw);
+    const size_t o_sent = carve(RR2 * h->s_raw);            // the sentinel-prefilled regions, back to back
+    const size_t o_srs = carve(RR2 * h->s_ts);
+    const size_t o_sag = carve(RR2 * h->s_ts);
     const size_t o_acc = carve((size_t)R * 2 * h->s_at);
     const size_t o_agx = carve(RR2 * h->s_at);
-    h->sent_bytes = RR2 * h->s_raw;
+    h->sent_bytes = o_sag + RR2 * h->s_ts - o_sent;
     h->ws_bytes = off;
 
     if (cudaMalloc(&h->ws, h->ws_bytes) != cudaSuccess) {
@@ -313,6 +324,8 @@ sfar_t *sfar_create(int R, size_t max_bytes, sfar_dtype dt)
     h->r_rs = h->ws + o_rs;
     h->r_ag = h->ws + o_ag;
     h->r_sent = h->ws + o_sent;
+    h->r_srs = h->ws + o_srs;
+    h->r_sag = h->ws + o_sag;
     h->r_acc = h->ws + o_acc;
     h->r_agx = h->ws + o_agx;
 
@@ -528,6 +541,11 @@ sfar_status sfar_allreduce(sfar_t *h, const void *const in[], void *const out[],
         a.region2 = h->r_agx;
         a.slot = h->s_at;
         break;
+    case SFAR_TWOSHOT_SENTINEL:
+        a.region = h->r_srs;
+        a.region2 = h->r_sag;
+        a.slot = h->s_ts;
+        break;
     case SFAR_TWOSHOT_TMA:
         a.fa = h->fc;
         a.fb = h->fd;
@@ -543,9 +561,15 @@ sfar_status sfar_allreduce(sfar_t *h, const void *const in[], void *const out[],
     cfg.dynamicSmemBytes = smem_for(h, p);
     cfg.stream = (cudaStream_t)s;
     cudaLaunchAttribute attr[1];
-    if (h->mode != SFAR_LAUNCH_PLAIN) {
+    if (h->mode == SFAR_LAUNCH_SERIAL || h->mode == SFAR_LAUNCH_OVERLAP) {
         attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
         attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+    } else if (h->mode == SFAR_LAUNCH_COOPERATIVE) {
+        // every CTA of the grid is placed at once, or the launch fails
+        attr[0].id = cudaLaunchAttributeCooperative;
+        attr[0].val.cooperative = 1;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
     }
@@ -918,7 +942,7 @@ static sfar_status fused_call(sfar *h, const void *const in[], const void *const
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     int na_attr = 1;
-    if (h->mode != SFAR_LAUNCH_PLAIN && !solo) {
+    if ((h->mode == SFAR_LAUNCH_SERIAL || h->mode == SFAR_LAUNCH_OVERLAP) && !solo) {
         attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
         attr[1].val.programmaticStreamSerializationAllowed = 1;
         na_attr = 2;
@@ -1019,7 +1043,7 @@ sfar_status sfar_rowpar_gemv(sfar_t *h, const void *const x[], const void *const
     cfg.blockDim = dim3(SFAR_GEMV_SEGMENTS * 32);
     cfg.stream = (cudaStream_t)s;
     cudaLaunchAttribute attr[1];
-    if (h->mode != SFAR_LAUNCH_PLAIN) {
+    if (h->mode == SFAR_LAUNCH_SERIAL || h->mode == SFAR_LAUNCH_OVERLAP) {
         attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
         attr[0].val.programmaticStreamSerializationAllowed = 1;
         cfg.attrs = attr;
@@ -1129,7 +1153,8 @@ sfar_status sfar_test_force_single_buffer(sfar_t *h, int on, sfar_stream_t s)
 
 sfar_status sfar_set_launch_mode(sfar_t *h, int mode)
 {
-    if (!h || (mode != SFAR_LAUNCH_SERIAL && mode != SFAR_LAUNCH_OVERLAP && mode != SFAR_LAUNCH_PLAIN))
+    if (!h || (mode != SFAR_LAUNCH_SERIAL && mode != SFAR_LAUNCH_OVERLAP && mode != SFAR_LAUNCH_PLAIN &&
+               mode != SFAR_LAUNCH_COOPERATIVE))
         return SFAR_ERR_INVALID;
     h->mode = mode;
     h->last_key = -1;

@@ -64,6 +64,7 @@ const void *sfar_kernel_ll128(int dt, int wide, int test);
 const void *sfar_kernel_sentinel(int dt, int wide, int test);
 const void *sfar_kernel_db(int dt, int wide, int test, int baseline);
 const void *sfar_kernel_twoshot(int dt, int wide, int test);
+const void *sfar_kernel_twoshot_sent(int dt, int wide, int test);
 const void *sfar_kernel_tma(int dt, int test);
 const void *sfar_kernel_atomic(int dt, int wide, int test);
 const void *sfar_kernel_set_knob();

@@ -17,6 +17,11 @@
 // cleared between calls), and the receive region is never cleared because
 // each call's flags carry a larger epoch than anything left behind.  Calls
 // whose kernels overlap on the GPU (concurrent streams) race on the array.
+//
+// Failures: a bounded device wait that gives up records itself in the
+// array's status block, and every later kernel then exits at once.
+// sfar_noalloc_status reads that record (and, once it has reported a
+// failure, makes later calls return SFAR_ERR_POISONED), or clears it.
 #include <cuda_runtime.h>
 #include <string.h>
 
@@ -24,6 +29,7 @@
 
 #include "sfar.h"
 #include "sfar_internal.h"
+#include "sfar_test.h"
 
 namespace {
 
@@ -85,6 +91,16 @@ namespace {
 std::mutex g_mu;
 unsigned char *g_ptr[kMaxDevices];     // device address of the array, per device
 bool g_ready[kMaxDevices];
+bool g_poisoned[kMaxDevices];          // a device-side failure was reported and not cleared
+
+// The status block's first 32 bytes: the code and the fault record.
+struct FaultRecord {
+    int status, f_rank, f_cta, f_peer;
+    uint32_t f_epoch;
+    int f_where;
+    int pad[2];
+};
+static_assert(sizeof(FaultRecord) == 32, "status block prefix");
 
 // Once per device, with that device current: find the array's device address
 // (in host code its name is only a stand-in), check that the grid of the
@@ -168,6 +184,11 @@ extern "C" sfar_status sfar_allreduce_noalloc(const void *const in[], void *cons
     const sfar_status st = setup(dev, (cudaStream_t)s, &base);
     if (st != SFAR_OK)
         return st;
+    {
+        std::lock_guard<std::mutex> lock(g_mu);
+        if (g_poisoned[dev])
+            return SFAR_ERR_POISONED;
+    }
 
     SfarArgs a;
     memset(&a, 0, sizeof a);
@@ -203,4 +224,86 @@ extern "C" sfar_status sfar_allreduce_noalloc(const void *const in[], void *cons
         return SFAR_ERR_CUDA;
     }
     return SFAR_OK;
+}
+
+namespace {
+
+sfar_status current_device(int *dev)
+{
+    if (cudaGetDevice(dev) != cudaSuccess || *dev < 0 || *dev >= kMaxDevices) {
+        cudaGetLastError();
+        return SFAR_ERR_CUDA;
+    }
+    return SFAR_OK;
+}
+
+sfar_status write_record(unsigned char *base, const FaultRecord &rec)
+{
+    if (cudaMemcpy(base, &rec, sizeof rec, cudaMemcpyHostToDevice) != cudaSuccess) {
+        cudaGetLastError();
+        return SFAR_ERR_CUDA;
+    }
+    return SFAR_OK;
+}
+
+}  // namespace
+
+extern "C" sfar_status sfar_noalloc_status(sfar_fault *info, int clear)
+{
+    int dev = 0;
+    sfar_status st = current_device(&dev);
+    if (st != SFAR_OK)
+        return st;
+    unsigned char *base = nullptr;
+    {
+        std::lock_guard<std::mutex> lock(g_mu);
+        if (g_ready[dev])
+            base = g_ptr[dev];
+    }
+    FaultRecord rec;
+    memset(&rec, 0, sizeof rec);
+    if (base && cudaMemcpy(&rec, base, sizeof rec, cudaMemcpyDeviceToHost) != cudaSuccess) {
+        cudaGetLastError();
+        return SFAR_ERR_CUDA;
+    }
+    const sfar_status code = rec.status;
+    if (info) {
+        info->code = code;
+        info->rank = code ? rec.f_rank : -1;
+        info->cta = code ? rec.f_cta : -1;
+        info->peer = code ? rec.f_peer : -1;
+        info->epoch = code ? rec.f_epoch : 0;
+        info->where = code ? rec.f_where : 0;
+    }
+    if (clear && base) {
+        FaultRecord zero;
+        memset(&zero, 0, sizeof zero);
+        zero.f_rank = zero.f_cta = zero.f_peer = -1;
+        st = write_record(base, zero);
+        if (st != SFAR_OK)
+            return st;
+    }
+    std::lock_guard<std::mutex> lock(g_mu);
+    g_poisoned[dev] = clear ? false : (g_poisoned[dev] || code != SFAR_OK);
+    return code;
+}
+
+extern "C" sfar_status sfar_test_noalloc_record_failure(int rank, int peer, int where)
+{
+    int dev = 0;
+    sfar_status st = current_device(&dev);
+    if (st != SFAR_OK)
+        return st;
+    unsigned char *base = nullptr;
+    st = setup(dev, nullptr, &base);
+    if (st != SFAR_OK)
+        return st;
+    FaultRecord rec;
+    memset(&rec, 0, sizeof rec);
+    rec.status = SFAR_ERR_TIMEOUT;
+    rec.f_rank = rank;
+    rec.f_cta = 0;
+    rec.f_peer = peer;
+    rec.f_where = where;
+    return write_record(base, rec);
 }

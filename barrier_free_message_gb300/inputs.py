@@ -14,6 +14,10 @@ bf16, or kept as fp32.
 Because every call has its own generator, any single call can be redrawn on
 its own (the sampled parity checks at full size rely on this).  Values are
 finite, so they never equal the sentinel bit patterns (all ones).
+
+The large-message (bandwidth) workloads, 4-256 MB per rank, draw the same
+distributions with the device's generator instead (:func:`draw_device`);
+their bits reach the oracle by a copy to the host.
 """
 from dataclasses import dataclass
 
@@ -73,6 +77,27 @@ def draw(seed: int, call: int, R: int, n: int, dist: str = "uniform", sigma: flo
 
 def draw_workload_call(w: Workload, call: int) -> torch.Tensor:
     return draw(w.seed, call, w.R, w.n, w.dist, w.sigma, w.dtype)
+
+
+def draw_device(seed: int, call: int, R: int, n: int, dist: str = "normal", sigma: float = 1.0,
+                dtype: str = "bf16", device="cuda") -> list:
+    """Inputs of the large-message workloads (hundreds of MB per rank, too slow
+    to draw on the host): R separate device buffers of n elements, drawn by
+    the device's own generator seeded with ``seed * 2**32 + call``, one rank
+    after another, with the same distributions and rounding as :func:`draw`.
+    The bit patterns differ from :func:`draw`'s; both sides of a comparison
+    read the same buffers (the oracle after a copy to the host)."""
+    g = torch.Generator(device=device).manual_seed(int(seed) * (1 << 32) + int(call))
+    out = []
+    for _ in range(R):
+        if dist == "uniform":
+            x = torch.rand(n, generator=g, device=device) * 2.0 - 1.0
+        elif dist == "normal":
+            x = torch.randn(n, generator=g, device=device) * sigma
+        else:
+            raise ValueError(f"unknown distribution {dist!r}")
+        out.append(x.to(torch.bfloat16) if dtype == "bf16" else x)
+    return out
 
 
 def to_bits(x: torch.Tensor) -> np.ndarray:

@@ -14,17 +14,18 @@ from . import _build
 
 SFAR_BF16, SFAR_FP32 = 0, 1
 SFAR_BASELINE, SFAR_DB, SFAR_LL, SFAR_LL128, SFAR_SENTINEL, SFAR_TWOSHOT, SFAR_TWOSHOT_TMA, \
-    SFAR_LL128_ATOMIC = range(8)
+    SFAR_LL128_ATOMIC, SFAR_TWOSHOT_SENTINEL = range(9)
 PROTOS = {"baseline": SFAR_BASELINE, "db": SFAR_DB, "ll": SFAR_LL, "ll128": SFAR_LL128,
           "sentinel": SFAR_SENTINEL, "twoshot": SFAR_TWOSHOT, "twoshot_tma": SFAR_TWOSHOT_TMA,
-          "ll128_atomic": SFAR_LL128_ATOMIC}
+          "ll128_atomic": SFAR_LL128_ATOMIC, "twoshot_sent": SFAR_TWOSHOT_SENTINEL}
 # every protocol but ll128_atomic returns the rank-order fold bit for bit
 EXACT_PROTOS = [p for p in PROTOS if p != "ll128_atomic"]
 DTYPES = {"bf16": SFAR_BF16, "fp32": SFAR_FP32}
 SFAR_OK, SFAR_ERR_INVALID, SFAR_ERR_CUDA, SFAR_ERR_OOM, SFAR_ERR_TIMEOUT, SFAR_ERR_UNSUPPORTED, \
     SFAR_ERR_POISONED = range(7)
-SFAR_LAUNCH_SERIAL, SFAR_LAUNCH_OVERLAP, SFAR_LAUNCH_PLAIN = 0, 1, 2
-MODES = {"serial": SFAR_LAUNCH_SERIAL, "overlap": SFAR_LAUNCH_OVERLAP, "plain": SFAR_LAUNCH_PLAIN}
+SFAR_LAUNCH_SERIAL, SFAR_LAUNCH_OVERLAP, SFAR_LAUNCH_PLAIN, SFAR_LAUNCH_COOPERATIVE = 0, 1, 2, 3
+MODES = {"serial": SFAR_LAUNCH_SERIAL, "overlap": SFAR_LAUNCH_OVERLAP, "plain": SFAR_LAUNCH_PLAIN,
+         "cooperative": SFAR_LAUNCH_COOPERATIVE}
 WAIT_NAMES = {1: "done", 2: "ll", 3: "sentinel", 4: "ready", 5: "bottom", 6: "ll128", 7: "rs", 8: "ag",
               9: "arrive", 10: "complete", 11: "copy", 12: "counter",
               13: "cluster"}
@@ -58,6 +59,8 @@ _SIGS = [
     ("sfar_max_bytes", ctypes.c_size_t, [ctypes.c_void_p, ctypes.c_int]),
     ("sfar_allreduce_noalloc", ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t,
                                               ctypes.c_int, ctypes.c_void_p]),
+    ("sfar_noalloc_status", ctypes.c_int, [ctypes.POINTER(SfarFault), ctypes.c_int]),
+    ("sfar_test_noalloc_record_failure", ctypes.c_int, [ctypes.c_int, ctypes.c_int, ctypes.c_int]),
     ("sfar_allreduce_add_rmsnorm", ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
                                                   ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t,
                                                   ctypes.c_size_t, ctypes.c_float, ctypes.c_void_p]),
@@ -185,6 +188,18 @@ def sfar_test_query_fused_path(h, rows: int, hidden: int):
 def sfar_allreduce_noalloc(in_ptrs, out_ptrs, R: int, n: int, dtype="bf16", stream=None) -> int:
     dt = DTYPES[dtype] if isinstance(dtype, str) else int(dtype)
     return lib().sfar_allreduce_noalloc(_ptr_array(in_ptrs), _ptr_array(out_ptrs), R, n, dt, _stream(stream))
+
+
+def sfar_noalloc_status(clear: bool = False):
+    """(code, fault) of sfar_allreduce_noalloc on the current device; clear
+    erases a recorded failure."""
+    f = SfarFault()
+    code = lib().sfar_noalloc_status(ctypes.byref(f), 1 if clear else 0)
+    return code, f
+
+
+def sfar_test_noalloc_record_failure(rank: int, peer: int, where: int) -> int:
+    return lib().sfar_test_noalloc_record_failure(rank, peer, where)
 
 
 def sfar_status_get(h):

@@ -62,7 +62,7 @@ typedef enum {
                              buffered (medium messages)                               */
     SFAR_TWOSHOT_TMA = 6, /* reduce-scatter + all-gather straight from the inputs to
                              the outputs with TMA bulk copies (large messages)        */
-    SFAR_LL128_ATOMIC = 7 /* reduce-scatter by hardware atomic adds into 128-byte
+    SFAR_LL128_ATOMIC = 7, /* reduce-scatter by hardware atomic adds into 128-byte
                              lines whose first word counts the arrivals, then an
                              all-gather over flagged lines (page 1, "Four
                              barrier-free mechanisms", part 4).  NOT bit-exact: the
@@ -72,9 +72,14 @@ typedef enum {
                              the output type (exact when every partial sum is
                              representable, e.g. small integers).  Identical on
                              every rank.                                               */
+    SFAR_TWOSHOT_SENTINEL = 8 /* reduce-scatter + all-gather over sentinel-prefilled,
+                                 double-buffered receive buffers: the pages' two-phase
+                                 LLBuffer algorithm for 64 KB - 1 MB (page 1, "Unified
+                                 primitives and API design", table of variants).  Inputs
+                                 must not contain the sentinel pattern (as SFAR_SENTINEL) */
 } sfar_proto;
 
-#define SFAR_NUM_PROTOS 8
+#define SFAR_NUM_PROTOS 9
 
 typedef int sfar_status;
 #define SFAR_OK 0
@@ -259,13 +264,32 @@ sfar_status sfar_add_rmsnorm(sfar_t *h, const void *const a[], const void *const
  * the last call left (its call counters keep counting); calls whose kernels
  * overlap on the GPU, e.g. on two streams at once, race on it.  Returns
  * SFAR_ERR_UNSUPPORTED on a device that is not sm_103 and SFAR_ERR_CUDA if a
- * CUDA call fails.  A device-side failure stays recorded in the array and
- * makes later calls return without writing their outputs.
+ * CUDA call fails.  A device-side failure (a bounded wait that gave up)
+ * stays recorded in the array, and every later kernel then returns without
+ * writing its outputs; sfar_noalloc_status reports it, after which calls
+ * return SFAR_ERR_POISONED and enqueue nothing until the record is cleared.
  */
 #define SFAR_NOALLOC_MAX_RANKS 8
 #define SFAR_NOALLOC_MAX_BYTES 16384
 sfar_status sfar_allreduce_noalloc(const void *const in[], void *const out[], int R, size_t n, sfar_dtype dt,
                                    sfar_stream_t s);
+
+/*
+ * sfar_noalloc_status: the outcome of the sfar_allreduce_noalloc calls made
+ * so far on the current device, read from the fixed array's status block by
+ * a synchronous copy (synchronise the streams of those calls first).  Returns
+ * SFAR_OK, or SFAR_ERR_TIMEOUT if a bounded device wait of one of them gave
+ * up, and fills *info (if not NULL) as sfar_status_get does.  With clear == 0
+ * a reported failure poisons the entry point on this device: later
+ * sfar_allreduce_noalloc calls return SFAR_ERR_POISONED.  With clear != 0 it
+ * returns the recorded code, then erases the record and the poison, and
+ * later calls compute again: the array's call counters stay consistent
+ * across a failed call, so nothing else needs resetting.  Clear only while
+ * no kernel of the entry point runs on the device.  SFAR_OK on a device that
+ * has made no such call; SFAR_ERR_CUDA if a copy fails.  Like the entry point
+ * itself, it has no counterpart in the pages.
+ */
+sfar_status sfar_noalloc_status(sfar_fault *info, int clear);
 
 #ifdef __cplusplus
 }

@@ -62,10 +62,16 @@ sfar_status sfar_test_force_single_buffer(sfar_t *h, int on, sfar_stream_t s);
  * more than three quarters of the device's co-resident clusters, and every
  * two-shot fused call, runs with serial semantics; the first of those also
  * without programmatic launch, and lets no successor launch before it ends.
+ * SFAR_LAUNCH_COOPERATIVE: stream order, and sfar_allreduce launches its
+ * kernel as a cooperative grid, so the device places all of its CTAs at
+ * once or the launch fails (SFAR_ERR_CUDA) instead of a wait timing out;
+ * no programmatic launch.  The fused and projection calls launch as in
+ * SFAR_LAUNCH_PLAIN.
  */
 #define SFAR_LAUNCH_SERIAL 0
 #define SFAR_LAUNCH_OVERLAP 1
 #define SFAR_LAUNCH_PLAIN 2
+#define SFAR_LAUNCH_COOPERATIVE 3
 sfar_status sfar_set_launch_mode(sfar_t *h, int mode);
 
 /*
@@ -75,8 +81,10 @@ sfar_status sfar_set_launch_mode(sfar_t *h, int mode);
  * trace[((e mod calls) * grid + b) * 8 + point], e the CTA's epoch and grid
  * R * CTAs per rank of that call.  Points: 0 kernel entry, 1 programmatic
  * launch wait returned, 2 epoch known (overlap mode: after the hand-off),
- * 3 first input vector arrived, 4 sends issued (DB/baseline: top barrier
- * passed), 5 receive and reduction done, 6 exit; slot 7 holds e itself.
+ * 3 first input vector arrived (SFAR_TWOSHOT_TMA: the CTA's tiles are all
+ * folded and stored), 4 sends issued (DB/baseline: top barrier passed;
+ * SFAR_TWOSHOT_TMA: every rank arrived), 5 receive and reduction done
+ * (SFAR_TWOSHOT_TMA: every owner completed), 6 exit; slot 7 holds e itself.
  * trace is a DEVICE array of calls * grid * 8 uint64 owned by the caller;
  * NULL or calls == 0 disarms.
  */
@@ -111,6 +119,13 @@ sfar_status sfar_test_set_fused_path(sfar_t *h, int path);
  * under the current setting: *path = 1 (one-shot) or 2 (two-shot).  Returns
  * what the call would return for the shape, without launching anything. */
 sfar_status sfar_test_query_fused_path(sfar_t *h, size_t rows, size_t hidden, int *path);
+
+/* Records in sfar_allreduce_noalloc's status block on the current device a
+ * wait that gave up (SFAR_ERR_TIMEOUT, the given rank, peer and where code),
+ * exactly as a device wait that runs out would: the host-side stand-in for a
+ * lost message, to test what callers of that entry point see afterwards.
+ * Synchronous; sets the fixed array up first if no call has done so yet. */
+sfar_status sfar_test_noalloc_record_failure(int rank, int peer, int where);
 
 /*
  * Latency floor probes.

@@ -8,8 +8,8 @@ from barrier_free_message_gb300 import _build, inputs, sfar
 
 TORCH_DT = {"bf16": torch.bfloat16, "fp32": torch.float32}
 ONESHOT = ["ll", "ll128", "sentinel", "db", "baseline"]
-ALL_PROTOS = ONESHOT + ["twoshot", "twoshot_tma"]
-DOUBLE_BUFFERED = ["ll", "ll128", "sentinel", "db", "twoshot"]
+ALL_PROTOS = ONESHOT + ["twoshot", "twoshot_sent", "twoshot_tma"]
+DOUBLE_BUFFERED = ["ll", "ll128", "sentinel", "db", "twoshot", "twoshot_sent"]
 
 
 def ensure_built():

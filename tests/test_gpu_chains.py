@@ -100,8 +100,8 @@ def decode_chain():
     return w, x_dev, out, exp
 
 
-@pytest.mark.parametrize("mode", ["serial", "overlap"])
-@pytest.mark.parametrize("proto", ONESHOT)
+@pytest.mark.parametrize("mode", ["serial", "overlap", "cooperative"])
+@pytest.mark.parametrize("proto", ALL_PROTOS)
 def test_decode_chain_10240_calls(decode_chain, proto, mode):
     w, x_dev, out, exp = decode_chain
     h = sfar.Sfar(w.R, w.bytes_per_rank, w.dtype)
@@ -124,17 +124,94 @@ def test_decode_chain_10240_calls(decode_chain, proto, mode):
         h.close()
 
 
+@pytest.fixture(scope="module")
+def fused_decode_chain(decode_chain):
+    """The fused AllReduce + residual add + RMSNorm over the decode chain: call
+    c reduces the decode workload's call c (one row of 8192 bf16 per rank)
+    with call (c + 1) mod 10,240 as its residual; weight normal(0, 1) seed 8.
+    Returns the device buffers and the oracle's y and z, [R, calls, n] each
+    (computed on the host in blocks of rows, one thread per block)."""
+    import concurrent.futures as cf
+    w, x_dev, _, _ = decode_chain
+    calls, R, n = x_dev.shape
+    eps = 1e-5
+    wt = inputs.draw(8, 0, 1, n, "normal", 1.0, "bf16")[0]
+    xb = inputs.to_bits(x_dev.cpu())                              # [calls, R, n]
+    X = np.ascontiguousarray(xb.transpose(1, 0, 2))               # [R, calls, n]
+    RES = np.roll(X, -1, axis=1)
+    wb = inputs.to_bits(wt[None, :])[0]
+    ys, zs = np.empty_like(X), np.empty_like(X)
+    step = -(-calls // THREADS)
+
+    def block(b0):
+        b1 = min(calls, b0 + step)
+        y, z = oracle.add_rmsnorm(X[:, b0:b1].reshape(R, -1), RES[:, b0:b1].reshape(R, -1), wb, eps, n)
+        ys[:, b0:b1] = y.reshape(R, b1 - b0, n)
+        zs[:, b0:b1] = z.reshape(R, b1 - b0, n)
+
+    with cf.ThreadPoolExecutor(THREADS) as ex:
+        list(ex.map(block, range(0, calls, step)))
+    del X, RES, xb
+    return wt.cuda(), eps, ys, zs
+
+
+@pytest.mark.parametrize("mode", ["serial", "overlap"])
+def test_fused_decode_chain_10240_calls(decode_chain, fused_decode_chain, mode):
+    """10,240 fused calls (R = 8, one row of 8192 bf16) in one graph, replayed
+    twice, every rank of every call bit for bit against the oracle."""
+    w, x_dev, _, _ = decode_chain
+    wd, eps, ys, zs = fused_decode_chain
+    calls, R, n = x_dev.shape
+    y = torch.empty_like(x_dev)
+    z = torch.empty_like(x_dev)
+    h = sfar.Sfar(R, 2 * n, "bf16")
+    try:
+        h.set_mode(mode)
+        P = lambda t, c: [t[c, r].data_ptr() for r in range(R)]
+        assert sfar.sfar_allreduce_add_rmsnorm(h.h, P(x_dev, 0), P(x_dev, 1), wd.data_ptr(), P(y, 0), P(z, 0), 1, n,
+                                               eps) == sfar.SFAR_OK
+        torch.cuda.synchronize()
+        status_ok(h.h, "fused warm-up")
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for c in range(calls):
+                code = sfar.sfar_allreduce_add_rmsnorm(h.h, P(x_dev, c), P(x_dev, (c + 1) % calls), wd.data_ptr(),
+                                                       P(y, c), P(z, c), 1, n, eps)
+                assert code == sfar.SFAR_OK
+        ey = torch.from_numpy(ys.view(np.int16)).cuda()
+        ez = torch.from_numpy(zs.view(np.int16)).cuda()
+        for rep in range(2):
+            y.view(torch.int16).fill_(-1)
+            z.view(torch.int16).fill_(-1)
+            g.replay()
+            torch.cuda.synchronize()
+            status_ok(h.h, f"fused {mode} replay {rep}")
+            for name, got, want in (("y", y, ey), ("z", z, ez)):
+                eq = (got.view(torch.int16).transpose(0, 1) == want).all(dim=2)      # [R, calls]
+                if not bool(eq.all()):
+                    r, c = (int(v) for v in torch.nonzero(~eq)[0])
+                    raise AssertionError(f"fused {mode} replay {rep}: {name} differs in "
+                                         f"{int((~eq).sum())} (rank, call) pairs, first rank {r} call {c}")
+        del g
+    finally:
+        h.close()
+
+
 def straggler_delays(calls, seed=3, hi_ns=20000):
     g = torch.Generator().manual_seed(seed)
     return torch.randint(0, hi_ns + 1, (calls,), generator=g, dtype=torch.int64).to(torch.int32).cuda()
 
 
 @pytest.mark.parametrize("phase", [0, 1])
-@pytest.mark.parametrize("proto", DOUBLE_BUFFERED)
+@pytest.mark.parametrize("proto", DOUBLE_BUFFERED + ["twoshot_tma"])
 def test_decode_chain_overlap_with_straggler(decode_chain, proto, phase):
-    """Calls overtake one another across ranks; double buffering keeps every call exact."""
+    """All 10,240 calls of the decode chain in one graph, in overlap mode, with
+    a straggler rank (call mod R) delayed 0-20 us per call: calls overtake one
+    another across ranks, and double buffering (the arrival and completion
+    flags for the TMA path, which has no receive buffers) keeps every call
+    exact."""
     w, x_dev, out, exp = decode_chain
-    calls = 1600
+    calls = w.calls
     h = sfar.Sfar(w.R, w.bytes_per_rank, w.dtype)
     try:
         h.set_mode("overlap")

@@ -31,6 +31,8 @@ Models (one CTA index; the protocols are per CTA index):
   buffers) or one buffer with a top and a bottom barrier (BASELINE).
 * two-shot over flagged lines: reduce-scatter into the owner's lines, then an
   all-gather into every rank's lines, both epoch-tagged.
+* two-shot over sentinels: the same two phases with raw values into
+  sentinel-prefilled slots, each refilled by its reader.
 * atomic accumulation: every rank adds into the owner's line and bumps its
   counter; the owner reads at counter = R, clears the line, all-gathers.
 
@@ -229,6 +231,87 @@ def test_two_shot_pull_planted_mistakes_are_caught(planted):
         except Race:
             caught += 1
     assert caught > 0, planted
+
+
+# ------------------------------------------------- two-shot over sentinels
+def twoshot_sentinel_model(R, double_buffer=True, refill=True, empty_owner=False, ag_wait=True):
+    """The pages' two-phase LLBuffer algorithm ("Every Microsecond Counts",
+    page 1, "Unified primitives and API design", table of variants: sentinel
+    synchronisation + double buffering): rank q stores share j raw into owner
+    j's slot rs[j][par][q]; the owner polls until none of its R - 1 slots
+    holds the sentinel, reads and refills them, then stores the reduced share
+    into ag[p][par][j] of every rank p, which polls, reads and refills.  With
+    empty_owner, the last rank's share is empty (a message shorter than
+    (R - 1) chunks): nobody sends it a share and nobody waits for its
+    all-gather."""
+    def procs_of(r, e, st):
+        rs = st.setdefault("rs", {})
+        ag = st.setdefault("ag", {})
+        par = e & 1 if double_buffer else 0
+        peers = [q for q in range(R) if q != r]
+        owns = lambda j: not (empty_owner and j == R - 1)
+
+        def put(region, key, val):
+            if region.get(key, SENT) is not SENT:
+                raise Race(f"rank {r} call {e} stored over {region[key]} at {key} (not read or refilled)")
+            region[key] = val
+
+        def take(region, key, want):
+            if region[key] != want:
+                raise Race(f"rank {r} call {e} read {region[key]} at {key}, wanted {want}")
+            region[key] = SENT if refill else ("stale",) + want
+
+        for j in peers:
+            if owns(j):
+                put(rs, (j, par, r), (r, e))
+                yield None
+        if owns(r):
+            for q in random.Random(r * 31 + e).sample(peers, len(peers)):
+                yield (lambda q=q: rs.get((r, par, q), SENT) is not SENT)
+                take(rs, (r, par, q), (q, e))
+                yield None
+            for p in peers:
+                put(ag, (p, par, r), (r, e))
+                yield None
+        for j in random.Random(r * 37 + e).sample(peers, len(peers)):
+            if owns(j) and ag_wait:
+                yield (lambda j=j: ag.get((r, par, j), SENT) is not SENT)
+                take(ag, (r, par, j), (j, e))
+                yield None
+    return procs_of
+
+
+@pytest.mark.parametrize("empty_owner", [False, True])
+@pytest.mark.parametrize("overlap", [False, True])
+@pytest.mark.parametrize("R", [2, 3, 4])
+def test_twoshot_sentinel_has_no_race(R, overlap, empty_owner):
+    for seed in SEEDS:
+        run(twoshot_sentinel_model(R, empty_owner=empty_owner), R, calls=6, overlap=overlap, seed=seed)
+
+
+@pytest.mark.parametrize("planted", ["no refill", "no all-gather wait"])
+def test_twoshot_sentinel_planted_mistakes_are_caught(planted):
+    kw = {"refill": planted != "no refill", "ag_wait": planted != "no all-gather wait"}
+    caught = 0
+    for seed in SEEDS:
+        try:
+            run(twoshot_sentinel_model(3, **kw), 3, calls=6, overlap=True, seed=seed)
+        except (Race, Deadlock):
+            caught += 1
+    assert caught > 0, planted
+
+
+@pytest.mark.parametrize("empty_owner", [False, True])
+def test_twoshot_sentinel_all_gather_orders_slot_reuse(empty_owner):
+    """As for the two-shot over flagged lines, the all-gather alone orders the
+    reuse of every slot: a single buffer is race-free too, so the second
+    buffer is extra safety, not a requirement (a sender reaches call e + 1
+    only after the owner's call-e all-gather, sent after its call-e reads;
+    an owner's call-e + 1 all-gather follows every rank's call-e + 1 send,
+    which follows that rank's call-e reads)."""
+    for seed in SEEDS:
+        run(twoshot_sentinel_model(3, double_buffer=False, empty_owner=empty_owner), 3, calls=6, overlap=True,
+            seed=seed)
 
 
 # ------------------------------------------------------------ DB / BASELINE

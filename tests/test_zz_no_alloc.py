@@ -47,6 +47,7 @@ def test_noalloc_matches_the_handle_path_on_two_calls(dtype, R, n):
             assert code == sfar.SFAR_OK, sfar.strerror(code)
             torch.cuda.synchronize()
             status_ok(h.h)
+            assert sfar.sfar_noalloc_status()[0] == sfar.SFAR_OK
             want = expected_bits(x)
             for r in range(R):
                 # bit-exact: the same fixed-order reduction on both paths
@@ -79,6 +80,65 @@ def test_noalloc_in_a_graph_after_setup():
             want = expected_bits(x)
             for r in range(R):
                 assert np.array_equal(_bits(outs[r]), as_uint(want[r]))
+
+
+def _noalloc_call(x, dtype):
+    R, n = x.shape
+    ins, outs = device_io(x)
+    code = sfar.sfar_allreduce_noalloc([t.data_ptr() for t in ins], [t.data_ptr() for t in outs], R, n, dtype)
+    return code, outs
+
+
+def test_noalloc_chain_of_mixed_sizes_and_types():
+    """R = 8 calls of different sizes (so different grids: 8192 elements, 37,
+    4099) and both element types in a row on the shared array, each compared
+    bit for bit with the oracle; the array's status stays clear."""
+    R = 8
+    plan = [("bf16", 8192), ("bf16", 37), ("fp32", 4093), ("bf16", 4099), ("fp32", 37), ("fp32", 4096),
+            ("bf16", 8192), ("fp32", 1)]
+    for i, (dtype, n) in enumerate(plan * 2):
+        x = inputs.draw(33, i, R, n, "normal", 1.0, dtype)
+        code, outs = _noalloc_call(x, dtype)
+        assert code == sfar.SFAR_OK, sfar.strerror(code)
+        torch.cuda.synchronize()
+        want = expected_bits(x)
+        for r in range(R):
+            assert np.array_equal(_bits(outs[r]), as_uint(want[r])), (i, dtype, n, r)
+    code, f = sfar.sfar_noalloc_status()
+    assert code == sfar.SFAR_OK, (code, f.where)
+
+
+def test_noalloc_failure_is_reported_then_cleared():
+    """A failed device wait (recorded on the host, as a wait that ran out
+    would record it): the next kernel writes nothing, the status call reports
+    the failure, later calls are refused until the record is cleared, and
+    calls after the clear compute the right sums again."""
+    R, n = 4, 1000
+    try:
+        assert sfar.sfar_test_noalloc_record_failure(2, 1, 2) == sfar.SFAR_OK
+        x = inputs.draw(34, 0, R, n, "normal", 1.0, "bf16")
+        code, outs = _noalloc_call(x, "bf16")
+        assert code == sfar.SFAR_OK                  # enqueued: the host has not read the record yet
+        torch.cuda.synchronize()
+        for o in outs:                               # the kernel saw the record and wrote nothing
+            assert (o.view(torch.uint8) == 0xA5).all()
+        code, f = sfar.sfar_noalloc_status()
+        assert code == sfar.SFAR_ERR_TIMEOUT and (f.rank, f.peer, f.where) == (2, 1, 2)
+        code, _ = _noalloc_call(x, "bf16")
+        assert code == sfar.SFAR_ERR_POISONED        # reported, so refused on the host
+        code, f = sfar.sfar_noalloc_status(clear=True)
+        assert code == sfar.SFAR_ERR_TIMEOUT         # the clearing read still returns what it cleared
+    finally:
+        sfar.sfar_noalloc_status(clear=True)
+    assert sfar.sfar_noalloc_status()[0] == sfar.SFAR_OK
+    for c in range(3):
+        x = inputs.draw(34, 1 + c, R, n, "normal", 1.0, "bf16")
+        code, outs = _noalloc_call(x, "bf16")
+        assert code == sfar.SFAR_OK
+        torch.cuda.synchronize()
+        want = expected_bits(x)
+        for r in range(R):
+            assert np.array_equal(_bits(outs[r]), as_uint(want[r])), (c, r)
 
 
 def test_noalloc_rejects_what_does_not_fit():
