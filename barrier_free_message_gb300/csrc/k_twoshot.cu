@@ -47,14 +47,22 @@ __global__ void __launch_bounds__(SFAR_THREADS) k_twoshot(const __grid_constant_
     const uint4 zero = make_uint4(0, 0, 0, 0);
     uint8_t *rs = a.region, *ag = a.region2;
 
-    // 1. reduce-scatter send
+    // 1. reduce-scatter send: per line group, every peer's input vector is
+    // loaded before the first store, so the R - 1 loads are in flight together
     if (!c.drop) {
-        for (int i = 0; i < R - 1; ++i) {
-            const int j = peer_of(r, i);
-            uint8_t *dst = rs + ((size_t)(j * 2 + c.par) * R + r) * slot;
-            for (unsigned long long it = it0; it < nitc; it += its) {
-                const uint4 x = lane < 31 ? load_vec<ES>(a.in[r], j * cvec + it * 31ull + lane, nbytes) : zero;
-                ll128_store_data(dst + (it * 4ull + g) * 128ull, m, ll128_pack(x, lane));
+        for (unsigned long long it = it0; it < nitc; it += its) {
+            uint4 xs[RB - 1];
+#pragma unroll
+            for (int i = 0; i < RB - 1; ++i)
+                if (i < R - 1)
+                    xs[i] = lane < 31 ? load_vec<ES>(a.in[r], peer_of(r, i) * cvec + it * 31ull + lane, nbytes) : zero;
+#pragma unroll
+            for (int i = 0; i < RB - 1; ++i) {
+                if (i < R - 1) {
+                    const int j = peer_of(r, i);
+                    uint8_t *dst = rs + ((size_t)(j * 2 + c.par) * R + r) * slot;
+                    ll128_store_data(dst + (it * 4ull + g) * 128ull, m, ll128_pack(xs[i], lane));
+                }
             }
         }
         __syncwarp();

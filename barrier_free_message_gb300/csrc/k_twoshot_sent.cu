@@ -96,16 +96,21 @@ __global__ void __launch_bounds__(SFAR_THREADS, 2) k_twoshot_sent(const __grid_c
     const size_t slot = a.slot;
     uint8_t *rs = a.region, *ag = a.region2;
 
-    // 1. reduce-scatter send
+    // 1. reduce-scatter send: every peer's unit is loaded before the first
+    // store, so the R - 1 loads are in flight together
     if (!c.drop) {
         for (unsigned long long u = u0; u < cu; u += stride) {
+            unsigned long long xs[RB - 1];
+#pragma unroll
+            for (int i = 0; i < RB - 1; ++i)
+                if (i < R - 1)
+                    xs[i] = as_word(in_unit(peer_of(r, i), u));
 #pragma unroll
             for (int i = 0; i < RB - 1; ++i) {
                 if (i < R - 1) {
                     const int j = peer_of(r, i);
                     if (valid(j, u))
-                        st_relaxed_u64(rs + ((size_t)(j * 2 + c.par) * R + r) * slot + u * TS_UB,
-                                       as_word(in_unit(j, u)));
+                        st_relaxed_u64(rs + ((size_t)(j * 2 + c.par) * R + r) * slot + u * TS_UB, xs[i]);
                 }
             }
         }

@@ -560,19 +560,21 @@ sfar_status sfar_allreduce(sfar_t *h, const void *const in[], void *const out[],
     cfg.blockDim = dim3((unsigned)threads);
     cfg.dynamicSmemBytes = smem_for(h, p);
     cfg.stream = (cudaStream_t)s;
-    cudaLaunchAttribute attr[1];
-    if (h->mode == SFAR_LAUNCH_SERIAL || h->mode == SFAR_LAUNCH_OVERLAP) {
-        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-        attr[0].val.programmaticStreamSerializationAllowed = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
-    } else if (h->mode == SFAR_LAUNCH_COOPERATIVE) {
-        // every CTA of the grid is placed at once, or the launch fails
-        attr[0].id = cudaLaunchAttributeCooperative;
-        attr[0].val.cooperative = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
+    cudaLaunchAttribute attr[2];
+    int nattr = 0;
+    if (h->mode != SFAR_LAUNCH_PLAIN) {
+        attr[nattr].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[nattr].val.programmaticStreamSerializationAllowed = 1;
+        ++nattr;
     }
+    if (h->mode == SFAR_LAUNCH_COOPERATIVE) {
+        // every CTA of the grid is placed at once, or the launch fails
+        attr[nattr].id = cudaLaunchAttributeCooperative;
+        attr[nattr].val.cooperative = 1;
+        ++nattr;
+    }
+    cfg.attrs = attr;
+    cfg.numAttrs = nattr;
     void *args[] = {&a};
     int cur = -1;
     cudaGetDevice(&cur);
@@ -906,7 +908,10 @@ static sfar_status fused_call(sfar *h, const void *const in[], const void *const
         ++c;
     na.F = 53 - c;
     a.overlap = 0;
-    const bool solo = allreduce && solo_grid(R * G, maxc);
+    // cooperative mode: the device places the whole grid at once, so no grid
+    // needs to run solo to be sure all of its clusters start
+    const bool coop = h->mode == SFAR_LAUNCH_COOPERATIVE;
+    const bool solo = allreduce && !coop && solo_grid(R * G, maxc);
     a.solo = solo ? 1 : 0;
     if (path == 2 || solo) {
         // the two-shot kernel and a solo grid never overtake a call, and the
@@ -936,16 +941,21 @@ static sfar_status fused_call(sfar *h, const void *const in[], const void *const
     cfg.gridDim = dim3((unsigned)(R * K));
     cfg.blockDim = dim3((unsigned)threads);
     cfg.stream = (cudaStream_t)s;
-    cudaLaunchAttribute attr[2];
+    cudaLaunchAttribute attr[3];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = (unsigned)CL;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     int na_attr = 1;
-    if ((h->mode == SFAR_LAUNCH_SERIAL || h->mode == SFAR_LAUNCH_OVERLAP) && !solo) {
-        attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-        attr[1].val.programmaticStreamSerializationAllowed = 1;
-        na_attr = 2;
+    if (h->mode != SFAR_LAUNCH_PLAIN && !solo) {
+        attr[na_attr].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[na_attr].val.programmaticStreamSerializationAllowed = 1;
+        ++na_attr;
+    }
+    if (coop && allreduce) {
+        attr[na_attr].id = cudaLaunchAttributeCooperative;
+        attr[na_attr].val.cooperative = 1;
+        ++na_attr;
     }
     cfg.attrs = attr;
     cfg.numAttrs = na_attr;
@@ -1043,7 +1053,7 @@ sfar_status sfar_rowpar_gemv(sfar_t *h, const void *const x[], const void *const
     cfg.blockDim = dim3(SFAR_GEMV_SEGMENTS * 32);
     cfg.stream = (cudaStream_t)s;
     cudaLaunchAttribute attr[1];
-    if (h->mode == SFAR_LAUNCH_SERIAL || h->mode == SFAR_LAUNCH_OVERLAP) {
+    if (h->mode != SFAR_LAUNCH_PLAIN) {
         attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
         attr[0].val.programmaticStreamSerializationAllowed = 1;
         cfg.attrs = attr;

@@ -508,13 +508,15 @@ def run_suite(args):
                 continue
             h = sfar.Sfar(R, 1 << 20, "bf16")
             for b in inputs.SWEEP_BYTES:
+                if args.suite_bytes and b != args.suite_bytes:
+                    continue
                 n, calls = b // 2, 32
                 x = torch.stack([inputs.draw(2, c, R, n, "uniform", 1.0, "bf16") for c in range(calls)])
                 xd = x.cuda()
                 od = torch.empty_like(xd)
                 for mode in ("serial", "overlap"):
                     h.set_mode(mode)
-                    for proto in ALL:
+                    for proto in (args.suite_protos.split(",") if args.suite_protos else ALL):
                         us = _time_chain(h, xd, od, proto)
                         k, t = h.launch(n, proto)
                         print(json.dumps({"suite": "latency", "R": R, "bytes": b, "mode": mode, "proto": proto,
@@ -1075,7 +1077,9 @@ def main():
     ap.add_argument("--large-dtype", choices=["bf16", "fp32"], default="bf16")
     ap.add_argument("--suite-r", type=int, default=0, help="atomic and fused suites: only this rank count")
     ap.add_argument("--suite-rows", type=int, default=0, help="fused suite: only this row count")
-    ap.add_argument("--suite-bytes", type=int, default=0, help="atomic suite: only this message size per rank")
+    ap.add_argument("--suite-bytes", type=int, default=0, help="latency and atomic suites: only this message size "
+                    "per rank")
+    ap.add_argument("--suite-protos", default="", help="latency suite: comma list of protocols (default: all)")
     ap.add_argument("--decode-layers", type=int, default=80, help="decode suite: layers per token")
     ap.add_argument("--suite", default="", help="comma list of latency,bandwidth,barriers,atomic,fused,decode: sweeps as JSON lines")
     args = ap.parse_args()

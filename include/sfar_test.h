@@ -62,11 +62,11 @@ sfar_status sfar_test_force_single_buffer(sfar_t *h, int on, sfar_stream_t s);
  * more than three quarters of the device's co-resident clusters, and every
  * two-shot fused call, runs with serial semantics; the first of those also
  * without programmatic launch, and lets no successor launch before it ends.
- * SFAR_LAUNCH_COOPERATIVE: stream order, and sfar_allreduce launches its
- * kernel as a cooperative grid, so the device places all of its CTAs at
- * once or the launch fails (SFAR_ERR_CUDA) instead of a wait timing out;
- * no programmatic launch.  The fused and projection calls launch as in
- * SFAR_LAUNCH_PLAIN.
+ * SFAR_LAUNCH_COOPERATIVE: as SFAR_LAUNCH_SERIAL, and every AllReduce
+ * kernel (sfar_allreduce, sfar_allreduce_add_rmsnorm) is launched as a
+ * cooperative grid, so the device places all of its CTAs at once or the
+ * launch fails (SFAR_ERR_CUDA) instead of a wait timing out; no fused grid
+ * then runs solo.
  */
 #define SFAR_LAUNCH_SERIAL 0
 #define SFAR_LAUNCH_OVERLAP 1

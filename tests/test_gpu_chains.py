@@ -155,7 +155,7 @@ def fused_decode_chain(decode_chain):
     return wt.cuda(), eps, ys, zs
 
 
-@pytest.mark.parametrize("mode", ["serial", "overlap"])
+@pytest.mark.parametrize("mode", ["serial", "overlap", "cooperative"])
 def test_fused_decode_chain_10240_calls(decode_chain, fused_decode_chain, mode):
     """10,240 fused calls (R = 8, one row of 8192 bf16) in one graph, replayed
     twice, every rank of every call bit for bit against the oracle."""

@@ -144,7 +144,7 @@ def test_special_rows_and_ranges():
         h.close()
 
 
-@pytest.mark.parametrize("mode", ["serial", "overlap"])
+@pytest.mark.parametrize("mode", ["serial", "overlap", "cooperative"])
 def test_fused_chain_1024_calls(mode):
     """The decode shape (R = 8, one row of 8192 bf16) for 1,024 graph-chained
     calls, each with its own inputs and residual."""
@@ -504,13 +504,15 @@ def test_two_shot_dropped_rank_times_out_and_reset_recovers():
         h.close()
 
 
-def test_large_grid_chain_does_not_stall():
+@pytest.mark.parametrize("mode", ["serial", "cooperative"])
+def test_large_grid_chain_does_not_stall(mode):
     """A one-shot grid that fills most of the device (R = 8, eight rows of
-    8192 bf16: 32 clusters of 8 CTAs) chained in a graph in serial mode:
-    launched as a programmatic dependent it sometimes had a cluster that
-    never started (its peers timed out); such grids now run solo.  Twenty
-    replays of 32 calls with a 50 ms wait limit, then the last call against
-    the oracle."""
+    8192 bf16: 32 clusters of 8 CTAs) chained in a graph: launched as a
+    programmatic dependent it sometimes had a cluster that never started
+    (its peers timed out), so in serial mode such grids run solo; in
+    cooperative mode they keep the programmatic launch and the device places
+    the whole grid at once.  Twenty replays of 32 calls with a 50 ms wait
+    limit, then the last call against the oracle."""
     R, rows, hidden, calls, eps = 8, 8, 8192, 32, 1e-5
     n = rows * hidden
     x = torch.stack([inputs.draw(1500, c, R, n, "normal", 1.0, "bf16") for c in range(calls)])
@@ -518,7 +520,7 @@ def test_large_grid_chain_does_not_stall():
     w = inputs.draw(1502, 0, 1, hidden, "normal", 1.0, "bf16")[0]
     h = sfar.Sfar(R, 2 * n, "bf16")
     try:
-        h.set_mode("serial")
+        h.set_mode(mode)
         assert sfar.sfar_test_set_fused_path(h.h, "oneshot") == sfar.SFAR_OK
         code, k, cl, t = sfar.sfar_test_query_norm_launch(h.h, rows, hidden)
         assert code == sfar.SFAR_OK and k * R // cl >= 24, (k, cl)          # a grid of most of the device
