@@ -895,7 +895,7 @@ def run_ours(args, world, rank):
     # the oracle's rows of every call that the replays and the end-to-end
     # loop compute (the replays run tokens (warm-up + i) % tokens)
     replay = replayed_tokens(tokens, args.warmup, args.steps)
-    e2e_tokens = sorted({i % tokens for i in range(max(e2e_steps, min(args.warmup, 3) if e2e_steps else 0))})
+    e2e_tokens = sorted({i % tokens for i in range(e2e_steps)})
     check_tokens = sorted(set(replay) | set(e2e_tokens))
     pos = {t: i for i, t in enumerate(check_tokens)}
     check_ids = [t * CALLS_PER_STEP + c for t in check_tokens for c in range(CALLS_PER_STEP)]
@@ -945,13 +945,16 @@ def run_ours(args, world, rank):
     h2d, d2h = torch.cuda.Stream(), torch.cuda.Stream()
     out_dev.view(torch.int16).fill_(-1)
     out_host.view(torch.int16).fill_(-1)
-    for i in range(min(args.warmup, 3) if e2e_steps else 0):
+    # warm-up: one untimed pass over the steps of the timed loop (the first
+    # host-to-device copies of a process ran at a tenth of the later rate)
+    for i in range(max(e2e_steps, min(args.warmup, 3)) if e2e_steps else 0):
         t = i % tokens
         sl = slice(t * CALLS_PER_STEP, (t + 1) * CALLS_PER_STEP)
         x_dev[sl].copy_(x_host[sl], non_blocking=True)
         graphs[t].replay()
         out_host[sl].copy_(out_dev[sl], non_blocking=True)
     torch.cuda.synchronize()
+    out_host.view(torch.int16).fill_(-1)
     barrier(world)
     s_ev, e_ev = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     ev_in = [torch.cuda.Event() for _ in range(e2e_steps)]
@@ -998,10 +1001,10 @@ def run_ours(args, world, rank):
 
     floor = floor_probe() if not args.no_floor else {"floor_us": float("nan")}
     large = large_message_roofline(hbm_peak) if not args.no_large else None
-    others = other_configs() if not args.no_configs else None
+    others = other_configs() if not args.no_configs and world == 1 else None
 
     cpu = None
-    if rank == 0 and not args.no_cpu:
+    if rank == 0 and world == 1 and not args.no_cpu:
         from oracle.build import build_oracle
         build_oracle()
         cpu_us, cpu_calls, cpu_s = oracle_cpu_time(x_host, budget_s=args.cpu_seconds)
@@ -1039,6 +1042,8 @@ def run_ours(args, world, rank):
             "protocols": per_proto,
             "floor": {k2: (round(v, 3) if isinstance(v, float) else v) for k2, v in floor.items()},
             "vs_floor": round(us / floor["floor_us"], 3),
+            "vs_floor_median_pair": (round(us / (floor["empty_kernel_us"] + floor["flag_rtt_median_us"]), 3)
+                                     if "flag_rtt_median_us" in floor else None),
             "roofline": roofline, "roofline_large": large, "configs": others,
             "e2e": ({"value": round(e2e_us, 3), "unit": "us/call", "h2d_bytes_per_step": step_bytes,
                      "d2h_bytes_per_step": step_bytes, "steps": e2e_steps, "bit_exact": e2e_ok,
@@ -1061,7 +1066,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--proto", choices=ALL, default="ll", help="headline protocol (the others of the one-shot "
                     "set are timed beside it unless --only)")
-    ap.add_argument("--mode", choices=["serial", "overlap", "plain", "cooperative"], default="serial")
+    ap.add_argument("--mode", choices=["serial", "overlap", "plain", "cooperative"], default="serial",
+                    help="launch mode of the handle (serial: the handle's default)")
     ap.add_argument("--no-large", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)

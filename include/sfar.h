@@ -145,8 +145,10 @@ sfar_status sfar_last_error(void);
  * capturable in a CUDA graph.  Returns, without enqueuing anything,
  * SFAR_ERR_INVALID for a bad argument, SFAR_ERR_POISONED after a device-side
  * failure that sfar_status_get has reported, SFAR_ERR_UNSUPPORTED if the
- * grid the call needs cannot be co-resident, and SFAR_ERR_CUDA if the launch
- * fails.  A device-side failure (a bounded wait giving up) does not show
+ * grid the call needs cannot be co-resident (every CTA of a call waits on
+ * others; the grid is sized for an idle device, and in the cooperative launch
+ * mode of sfar_test.h the device places it whole or refuses it), and
+ * SFAR_ERR_CUDA if the launch fails.  A device-side failure (a bounded wait giving up) does not show
  * here: it is recorded in the handle's status block (sticky) and every later
  * kernel of the handle exits at once; read it with sfar_status_get.
  */

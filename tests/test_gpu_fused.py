@@ -507,12 +507,12 @@ def test_two_shot_dropped_rank_times_out_and_reset_recovers():
 @pytest.mark.parametrize("mode", ["serial", "cooperative"])
 def test_large_grid_chain_does_not_stall(mode):
     """A one-shot grid that fills most of the device (R = 8, eight rows of
-    8192 bf16: 32 clusters of 8 CTAs) chained in a graph: launched as a
-    programmatic dependent it sometimes had a cluster that never started
-    (its peers timed out), so in serial mode such grids run solo; in
-    cooperative mode they keep the programmatic launch and the device places
-    the whole grid at once.  Twenty replays of 32 calls with a 50 ms wait
-    limit, then the last call against the oracle."""
+    8192 bf16: 32 clusters of 8 CTAs) chained in a graph: launched as a plain
+    programmatic dependent it sometimes had a cluster that never started (its
+    peers timed out).  In serial and cooperative mode the grid is now a
+    cooperative grid, which the device places whole, and keeps the
+    programmatic launch.  Twenty replays of 32 calls with a 50 ms wait limit,
+    then the last call against the oracle."""
     R, rows, hidden, calls, eps = 8, 8, 8192, 32, 1e-5
     n = rows * hidden
     x = torch.stack([inputs.draw(1500, c, R, n, "normal", 1.0, "bf16") for c in range(calls)])
