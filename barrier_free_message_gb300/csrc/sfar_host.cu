@@ -179,6 +179,10 @@ static int geometry(const sfar *h, int p, size_t n, size_t *chunk, size_t *sub, 
         K = 1;
     if (K > (size_t)h->kmax[p][ti])
         K = (size_t)h->kmax[p][ti];
+    // TMA path: one CTA per SM, so that the next call's CTAs, launched early,
+    // find room beside this call's (two fit by shared memory from R = 4)
+    if (p == SFAR_TWOSHOT_TMA && K > (size_t)h->sms / (size_t)h->R)
+        K = (size_t)h->sms / (size_t)h->R;
     if (p == SFAR_TWOSHOT_TMA)
         *sub = align_up(ceil_div(*chunk, K), 16 / (size_t)h->es);
     return (int)K;
@@ -329,15 +333,19 @@ sfar_t *sfar_create(int R, size_t max_bytes, sfar_dtype dt)
     h->r_acc = h->ws + o_acc;
     h->r_agx = h->ws + o_agx;
 
-    // TMA path: a stage holds R tiles (about 48 KB in all); as many stages as
-    // fit in 220 KB of shared memory next to 3 output buffers, 2 to 8
+    // TMA path: a stage holds R tiles (about 48 KB in all, 32 KB at R = 2);
+    // as many stages as keep about 96 KB of input tiles in flight per SM, at
+    // least 2.  Measured against filling 220 KB of shared memory (R = 2 to
+    // 16, 16-256 MB per rank): 2-4 stages of about 48 KB beat 3-5 (R = 8,
+    // 64 MB: 0.915 -> 0.947 of the copy bandwidth; R = 16: 0.897 -> 0.982),
+    // and at R = 2 three stages of 32 KB beat two and five.
     {
         size_t tb = 49152 / (size_t)R;
         if (tb < 2048) tb = 2048;
         if (tb > 16384) tb = 16384;
         tb &= ~(size_t)15;
-        const size_t budget = 220u << 10, outb = 3 * tb;
-        size_t ns = (budget - outb) / ((size_t)R * tb);
+        const size_t in_flight = 96u << 10, outb = 3 * tb;
+        size_t ns = in_flight / ((size_t)R * tb);
         if (ns < 2) ns = 2;
         if (ns > 8) ns = 8;
         h->tma_tb = (int)tb;
