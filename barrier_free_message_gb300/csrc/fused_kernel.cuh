@@ -135,6 +135,8 @@ __global__ void __launch_bounds__(SFAR_NORM_THREADS, UB == 8 && RB <= 8 ? 2 : 1)
     const int r = blockIdx.x / K, k = blockIdx.x - r * K;
     const int g = k / CL, cr = k - g * CL;      // 1-D clusters of CL consecutive CTAs: the rank in the cluster
     const int T = blockDim.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    if (wrong_cluster_shape(a.ctl, CL, r, k))
+        return;
     const unsigned long long h = na.hidden, rows = na.rows;
     const unsigned long long VR = h * ES / (unsigned long long)UB;       // units per row
     const unsigned long long ustride = (unsigned long long)CL * T;

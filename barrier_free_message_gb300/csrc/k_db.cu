@@ -34,11 +34,11 @@ __device__ __forceinline__ bool flag_exchange(const SfarArgs &a, uint32_t *flags
                                         // caller's __syncthreads) before the flags
     if (send)
         for (int i = lane; i < R - 1; i += 32)
-            st_relaxed_u32(flags + ((size_t)peer_of(r, i) * R + r) * SFAR_KMAX + k, e);
+            st_relaxed_u32(flags + sfar_flag((size_t)peer_of(r, i) * R + r, k), e);
     int ok = 1;
     for (int i = lane; i < R - 1 && ok; i += 32) {
         const int q = peer_of(r, i);
-        if (!poll_flag_ge(flags + ((size_t)r * R + q) * SFAR_KMAX + k, e, a.ctl, where == SFAR_WAIT_BOTTOM)) {
+        if (!poll_flag_ge(flags + sfar_flag((size_t)r * R + q, k), e, a.ctl, where == SFAR_WAIT_BOTTOM)) {
             sfar_record_fault(a.ctl, r, k, q, e, where);
             ok = 0;
         }

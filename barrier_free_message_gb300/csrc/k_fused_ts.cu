@@ -109,6 +109,8 @@ __global__ void __launch_bounds__(SFAR_NORM_THREADS, RB <= 8 ? 2 : 1)
     const int r = blockIdx.x / K, k = blockIdx.x - r * K;
     const int g = k / CL, cr = k - g * CL;      // 1-D clusters of CL consecutive CTAs
     const int T = blockDim.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    if (wrong_cluster_shape(a.ctl, CL, r, k))
+        return;
     const unsigned long long h = na.hidden, rows = na.rows;
     const unsigned long long VR = h * ES / 16ull;                 // units per row
     const unsigned long long u = (unsigned long long)cr * T + tid;
@@ -144,11 +146,11 @@ __global__ void __launch_bounds__(SFAR_NORM_THREADS, RB <= 8 ? 2 : 1)
     // arrival: this rank's input and residual are ready and its outputs free
     if (tid < 32) {
         if (tid == 0 && alive && !c.drop)
-            st_release_u32(a.fa + r * SFAR_KMAX + k, e);
+            st_release_u32(a.fa + sfar_pull_flag(r, k), e);
         int wok = alive ? 1 : 0;
         for (int i = lane; i < R - 1 && wok; i += 32) {
             const int q = peer_of(r, i);
-            if (!poll_flag_ge(a.fa + q * SFAR_KMAX + k, e, a.ctl)) {
+            if (!poll_flag_ge(a.fa + sfar_pull_flag(q, k), e, a.ctl)) {
                 sfar_record_fault(a.ctl, r, k, q, e, SFAR_WAIT_ARRIVE);
                 wok = 0;
             }
@@ -326,11 +328,11 @@ __global__ void __launch_bounds__(SFAR_NORM_THREADS, RB <= 8 ? 2 : 1)
         if (ok && !c.drop)
             for (int p = lane; p < R; p += 32)
                 if (p != r)
-                    st_relaxed_u32(a.fb + ((size_t)p * R + r) * SFAR_KMAX + k, e);
+                    st_relaxed_u32(a.fb + sfar_pull_flag((size_t)p * R + r, k), e);
         int wok = ok ? 1 : 0;
         for (int i = lane; i < R - 1 && wok; i += 32) {
             const int q = peer_of(r, i);
-            if (!poll_flag_ge(a.fb + ((size_t)r * R + q) * SFAR_KMAX + k, e, a.ctl, true)) {
+            if (!poll_flag_ge(a.fb + sfar_pull_flag((size_t)r * R + q, k), e, a.ctl, true)) {
                 sfar_record_fault(a.ctl, r, k, q, e, SFAR_WAIT_COMPLETE);
                 wok = 0;
             }

@@ -132,11 +132,11 @@ __global__ void __launch_bounds__(SFAR_TMA_THREADS, 1) k_tma(const __grid_consta
     // arrival: this rank's input is ready and its output free for this call
     if (tid < 32) {
         if (tid == 0 && !c.drop)
-            st_release_u32(arrive + r * SFAR_KMAX + k, e);
+            st_release_u32(arrive + sfar_pull_flag(r, k), e);
         int ok = 1;
         for (int i = lane; i < R - 1 && ok; i += 32) {
             const int q = peer_of(r, i);
-            if (!poll_flag_ge(arrive + q * SFAR_KMAX + k, e, a.ctl)) {
+            if (!poll_flag_ge(arrive + sfar_pull_flag(q, k), e, a.ctl)) {
                 sfar_record_fault(a.ctl, r, k, q, e, SFAR_WAIT_ARRIVE);
                 ok = 0;
             }
@@ -304,11 +304,11 @@ __global__ void __launch_bounds__(SFAR_TMA_THREADS, 1) k_tma(const __grid_consta
         if (ok && !c.drop)
             for (int p = lane; p < R; p += 32)
                 if (p != r)
-                    st_relaxed_u32(cmpl + ((size_t)p * R + r) * SFAR_KMAX + k, e);
+                    st_relaxed_u32(cmpl + sfar_pull_flag((size_t)p * R + r, k), e);
         int wok = ok ? 1 : 0;
         for (int i = lane; i < R - 1 && wok; i += 32) {
             const int q = peer_of(r, i);
-            if (!poll_flag_ge(cmpl + ((size_t)r * R + q) * SFAR_KMAX + k, e, a.ctl, true)) {
+            if (!poll_flag_ge(cmpl + sfar_pull_flag((size_t)r * R + q, k), e, a.ctl, true)) {
                 sfar_record_fault(a.ctl, r, k, q, e, SFAR_WAIT_COMPLETE);
                 wok = 0;
             }

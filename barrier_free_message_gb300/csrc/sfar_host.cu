@@ -292,10 +292,10 @@ sfar_t *sfar_create(int R, size_t max_bytes, sfar_dtype dt)
     h->ctl_bytes = off;
     const size_t o_epoch = carve((size_t)R * sizeof(unsigned long long));
     const size_t o_done = carve((size_t)R * SFAR_KMAX * 4);
-    const size_t o_fa = carve((size_t)R * R * SFAR_KMAX * 4);
-    const size_t o_fb = carve((size_t)R * R * SFAR_KMAX * 4);
-    const size_t o_fc = carve((size_t)R * SFAR_KMAX * 4);
-    const size_t o_fd = carve((size_t)R * R * SFAR_KMAX * 4);
+    const size_t o_fa = carve((size_t)R * R * SFAR_KMAX * SFAR_FLAG_STRIDE * 4);
+    const size_t o_fb = carve((size_t)R * R * SFAR_KMAX * SFAR_FLAG_STRIDE * 4);
+    const size_t o_fc = carve((size_t)R * SFAR_KMAX * SFAR_PULL_FLAG_STRIDE * 4);
+    const size_t o_fd = carve((size_t)R * R * SFAR_KMAX * SFAR_PULL_FLAG_STRIDE * 4);
     const size_t o_raw = carve(RR2 * h->s_raw);
     const size_t o_ll = carve(RR2 * h->s_ll);
     const size_t o_ll128 = carve(RR2 * h->s_ll128);
@@ -649,11 +649,11 @@ static int norm_max_clusters(sfar *h, int allreduce, int test, int batch, int un
     return slot;
 }
 
-// In overlap mode (and plain mode), a fused AllReduce grid whose clusters
-// take more than three quarters of `maxc` (the co-resident clusters that the
+// Except in cooperative mode, a fused AllReduce grid whose clusters take
+// more than three quarters of `maxc` (the co-resident clusters that the
 // occupancy query reports for an idle device) runs solo: launched without
 // programmatic overlap, it starts on an idle device and lets no successor
-// launch before it ends.  Serial and cooperative mode launch the grid as a
+// launch before it ends.  Cooperative mode launches the grid as a
 // cooperative grid instead (see fused_call).  Every CTA of
 // such a grid waits on others, and a large cluster grid launched early, while
 // its predecessor still held the device, did not always get all of its
@@ -918,12 +918,14 @@ static sfar_status fused_call(sfar *h, const void *const in[], const void *const
         ++c;
     na.F = 53 - c;
     a.overlap = 0;
-    // Serial and cooperative mode launch a fused AllReduce grid as a
-    // cooperative grid: the device places it whole, so it keeps its
-    // programmatic launch and never needs to run solo to be sure that all of
-    // its clusters start.  (Measured: no cost at one row, 0.9 us gained at
-    // four rows of 8192, where the grid used to run solo.)
-    const bool coop = allreduce && (h->mode == SFAR_LAUNCH_COOPERATIVE || h->mode == SFAR_LAUNCH_SERIAL);
+    // Cooperative mode launches a fused AllReduce grid as a cooperative grid:
+    // the device places it whole, so it keeps its programmatic launch and
+    // never needs to run solo to be sure that all of its clusters start
+    // (measured: no cost at one row, 0.9 us gained at four rows of 8192).
+    // It is not the default: Nsight Compute's replay of such a launch ran the
+    // grid without its clusters (see wrong_cluster_shape), while the
+    // programmatic launch of a plain cluster grid profiles correctly.
+    const bool coop = allreduce && h->mode == SFAR_LAUNCH_COOPERATIVE;
     const bool solo = allreduce && !coop && solo_grid(R * G, maxc);
     a.solo = solo ? 1 : 0;
     if (path == 2 || solo) {

@@ -15,6 +15,33 @@
 #define SFAR_LL_UNIT_NARROW 8               // LL kernel: input bytes per thread for R <= 8 (16, 8 or 4)
 #define SFAR_LL_UNIT_WIDE 8                 // and for R > 8
 #define SFAR_SENT_UNIT 8                    // sentinel kernel: input bytes per thread (16 or 8)
+#define SFAR_FLAG_STRIDE 1                  // u32 words between the flags of consecutive CTA indices
+// Arrival and completion flags of the pull protocols (TMA AllReduce, two-shot
+// fused normalisation): one 128-byte line per flag.  Packed, the flags of the
+// up to 128 CTAs of a rank shared a few lines that every CTA of every peer
+// polls; spread out, a two-shot fused call of 64 rows of 7168 at R = 8 passed
+// its arrival barrier in 2.6 instead of 5.4 us (24.9 -> 21.3 us per call),
+// and the TMA AllReduce at 1 MB per rank took 10.0 instead of 10.8 us.  The
+// ready flags of DB and BASELINE stay packed (3% faster that way).
+#define SFAR_PULL_FLAG_STRIDE 32
+
+// Index of the flag of CTA index k in row `row` of a flag array laid out
+// [rows][SFAR_KMAX] with SFAR_FLAG_STRIDE (or, for the pull protocols,
+// SFAR_PULL_FLAG_STRIDE) words per flag.
+#ifdef __CUDACC__
+__host__ __device__
+#endif
+inline size_t sfar_flag(size_t row, int k)
+{
+    return (row * SFAR_KMAX + (size_t)k) * SFAR_FLAG_STRIDE;
+}
+#ifdef __CUDACC__
+__host__ __device__
+#endif
+inline size_t sfar_pull_flag(size_t row, int k)
+{
+    return (row * SFAR_KMAX + (size_t)k) * SFAR_PULL_FLAG_STRIDE;
+}
 
 // Device status block of one handle.  The first 32 bytes are the sticky
 // status and the fault record; the knobs follow.

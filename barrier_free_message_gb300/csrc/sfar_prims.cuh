@@ -192,10 +192,11 @@ __device__ __forceinline__ SfarEntry sfar_entry(const SfarArgs &a)
 }
 
 // ------------------------------------------------------------ bounded waits
-__device__ __forceinline__ void sfar_record_fault(SfarCtl *ctl, int rank, int cta, int peer, uint32_t e,
-                                                  int where)
+// Records status `code` (the first failure wins) with where it happened.
+__device__ __forceinline__ void sfar_record_code(SfarCtl *ctl, int code, int rank, int cta, int peer, uint32_t e,
+                                                 int where)
 {
-    if (atomicCAS(&ctl->status, 0, SFAR_ERR_TIMEOUT) == 0) {
+    if (atomicCAS(&ctl->status, 0, code) == 0) {
         volatile SfarCtl *c = ctl;
         c->f_rank = rank;
         c->f_cta = cta;
@@ -203,6 +204,13 @@ __device__ __forceinline__ void sfar_record_fault(SfarCtl *ctl, int rank, int ct
         c->f_epoch = e;
         c->f_where = where;
     }
+}
+
+// A bounded wait gave up: SFAR_ERR_TIMEOUT.
+__device__ __forceinline__ void sfar_record_fault(SfarCtl *ctl, int rank, int cta, int peer, uint32_t e,
+                                                  int where)
+{
+    sfar_record_code(ctl, SFAR_ERR_TIMEOUT, rank, cta, peer, e, where);
 }
 
 // One waiter per poll loop.  tick() is cheap on the fast path (a counter);

@@ -567,6 +567,7 @@ def run_suite(args):
             xd, rd, wd = x.cuda(), res.cuda(), w.cuda()
             od, zd, ad = torch.empty_like(xd), torch.empty_like(xd), torch.empty_like(xd)
             h = sfar.Sfar(R, 2 * n, "bf16")
+            h.set_mode(args.mode)
             P = lambda t, c: [t[c, r].data_ptr() for r in range(R)]
 
             def fused(c):

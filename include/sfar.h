@@ -105,7 +105,8 @@ typedef int sfar_status;
 #define SFAR_WAIT_COPY 11     /* TMA path: bulk copy completion                        */
 #define SFAR_WAIT_COUNTER 12  /* atomic path: a line's arrival counter stayed below R  */
 #define SFAR_WAIT_CLUSTER 13  /* fused normalisation: a cluster peer's row statistics
-                                 (8 times the limit: every peer always sends)           */
+                                 (8 times the limit: every peer always sends); with
+                                 SFAR_ERR_UNSUPPORTED, the grid had no clusters       */
 
 typedef struct {
     sfar_status code; /* SFAR_OK or SFAR_ERR_TIMEOUT                          */
@@ -157,7 +158,10 @@ sfar_status sfar_allreduce(sfar_t *h, const void *const in[], void *const out[],
 
 /*
  * sfar_status_get: reads the handle's device status block through a private
- * stream and returns its code (SFAR_OK or SFAR_ERR_TIMEOUT); fills *info if
+ * stream and returns its code (SFAR_OK; SFAR_ERR_TIMEOUT; or
+ * SFAR_ERR_UNSUPPORTED with where = SFAR_WAIT_CLUSTER when a fused kernel
+ * found itself launched without the thread-block clusters it was planned
+ * for, e.g. by a tool replaying the launch, and ran nothing); fills *info if
  * info is not NULL.  It does not wait for the caller's streams: synchronise
  * them first to see the outcome of the work enqueued so far.  A non-OK code
  * poisons the handle on the host too, until sfar_reset.

@@ -58,17 +58,21 @@ sfar_status sfar_test_force_single_buffer(sfar_t *h, int on, sfar_stream_t s);
  * rank, not across ranks).  Calls may then overtake one another across
  * ranks, which is what double buffering has to survive.  Use OVERLAP only
  * for chains of calls whose inputs do not depend on the previous call's
- * outputs.  In serial mode a fused AllReduce + RMSNorm call
- * (sfar_allreduce_add_rmsnorm) is launched as a cooperative grid, which the
- * device places whole.  In overlap and plain mode a fused call whose grid
- * takes more than three quarters of the device's co-resident clusters runs
- * solo: without programmatic launch, letting no successor launch before it
- * ends.  Every two-shot fused call runs with serial semantics.
- * SFAR_LAUNCH_COOPERATIVE: as SFAR_LAUNCH_SERIAL, and sfar_allreduce's
- * kernels are cooperative grids too, so the device places every AllReduce
- * grid whole (or the call returns SFAR_ERR_UNSUPPORTED when the grid could
- * never be resident) instead of a partly placed grid's waits timing out, at
- * a cost of 0.05-0.17 us per call for the one-shot LL kernel.
+ * outputs.  In every mode but the cooperative one, a fused AllReduce +
+ * RMSNorm call whose grid takes more than three quarters of the device's
+ * co-resident clusters runs solo: without programmatic launch, letting no
+ * successor launch before it ends.  Every two-shot fused call runs with
+ * serial semantics.
+ * SFAR_LAUNCH_COOPERATIVE: as SFAR_LAUNCH_SERIAL, and every AllReduce
+ * kernel (sfar_allreduce, sfar_allreduce_add_rmsnorm) is launched as a
+ * cooperative grid, so the device places it whole (or the call returns
+ * SFAR_ERR_UNSUPPORTED when the grid could never be resident) instead of a
+ * partly placed grid's waits timing out, and no fused grid runs solo.  It
+ * costs the one-shot LL kernel 0.05-0.17 us per call and gains the fused
+ * call of four rows of 8192 0.9 us.  Do not profile this mode with Nsight
+ * Compute: its replay of a cooperative cluster grid ran the grid without its
+ * clusters (the fused kernels then record SFAR_ERR_UNSUPPORTED and run
+ * nothing).
  */
 #define SFAR_LAUNCH_SERIAL 0
 #define SFAR_LAUNCH_OVERLAP 1

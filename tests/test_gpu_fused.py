@@ -509,10 +509,10 @@ def test_large_grid_chain_does_not_stall(mode):
     """A one-shot grid that fills most of the device (R = 8, eight rows of
     8192 bf16: 32 clusters of 8 CTAs) chained in a graph: launched as a plain
     programmatic dependent it sometimes had a cluster that never started (its
-    peers timed out).  In serial and cooperative mode the grid is now a
-    cooperative grid, which the device places whole, and keeps the
-    programmatic launch.  Twenty replays of 32 calls with a 50 ms wait limit,
-    then the last call against the oracle."""
+    peers timed out).  In serial mode such a grid runs solo; in cooperative
+    mode it is a cooperative grid, which the device places whole, and keeps
+    the programmatic launch.  Twenty replays of 32 calls with a 50 ms wait
+    limit, then the last call against the oracle."""
     R, rows, hidden, calls, eps = 8, 8, 8192, 32, 1e-5
     n = rows * hidden
     x = torch.stack([inputs.draw(1500, c, R, n, "normal", 1.0, "bf16") for c in range(calls)])
