@@ -101,6 +101,37 @@ def test_fused_parity(R, dtype, path):
         h.close()
 
 
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp32"])
+@pytest.mark.parametrize("R", [3, 8, 16])
+def test_cooperative_mode_parity(R, dtype):
+    """The cooperative launch mode (every AllReduce kernel a cooperative grid,
+    the fused grids cooperative cluster grids that never run solo): the same
+    bits as the oracle for both fused kernels and the plain AllReduce."""
+    h = sfar.Sfar(R, 1 << 20, dtype)
+    es = 2 if dtype == "bf16" else 4
+    try:
+        h.set_mode("cooperative")
+        for path in ("oneshot", "twoshot", "auto"):
+            assert sfar.sfar_test_set_fused_path(h.h, path) == sfar.SFAR_OK
+            for rows, hidden in ((1, 8192), (4, 8192), (3, 7168), (2, 1000), (16, 4096 // es * 2)):
+                if rows * hidden * es > (1 << 20):
+                    continue
+                x, res, w = draw_case(2000 + R + rows, R, rows, hidden, dtype)
+                check(h, x, res, w, hidden, 1e-5, f"cooperative {path} R={R} {rows}x{hidden} {dtype}")
+        x = inputs.draw(2100 + R, 0, R, 8192 + 5, "normal", 1.0, dtype)
+        ins = [x[r].contiguous().cuda() for r in range(R)]
+        for proto in ("ll", "sentinel", "twoshot_sent", "twoshot_tma"):
+            outs = [torch.empty_like(t) for t in ins]
+            h.allreduce(ins, outs, proto)
+            torch.cuda.synchronize()
+            status_ok(h.h, f"cooperative {proto}")
+            want = oracle.allreduce(inputs.to_bits(x))
+            for r in range(R):
+                assert_equal_nan_aware(outs[r], want[r], f"cooperative {proto} R={R} rank {r}")
+    finally:
+        h.close()
+
 @pytest.mark.parametrize("dtype", ["bf16", "fp32"])
 @pytest.mark.parametrize("R", [8, 16])
 def test_norm_alone_parity(R, dtype):
