@@ -391,46 +391,48 @@ int sfar_oracle_add_rmsnorm(int R, size_t rows, size_t h, int dtype, const void 
  * the AllReduce after it.  Rank r holds the rows of the weight matrix that
  * match its slice of the input: y_r = x_r W_r, x_r of k elements, W_r of
  * k x h (row-major), y_r of h elements -- the partial sums the AllReduce
- * adds.  The pages fix no summation order.  Reading taken (bf16 inputs and
- * output): every product x[i] * W[i][j] is rounded to binary32 (exact
- * unless it under- or overflows: the significands have 8 bits); the k rows
- * are cut into S = 8 segments of c = ceil(k / 8)
- * consecutive rows (the last ones shorter or empty); within a segment the
- * products are added to a binary32 accumulator that starts at +0, in row
- * order; the S segment sums are folded left to right (segment 0 first);
- * one rounding to bf16.
+ * adds.  The pages fix no summation order; the reading taken is the plain
+ * definition of a matrix-vector product written as one sum per output
+ * (bf16 inputs and output): y[j] = x[0] W[0][j] + x[1] W[1][j] + ... +
+ * x[k-1] W[k-1][j], evaluated from the left -- every product rounded to
+ * binary32 (exact unless it under- or overflows: the significands have 8
+ * bits), added in row order (row 0 first) to a binary32 accumulator that
+ * starts at +0, each addition rounded to nearest even -- then one rounding
+ * to bf16.
  * ------------------------------------------------------------------------ */
-#define ORACLE_GEMV_SEGMENTS 8
-
 static float gemv_column(const uint16_t *x, const uint16_t *W, size_t k, size_t h, size_t j)
 {
-    const size_t c = (k + ORACLE_GEMV_SEGMENTS - 1) / ORACLE_GEMV_SEGMENTS;
-    float P[ORACLE_GEMV_SEGMENTS];
-    for (int sg = 0; sg < ORACLE_GEMV_SEGMENTS; ++sg) {
-        float acc = 0.0f;
-        for (size_t i = (size_t)sg * c; i < (size_t)(sg + 1) * c && i < k; ++i) {
-#if ORACLE_MUTANT == 20
-            const float p = widen_bf16(x[i]) * widen_bf16(W[j * k + i]);     /* mutant: W transposed */
+#if ORACLE_MUTANT == 21
+    /* mutant: 8 segments of ceil(k / 8) consecutive rows, each summed from +0,
+       the segment sums then folded in segment order */
+    const size_t c = (k + 7) / 8;
+    float total = 0.0f;
+    for (size_t s0 = 0; s0 < k; s0 += c) {
+        float part = 0.0f;
+        for (size_t i = s0; i < s0 + c && i < k; ++i)
+            part = part + widen_bf16(x[i]) * widen_bf16(W[i * h + j]);
+        total = s0 == 0 ? part : total + part;
+    }
+    return total;
+#endif
+    float acc = 0.0f;
+    for (size_t n = 0; n < k; ++n) {
+#if ORACLE_MUTANT == 18
+        const size_t i = k - 1 - n;                                           /* mutant: rows folded from the last */
 #else
-            const float p = widen_bf16(x[i]) * widen_bf16(W[i * h + j]);
+        const size_t i = n;
+#endif
+#if ORACLE_MUTANT == 20
+        const float p = widen_bf16(x[i]) * widen_bf16(W[j * k + i]);         /* mutant: W transposed */
+#else
+        const float p = widen_bf16(x[i]) * widen_bf16(W[i * h + j]);
 #endif
 #if ORACLE_MUTANT == 19
-            if (i + 1 == k) continue;                                        /* mutant: last row dropped */
+        if (i + 1 == k) continue;                                            /* mutant: last row dropped */
 #endif
-            acc = acc + p;
-        }
-        P[sg] = acc;
+        acc = acc + p;
     }
-#if ORACLE_MUTANT == 18
-    float y = P[ORACLE_GEMV_SEGMENTS - 1];                                   /* mutant: reversed fold */
-    for (int sg = ORACLE_GEMV_SEGMENTS - 2; sg >= 0; --sg)
-        y = y + P[sg];
-#else
-    float y = P[0];
-    for (int sg = 1; sg < ORACLE_GEMV_SEGMENTS; ++sg)
-        y = y + P[sg];
-#endif
-    return y;
+    return acc;
 }
 
 /*

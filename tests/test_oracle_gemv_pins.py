@@ -18,7 +18,8 @@ def test_rejects_bad_arguments():
         oracle.gemv(np.zeros((2, 4), np.uint16), np.zeros((2, 5, 8), np.uint16))
 
 
-MUTANTS = {18: "segment sums folded from the last", 19: "last row dropped", 20: "weights read transposed"}
+MUTANTS = {18: "rows folded from the last", 19: "last row dropped", 20: "weights read transposed",
+           21: "rows summed in 8 segments, then the segment sums"}
 
 
 @pytest.mark.parametrize("mutant", sorted(MUTANTS))
