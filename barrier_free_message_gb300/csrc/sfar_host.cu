@@ -10,6 +10,8 @@
 // arguments on the host and enqueues exactly one kernel; nothing is
 // allocated or synchronised per call, so calls can be captured in a CUDA
 // graph and replayed with no host involvement (the epochs live on the device).
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 #include <stdlib.h>
 #include <string.h>
@@ -377,6 +379,10 @@ sfar_t *sfar_create(int R, size_t max_bytes, sfar_dtype dt)
         if (cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)h->tma_smem) != cudaSuccess)
             st = SFAR_ERR_UNSUPPORTED;
     }
+    if (st == SFAR_OK &&
+        cudaFuncSetAttribute(sfar_kernel_gemv(), cudaFuncAttributeMaxDynamicSharedMemorySize, SFAR_GEMV_SMEM) !=
+            cudaSuccess)
+        st = SFAR_ERR_UNSUPPORTED;
     // co-residency: every CTA of a call must be resident at once (ranks wait
     // on each other), so K is capped by the occupancy of each variant
     for (int p = 0; p < SFAR_NUM_PROTOS && st == SFAR_OK; ++p) {
@@ -1026,11 +1032,28 @@ sfar_status sfar_add_rmsnorm(sfar_t *h, const void *const a[], const void *const
 }
 
 // ------------------------------------------------ row-parallel projection
+// The driver's tensor-map encoder, looked up once (no link against the driver library).
+static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder()
+{
+    static const PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess) {
+            cudaGetLastError();
+            p = nullptr;
+        }
+        return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }();
+    return fn;
+}
+
 sfar_status sfar_rowpar_gemv(sfar_t *h, const void *const x[], const void *const w[], void *const y[], size_t k,
                              size_t hidden, size_t prefetch_rows, sfar_stream_t s)
 {
-    if (!h || !x || !w || !y || h->dt != SFAR_BF16 || k == 0 || hidden == 0 || hidden % 8 ||
-        k > ((size_t)-1) / 2 / hidden)
+    if (!h || !x || !w || !y || h->dt != SFAR_BF16 || k == 0 || hidden == 0 || hidden % 8 || k >= (1ull << 31) ||
+        hidden >= (1ull << 31))
         return SFAR_ERR_INVALID;
     const int R = h->R;
     const size_t wbytes = k * hidden * 2, ybytes = hidden * 2, xbytes = k * 2;
@@ -1050,22 +1073,34 @@ sfar_status sfar_rowpar_gemv(sfar_t *h, const void *const x[], const void *const
                     return SFAR_ERR_INVALID;
             }
         }
+    const PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
+    if (!encode)
+        return SFAR_ERR_UNSUPPORTED;
     SfarGemvArgs g;
     memset(&g, 0, sizeof g);
+    const cuuint64_t dims[2] = {(cuuint64_t)hidden, (cuuint64_t)k};
+    const cuuint64_t strides[1] = {(cuuint64_t)hidden * 2};
+    const cuuint32_t box[2] = {SFAR_GEMV_COLS, SFAR_GEMV_ROWS}, unit[2] = {1, 1};
     for (int r = 0; r < R; ++r) {
         g.x[r] = x[r];
-        g.w[r] = w[r];
         g.y[r] = y[r];
+        if (encode(&g.wmap[r], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(w[r]), dims, strides, box, unit,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return SFAR_ERR_INVALID;
     }
+    g.ctl = h->ctl;
     g.k = k;
     g.h = hidden;
-    g.seg = ceil_div(k, SFAR_GEMV_SEGMENTS);
-    g.prefetch = prefetch_rows < g.seg ? prefetch_rows : g.seg;
+    // whole stages of the copy ring, at most the STAGES - 1 that its prologue issues
+    const size_t pre = ceil_div(prefetch_rows, SFAR_GEMV_ROWS);
+    g.pre = (int)(pre < SFAR_GEMV_STAGES - 1 ? pre : SFAR_GEMV_STAGES - 1);
     g.tiles = (int)ceil_div(hidden, SFAR_GEMV_COLS);
 
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3((unsigned)(R * g.tiles));
-    cfg.blockDim = dim3(SFAR_GEMV_SEGMENTS * 32);
+    cfg.blockDim = dim3(SFAR_GEMV_THREADS);
+    cfg.dynamicSmemBytes = SFAR_GEMV_SMEM;
     cfg.stream = (cudaStream_t)s;
     cudaLaunchAttribute attr[1];
     if (h->mode != SFAR_LAUNCH_PLAIN) {

@@ -640,7 +640,7 @@ def run_suite(args):
         wbytes = layers * R * sum(ks) * h * 2
         # (projection launch, AllReduce launch, prefetch rows): "serial" = as a
         # programmatic dependent of the kernel before it
-        configs = (("plain", "plain", 0), ("serial", "serial", 0), ("serial", "serial", 32), ("serial", "plain", 32))
+        configs = (("plain", "plain", 0), ("serial", "serial", 0), ("serial", "serial", 128), ("serial", "plain", 128))
         for ar in ("fused", "ll"):
             for gmode, amode, prefetch in configs:
                 hd.set_mode(amode)

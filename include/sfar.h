@@ -102,7 +102,7 @@ typedef int sfar_status;
 #define SFAR_WAIT_AG 8        /* two-shot all-gather line flag                         */
 #define SFAR_WAIT_ARRIVE 9    /* TMA / two-shot fused: peer arrival (top barrier)      */
 #define SFAR_WAIT_COMPLETE 10 /* TMA / two-shot fused: owner completion flags          */
-#define SFAR_WAIT_COPY 11     /* TMA path: bulk copy completion                        */
+#define SFAR_WAIT_COPY 11     /* TMA path or projection: bulk copy completion          */
 #define SFAR_WAIT_COUNTER 12  /* atomic path: a line's arrival counter stayed below R  */
 #define SFAR_WAIT_CLUSTER 13  /* fused normalisation: a cluster peer's row statistics
                                  (8 times the limit: every peer always sends); with

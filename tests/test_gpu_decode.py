@@ -40,7 +40,7 @@ def test_gemv_parity(R, mode):
     hd = sfar.Sfar(R, 1 << 16, "bf16")
     try:
         hd.set_mode(mode)
-        for k, h in ((1, 8), (7, 264), (24, 40), (1024, 8192), (3584, 1024), (1000, 2056)):
+        for k, h in ((1, 8), (7, 264), (24, 40), (33, 8), (257, 512), (1024, 8192), (3584, 1024), (1000, 2056)):
             x, W = draw_gemv(70 + k, R, k, h)
             want = oracle.gemv(inputs.to_bits(x), inputs.to_bits(W))
             for prefetch in (0, 16, 10 ** 6):

@@ -109,8 +109,8 @@ def test_projection_against_float64_product(R, k, hidden):
     y = np.stack([f32(t) for t in ys]).astype(np.float64)
     bad = np.abs(y - y64) > 2 * (k + 1) * 2.0 ** -24 * mag + 2.0 ** -8 * np.abs(y64)
     assert not bad.any(), f"R={R} k={k} h={hidden}: {int(bad.sum())} outputs off the float64 product"
-    # and not trivially: a projection that dropped one segment's worth of rows
-    # (the last eighth) would fail the bound in most outputs
+    # and not trivially: a projection that dropped the last eighth of the
+    # rows would fail the bound in most outputs
     c = -(-k // 8)
     y_drop = y64 - np.einsum("rk,rkh->rh", xf[:, k - c:], Wf[:, k - c:, :])
     miss = np.abs(y_drop - y64) > 2 * (k + 1) * 2.0 ** -24 * mag + 2.0 ** -8 * np.abs(y64)
