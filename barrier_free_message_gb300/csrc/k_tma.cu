@@ -20,6 +20,11 @@
 //   * the store warp: lane p issues the bulk copy shared -> global into rank
 //     p's output, and frees a buffer once the copies reading it are done.
 // No CTA-wide barrier in the steady state; every mbarrier wait is bounded.
+// A CTA in which a wait gave up lets every copy it issued land before it
+// leaves, so no copy writes into shared memory the CTA no longer owns.
+// (Copying the owner's own rank's first tiles before the arrival barrier, to
+// overlap the pipeline fill with the flag round trip, made the barrier
+// itself 1.5-2.3 us slower on GB300: the burst of reads delayed the flags.)
 // No multicast and no bulk reduction (its order of additions is not fixed).
 // Streaming copies carry an L2 evict-first hint: every byte is touched once.
 //
@@ -94,6 +99,20 @@ __device__ __forceinline__ void fence_proxy_async_global()
 __device__ __forceinline__ void mbar_arrive(uint32_t bar)
 {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+// Wait for phase `parity`, bounded by time only (not by the status word: it
+// is used after a failure, to let copies already issued land).
+__device__ __forceinline__ bool mbar_wait_for(uint32_t bar, uint32_t parity, unsigned long long limit_ns)
+{
+    if (mbar_try_wait(bar, parity))
+        return true;
+    const unsigned long long t0 = globaltimer();
+    for (uint32_t it = 1;; ++it) {
+        if (mbar_try_wait(bar, parity))
+            return true;
+        if ((it & 127u) == 0 && globaltimer() - t0 > limit_ns)
+            return false;
+    }
 }
 // Bounded wait for phase `parity` of an mbarrier; false if it gave up.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const SfarCtl *ctl)
@@ -193,9 +212,11 @@ __global__ void __launch_bounds__(SFAR_TMA_THREADS, 1) k_tma(const __grid_consta
             const unsigned long long off = t * TB;
             return (uint32_t)((len16 - off) < TB ? (len16 - off) : TB);
         };
+        unsigned long long issued = 0;  // producer: tiles whose copies went out
         if (warp == TMA_PRODUCER_WARP) {
             const uint64_t pol = policy_evict_first();
-            for (unsigned long long t = 0; t < ntiles; ++t) {
+            unsigned long long t = 0;
+            for (; t < ntiles; ++t) {
                 const int s = (int)(t % NS);
                 int wok = 1;
                 if (t >= (unsigned long long)NS)
@@ -215,6 +236,7 @@ __global__ void __launch_bounds__(SFAR_TMA_THREADS, 1) k_tma(const __grid_consta
                     bulk_g2s(smem_u32(stage0 + ((size_t)s * R + q) * TB), (const uint8_t *)a.in[q] + b0 + t * TB, tb,
                              bar, pol);
             }
+            issued = t;
         } else if (warp == TMA_STORE_WARP) {
             const uint64_t pol = policy_evict_first();
             for (unsigned long long t = 0; t < ntiles; ++t) {
@@ -273,6 +295,16 @@ __global__ void __launch_bounds__(SFAR_TMA_THREADS, 1) k_tma(const __grid_consta
         }
         __syncthreads();
         ok = ok && s_fail == 0;
+        if (!ok && warp == TMA_PRODUCER_WARP && lane == 0) {
+            // a wait gave up somewhere in the CTA: let the copies already
+            // issued land before the shared memory is released (the last tile
+            // issued into a slot completes after every earlier one there)
+            const unsigned long long limit_ns = ld_relaxed_u64(&a.ctl->timeout_ns);
+            for (int s = 0; s < NS && (unsigned long long)s < issued; ++s) {
+                const unsigned long long last = issued - 1 - ((issued - 1 - s) % NS);
+                mbar_wait_for(smem_u32(full + s), (uint32_t)((last / NS) & 1ull), limit_ns);
+            }
+        }
     }
     // a ragged end shorter than 16 bytes: element by element
     if (ok && tid == 0 && b1 == nbytes && (b1 - b0) > len16) {
