@@ -175,6 +175,34 @@ def test_special_rows_and_ranges():
         h.close()
 
 
+@pytest.mark.parametrize("path", ["oneshot", "twoshot"])
+@pytest.mark.parametrize("dtype", ["bf16", "fp32"])
+def test_rows_with_outliers(path, dtype):
+    """Rows whose largest magnitude sits in one place, 2^k above the rest
+    (k = 0 .. 12, also on one rank only): the kernels take the row's scale
+    from the whole row whatever the spread between the parts of it that
+    different warps hold, including spreads of 3 and 4 binades and beyond."""
+    R = 8
+    h = sfar.Sfar(R, 1 << 20, dtype)
+    try:
+        assert sfar.sfar_test_set_fused_path(h.h, path) == sfar.SFAR_OK
+        for rows, hidden in ((1, 8192), (4, 8192), (6, 2048), (3, 7168), (5, 64)):
+            code, got = sfar.sfar_test_query_fused_path(h.h, rows, hidden)
+            if code != sfar.SFAR_OK or got != (1 if path == "oneshot" else 2):
+                continue
+            x, res, w = draw_case(1200 + rows, R, rows, hidden, dtype)
+            for i in range(rows):
+                k = (0, 3, 4, 5, 12, 2)[i % 6]
+                j = i * hidden + (97 * i + 13) % hidden
+                x[:, j] *= 2.0 ** k
+                res[:, j] *= 2.0 ** k
+                if i % 2:
+                    x[i % R, (j + hidden // 2) % (rows * hidden)] *= 2.0 ** (k + 1)
+            check(h, x, res, w, hidden, 1e-5, f"{path} outliers {rows}x{hidden} {dtype}")
+    finally:
+        h.close()
+
+
 @pytest.mark.parametrize("mode", ["serial", "overlap", "cooperative"])
 def test_fused_chain_1024_calls(mode):
     """The decode shape (R = 8, one row of 8192 bf16) for 1,024 graph-chained
