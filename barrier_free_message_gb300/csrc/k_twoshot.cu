@@ -65,15 +65,15 @@ __global__ void __launch_bounds__(SFAR_THREADS) k_twoshot(const __grid_constant_
                 }
             }
         }
+        // the warp barrier orders every lane's payload stores before the flag
+        // lanes' release stores (one flag per lane and peer)
         __syncwarp();
-        fence_acq_rel_gpu();
-        for (int i = 0; i < R - 1; ++i) {
-            const int j = peer_of(r, i);
-            uint8_t *dst = rs + ((size_t)(j * 2 + c.par) * R + r) * slot;
-            for (unsigned long long it = it0; it < nitc; it += its)
-                if (m == 0)
-                    st_relaxed_u32((uint32_t *)(dst + (it * 4ull + g) * 128ull), e);
-        }
+        for (unsigned long long it = it0; it < nitc; it += its)
+            for (int i = m; i < R - 1; i += 8) {
+                const int j = peer_of(r, i);
+                st_release_u32((uint32_t *)(rs + ((size_t)(j * 2 + c.par) * R + r) * slot + (it * 4ull + g) * 128ull),
+                               e);
+            }
     }
 
     sfar_stamp(c, TP_SENT);
@@ -89,7 +89,7 @@ __global__ void __launch_bounds__(SFAR_THREADS) k_twoshot(const __grid_constant_
             const int q = peer_of(r, i);
             const uint32_t *f = (const uint32_t *)(rs_mine + (size_t)q * slot + loff);
             SfarWaiter w;
-            while (ld_relaxed_u32(f) != e) {
+            while (ld_acquire_u32(f) != e) {
                 if (w.tick(a.ctl)) {
                     sfar_record_fault(a.ctl, r, k, q, e, SFAR_WAIT_RS);
                     lok = 0;
@@ -100,7 +100,7 @@ __global__ void __launch_bounds__(SFAR_THREADS) k_twoshot(const __grid_constant_
         ok = __all_sync(SFAR_FULL, lok) != 0;
         if (!ok)
             break;
-        fence_acq_rel_gpu();
+        __syncwarp();                   // each lane's acquisition, passed on to the warp
         const unsigned long long vb = r * cvec + it * 31ull + lane;
         const uint4 x = lane < 31 ? load_vec<ES>(a.in[r], vb, nbytes) : zero;
         const uint4 own = ll128_pack(x, lane);
@@ -130,11 +130,10 @@ __global__ void __launch_bounds__(SFAR_THREADS) k_twoshot(const __grid_constant_
     }
     if (ok && !c.drop) {
         __syncwarp();
-        fence_acq_rel_gpu();
         for (unsigned long long it = it0; it < nitc; it += its)
             for (int i = m; i < R - 1; i += 8) {
                 const int p = peer_of(r, i);
-                st_relaxed_u32((uint32_t *)(ag + ((size_t)(p * 2 + c.par) * R + r) * slot + (it * 4ull + g) * 128ull),
+                st_release_u32((uint32_t *)(ag + ((size_t)(p * 2 + c.par) * R + r) * slot + (it * 4ull + g) * 128ull),
                                e);
             }
     }
@@ -150,7 +149,7 @@ __global__ void __launch_bounds__(SFAR_THREADS) k_twoshot(const __grid_constant_
             const int j = peer_of(r, i);
             const uint32_t *f = (const uint32_t *)(ag_mine + (size_t)j * slot + loff);
             SfarWaiter w(true);
-            while (ld_relaxed_u32(f) != e) {
+            while (ld_acquire_u32(f) != e) {
                 if (w.tick(a.ctl)) {
                     sfar_record_fault(a.ctl, r, k, j, e, SFAR_WAIT_AG);
                     lok = 0;
@@ -161,7 +160,7 @@ __global__ void __launch_bounds__(SFAR_THREADS) k_twoshot(const __grid_constant_
         ok = __all_sync(SFAR_FULL, lok) != 0;
         if (!ok)
             break;
-        fence_acq_rel_gpu();
+        __syncwarp();
         uint4 y[RB];
 #pragma unroll
         for (int q = 0; q < RB; ++q)
