@@ -114,6 +114,17 @@ __device__ __forceinline__ bool mbar_wait_for(uint32_t bar, uint32_t parity, uns
             return false;
     }
 }
+// Poll a flag of another rank until it reaches epoch e, with acquire loads
+// (the CTA barrier after the exchange passes the acquisition on); false if
+// the bounded wait gave up.
+__device__ __forceinline__ bool poll_acquire_ge(const uint32_t *f, uint32_t e, const SfarCtl *ctl, bool downstream)
+{
+    SfarWaiter w(downstream);
+    while (!epoch_ge(ld_acquire_u32(f), e))
+        if (w.tick(ctl))
+            return false;
+    return true;
+}
 // Bounded wait for phase `parity` of an mbarrier; false if it gave up.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const SfarCtl *ctl)
 {
@@ -155,13 +166,12 @@ __global__ void __launch_bounds__(SFAR_TMA_THREADS, 1) k_tma(const __grid_consta
         int ok = 1;
         for (int i = lane; i < R - 1 && ok; i += 32) {
             const int q = peer_of(r, i);
-            if (!poll_flag_ge(arrive + sfar_pull_flag(q, k), e, a.ctl)) {
+            if (!poll_acquire_ge(arrive + sfar_pull_flag(q, k), e, a.ctl, false)) {
                 sfar_record_fault(a.ctl, r, k, q, e, SFAR_WAIT_ARRIVE);
                 ok = 0;
             }
         }
         ok = __all_sync(SFAR_FULL, ok);
-        fence_acq_rel_gpu();
         if (tid == 0)
             s_ok = ok;
     }
@@ -331,22 +341,23 @@ __global__ void __launch_bounds__(SFAR_TMA_THREADS, 1) k_tma(const __grid_consta
     __syncthreads();
     sfar_stamp(c, TP_INPUT);        // this path: the CTA's tiles are folded and stored
     // completion: tell every rank this owner's part of its output is written
+    // (release stores after the CTA barrier that follows the store warp's
+    // bulk-store wait and proxy fence; acquire polls, passed on to the CTA by
+    // the epilogue's barrier)
     if (tid < 32) {
-        fence_acq_rel_gpu();
         if (ok && !c.drop)
             for (int p = lane; p < R; p += 32)
                 if (p != r)
-                    st_relaxed_u32(cmpl + sfar_pull_flag((size_t)p * R + r, k), e);
+                    st_release_u32(cmpl + sfar_pull_flag((size_t)p * R + r, k), e);
         int wok = ok ? 1 : 0;
         for (int i = lane; i < R - 1 && wok; i += 32) {
             const int q = peer_of(r, i);
-            if (!poll_flag_ge(cmpl + sfar_pull_flag((size_t)r * R + q, k), e, a.ctl, true)) {
+            if (!poll_acquire_ge(cmpl + sfar_pull_flag((size_t)r * R + q, k), e, a.ctl, true)) {
                 sfar_record_fault(a.ctl, r, k, q, e, SFAR_WAIT_COMPLETE);
                 wok = 0;
             }
         }
         __syncwarp();
-        fence_acq_rel_gpu();
     }
     sfar_stamp(c, TP_RECEIVED);
     sfar_epilogue(a, r, k, e);
