@@ -99,6 +99,17 @@ __device__ __forceinline__ unsigned long long warp_sums_transposed(unsigned long
     return v[0];
 }
 
+// Poll a flag of another rank until it reaches epoch e, with acquire loads;
+// false if the bounded wait gave up.
+__device__ __forceinline__ bool poll_acquire_ge(const uint32_t *f, uint32_t e, const SfarCtl *ctl, bool downstream)
+{
+    SfarWaiter w(downstream);
+    while (!epoch_ge(ld_acquire_u32(f), e))
+        if (w.tick(ctl))
+            return false;
+    return true;
+}
+
 template <int DT, int RB, bool TEST>
 __global__ void __launch_bounds__(SFAR_NORM_THREADS, RB <= 8 ? 2 : 1)
     k_fused_ts(const __grid_constant__ SfarArgs a, const __grid_constant__ SfarNormArgs na)
@@ -150,13 +161,12 @@ __global__ void __launch_bounds__(SFAR_NORM_THREADS, RB <= 8 ? 2 : 1)
         int wok = alive ? 1 : 0;
         for (int i = lane; i < R - 1 && wok; i += 32) {
             const int q = peer_of(r, i);
-            if (!poll_flag_ge(a.fa + sfar_pull_flag(q, k), e, a.ctl)) {
+            if (!poll_acquire_ge(a.fa + sfar_pull_flag(q, k), e, a.ctl, false)) {
                 sfar_record_fault(a.ctl, r, k, q, e, SFAR_WAIT_ARRIVE);
                 wok = 0;
             }
         }
-        wok = __all_sync(SFAR_FULL, wok);
-        fence_acq_rel_gpu();
+        wok = __all_sync(SFAR_FULL, wok);     // the CTA barrier below passes the acquisitions on
         if (tid == 0)
             s_ok = wok;
     }
@@ -321,24 +331,24 @@ __global__ void __launch_bounds__(SFAR_NORM_THREADS, RB <= 8 ? 2 : 1)
     if (!cluster_ready)
         cluster_wait();
 
-    // completion: every rank learns that this owner's part of its rows is written
+    // completion: every rank learns that this owner's part of its rows is
+    // written (release stores after the CTA barrier that orders the CTA's
+    // output stores; acquire polls, passed on by the epilogue's barrier)
     __syncthreads();
     if (tid < 32) {
-        fence_acq_rel_gpu();
         if (ok && !c.drop)
             for (int p = lane; p < R; p += 32)
                 if (p != r)
-                    st_relaxed_u32(a.fb + sfar_pull_flag((size_t)p * R + r, k), e);
+                    st_release_u32(a.fb + sfar_pull_flag((size_t)p * R + r, k), e);
         int wok = ok ? 1 : 0;
         for (int i = lane; i < R - 1 && wok; i += 32) {
             const int q = peer_of(r, i);
-            if (!poll_flag_ge(a.fb + sfar_pull_flag((size_t)r * R + q, k), e, a.ctl, true)) {
+            if (!poll_acquire_ge(a.fb + sfar_pull_flag((size_t)r * R + q, k), e, a.ctl, true)) {
                 sfar_record_fault(a.ctl, r, k, q, e, SFAR_WAIT_COMPLETE);
                 wok = 0;
             }
         }
         __syncwarp();
-        fence_acq_rel_gpu();
     }
     if (alive) {
         sfar_epilogue(a, r, k, e);
