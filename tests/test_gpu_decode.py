@@ -51,6 +51,33 @@ def test_gemv_parity(R, mode):
         hd.close()
 
 
+def test_gemv_sixteen_ranks_and_unaligned_input():
+    """R = 16 (a weight tensor map per rank in the kernel's parameters), and
+    inputs x that start 2 bytes past an aligned address (the API asks for
+    2-byte alignment of x only)."""
+    for R, k, h, shift in ((16, 300, 520, 0), (16, 64, 256, 1), (3, 129, 1032, 1)):
+        x, W = draw_gemv(90 + R + k, R, k, h)
+        want = oracle.gemv(inputs.to_bits(x), inputs.to_bits(W))
+        hd = sfar.Sfar(R, 1 << 16, "bf16")
+        try:
+            xb = [torch.zeros(k + 8, dtype=torch.bfloat16, device="cuda") for _ in range(R)]
+            xs = [b[shift:shift + k] for b in xb]
+            for r in range(R):
+                xs[r].copy_(x[r].cuda())
+            ws = [W[r].contiguous().cuda() for r in range(R)]
+            ys = [torch.empty(h, dtype=torch.bfloat16, device="cuda") for _ in range(R)]
+            for y in ys:
+                y.view(torch.int16).fill_(-1)
+            assert all((t.data_ptr() & 15) == (2 * shift) for t in xs)
+            hd.rowpar_gemv(xs, ws, ys, 64)
+            torch.cuda.synchronize()
+            got = inputs.to_bits(torch.stack([y.cpu() for y in ys]))
+            assert np.array_equal(got, want), f"R={R} k={k} h={h} x shifted by {shift}"
+            status_ok(hd.h)
+        finally:
+            hd.close()
+
+
 def test_gemv_products_that_underflow_or_overflow():
     R, k, h = 2, 64, 64
     g = torch.Generator().manual_seed(71)
