@@ -638,33 +638,50 @@ def run_suite(args):
         hg = sfar.Sfar(R, 2 * h, "bf16")          # the projections (own launch mode)
         P = lambda ts: [t.data_ptr() for t in ts]
         wbytes = layers * R * sum(ks) * h * 2
-        # (projection launch, AllReduce launch, prefetch rows): "serial" = as a
-        # programmatic dependent of the kernel before it
-        configs = (("plain", "plain", 0), ("serial", "serial", 0), ("serial", "serial", 128), ("serial", "plain", 128))
+        # (projection launch, AllReduce launch, prefetch rows, streams): "serial" =
+        # as a programmatic dependent of the kernel before it; two streams = the
+        # page's pattern (section three): the projection on a compute stream,
+        # the AllReduce on a communication stream, each waiting for the other's
+        # event
+        configs = (("plain", "plain", 0, 1), ("serial", "serial", 0, 1), ("serial", "serial", 128, 1),
+                   ("serial", "plain", 128, 1), ("plain", "plain", 0, 2))
+        comm = torch.cuda.Stream()
         for ar in ("fused", "ll"):
-            for gmode, amode, prefetch in configs:
+            for gmode, amode, prefetch, nstreams in configs:
                 hd.set_mode(amode)
                 hg.set_mode(gmode)
 
-                def gemv_call(c):
+                def gemv_call(c, st=None):
                     kind = c % 2
                     return sfar.sfar_rowpar_gemv(hg.h, P(X[kind][(c // 2) % nx]), P(W[(c // 2) % distinct][kind]),
-                                                 P(part[c]), ks[kind], h, prefetch)
+                                                 P(part[c]), ks[kind], h, prefetch, st)
 
-                def ar_call(c):
+                def ar_call(c, st=None):
                     if ar == "fused":
                         return sfar.sfar_allreduce_add_rmsnorm(hd.h, P(part[c]), P(res), wn.data_ptr(), P(out[c]),
-                                                               P(res), 1, h, eps)
-                    return sfar.sfar_allreduce(hd.h, P(part[c]), P(out[c]), h, "ll")
+                                                               P(res), 1, h, eps, st)
+                    return sfar.sfar_allreduce(hd.h, P(part[c]), P(out[c]), h, "ll", st)
 
                 for f in (gemv_call, ar_call):
                     assert f(0) == sfar.SFAR_OK
                 torch.cuda.synchronize()
                 graph = torch.cuda.CUDAGraph()
                 with torch.cuda.graph(graph):
+                    cap = torch.cuda.current_stream()
                     for c in range(calls):
-                        for f in (gemv_call, ar_call):
-                            code = f(c)
+                        if nstreams == 1:
+                            codes = (gemv_call(c), ar_call(c))
+                        else:
+                            g_done = torch.cuda.Event()
+                            code_g = gemv_call(c, cap.cuda_stream)
+                            g_done.record(cap)
+                            comm.wait_event(g_done)
+                            code_a = ar_call(c, comm.cuda_stream)
+                            a_done = torch.cuda.Event()
+                            a_done.record(comm)
+                            cap.wait_event(a_done)
+                            codes = (code_g, code_a)
+                        for code in codes:
                             if code != sfar.SFAR_OK:
                                 raise sfar.SfarError(code, "decode capture")
                 for _ in range(2):
@@ -688,7 +705,7 @@ def run_suite(args):
                     ok = ok and bool(np.array_equal(np.stack([inputs.to_bits(t.cpu()) for t in out[1]]),
                                                     oracle.allreduce(got)))
                 print(json.dumps({"suite": "decode", "ar": ar, "projection_launch": gmode, "allreduce_launch": amode,
-                                  "prefetch_rows": prefetch, "R": R,
+                                  "prefetch_rows": prefetch, "streams": nstreams, "R": R,
                                   "hidden": h, "layers": layers, "calls_per_token": calls,
                                   "us_per_token": round(us_token, 1),
                                   "us_per_projection_and_allreduce": round(us_token / calls, 3),
