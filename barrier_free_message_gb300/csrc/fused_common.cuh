@@ -63,13 +63,16 @@ __device__ __forceinline__ unsigned long long sq_term_narrow(float v, const SqSc
     float t = __fmul_rn(vs, vs);
     if (s.odd)
         t = __fmul_rn(t, 2.0f);
-    // floor(t) for 0 <= t < 2^53 (t is never negative: it is a square)
+    // floor(t) for 0 <= t < 2^53 (t is never negative: it is a square).  With
+    // t = m 2^(x - 150), m the 24-bit significand and x the exponent field,
+    // x - 150 <= 29, so floor(t) = (m 2^32) >> (182 - x): one 64-bit shift.
+    // For t < 1 (zero and subnormals included) the amount is at least 56 and
+    // the result 0; amounts above 63 are clamped by shr.b64 to a result of 0.
     const uint32_t b = __float_as_uint(t);
-    if (b < 0x3f800000u)
-        return 0ull;
-    const int sh = (int)(b >> 23) - 150;
-    const unsigned long long m = (b & 0x7fffffu) | 0x800000u;
-    return sh >= 0 ? m << sh : m >> -sh;
+    const unsigned long long m = (unsigned long long)((b & 0x7fffffu) | 0x800000u) << 32;
+    unsigned long long r;
+    asm("shr.b64 %0, %1, %2;" : "=l"(r) : "l"(m), "r"(182u - (b >> 23)));
+    return r;
 }
 
 __device__ __forceinline__ float mean_square(uint32_t M, unsigned long long S, unsigned long long h, int F)

@@ -97,3 +97,43 @@ def test_a_planted_mistake_is_caught():
         t = (vs * vs).astype(np.float32)
     wrong = np.trunc(t.astype(np.float64)).astype(np.int64)
     assert (wrong != exact_terms(v, E, F)).any()
+
+
+def floor_by_shift(t):
+    """The kernels' floor of a binary32 t in [0, 2^53): the significand with its
+    implicit bit, as m 2^32, shifted right by 182 - (exponent field), amounts
+    above 63 giving 0 (PTX shr.b64 clamps them)."""
+    b = t.view(np.uint32).astype(np.uint64)
+    m = ((b & np.uint64(0x7FFFFF)) | np.uint64(0x800000)) << np.uint64(32)
+    amt = np.uint64(182) - (b >> np.uint64(23))
+    out = np.zeros_like(m)
+    ok = amt < np.uint64(64)
+    out[ok] = m[ok] >> amt[ok]
+    return out.astype(np.int64)
+
+
+def test_floor_by_shift_is_the_floor():
+    # every exponent field a t in [0, 2^53) can have, with edge and random significands
+    rng = np.random.default_rng(5)
+    fields = np.arange(0, 127 + 53, dtype=np.uint32)
+    mant = np.concatenate([np.array([0, 1, 2, 0x400000, 0x7FFFFE, 0x7FFFFF], dtype=np.uint32),
+                           rng.integers(0, 0x800000, 4000, dtype=np.uint32)])
+    t = ((fields[:, None] << np.uint32(23)) | mant[None, :]).reshape(-1).view(np.float32)
+    want = np.floor(t.astype(np.float64)).astype(np.int64)
+    assert np.array_equal(floor_by_shift(t), want)
+    # and on every square the narrow path forms for the bf16 values
+    v = bf16_values()
+    for F in (36, 40, 53):
+        for dE in (0, 1, 5, 30):
+            E = exp_above(v) + dE
+            keep = E <= 128
+            k = F // 2 - E[keep]
+            k1 = k >> 1
+            s1 = ((127 + k1) << 23).astype(np.uint32).view(np.float32)
+            s2 = ((127 + k - k1) << 23).astype(np.uint32).view(np.float32)
+            with np.errstate(under="ignore"):
+                vs = ((v[keep] * s1).astype(np.float32) * s2).astype(np.float32)
+                tt = (vs * vs).astype(np.float32)
+                if F & 1:
+                    tt = (tt * np.float32(2.0)).astype(np.float32)
+            assert np.array_equal(floor_by_shift(tt), np.floor(tt.astype(np.float64)).astype(np.int64))
