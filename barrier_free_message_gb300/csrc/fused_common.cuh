@@ -12,6 +12,25 @@ namespace {
 
 __device__ __forceinline__ uint32_t mag_bits(float v) { return __float_as_uint(v) & 0x7fffffffu; }
 
+// Largest magnitude of the first n bf16 elements of a 16-byte vector, as
+// binary32 magnitude bits (a bf16's bits are the upper half of its binary32
+// bits, and magnitude bits compare as unsigned integers): pairwise maxima of
+// the 16-bit halves, then of the two halves left.  Lanes past n are cleared.
+__device__ __forceinline__ uint32_t max_mag_bf16(const uint4 &z, int n)
+{
+    uint32_t w[4] = {z.x, z.y, z.z, z.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const uint32_t keep = 2 * i + 1 < n ? 0x7fff7fffu : 2 * i < n ? 0x00007fffu : 0u;
+        w[i] &= keep;
+    }
+    uint32_t a, b, m;
+    asm("max.u16x2 %0, %1, %2;" : "=r"(a) : "r"(w[0]), "r"(w[1]));
+    asm("max.u16x2 %0, %1, %2;" : "=r"(b) : "r"(w[2]), "r"(w[3]));
+    asm("max.u16x2 %0, %1, %2;" : "=r"(m) : "r"(a), "r"(b));
+    return max(m >> 16, m & 0xffffu) << 16;
+}
+
 // smallest E with |v| < 2^E for the finite nonzero magnitude bits m
 __device__ __forceinline__ int exp_above(uint32_t m)
 {

@@ -281,9 +281,13 @@ __global__ void __launch_bounds__(SFAR_NORM_THREADS, UB == 8 && RB <= 8 ? 2 : 1)
                     zf[t] = t < NE ? __fadd_rn(V::get(av, t), V::get(rv[q], t)) : 0.f;
                 zv[q] = V::pack(zf);
                 uint32_t m = 0;
+                if (DT == 0) {
+                    m = max_mag_bf16(zv[q], NE);
+                } else {
 #pragma unroll
-                for (int t = 0; t < NE; ++t)
-                    m = max(m, mag_bits(V::get(zv[q], t)));
+                    for (int t = 0; t < NE; ++t)
+                        m = max(m, mag_bits(V::get(zv[q], t)));
+                }
                 lmax[NB == 1 ? 0 : q] = max(lmax[NB == 1 ? 0 : q], m);
                 if (ok)
                     st_unit<UB>((char *)na.res_out[r] + vq[q] * UB, zv[q]);    // z is final: stored now

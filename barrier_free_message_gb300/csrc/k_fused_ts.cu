@@ -55,6 +55,8 @@ template <int DT>
 __device__ __forceinline__ uint32_t unit_max(const uint4 &z)
 {
     using V = Vec<DT>;
+    if (DT == 0)
+        return max_mag_bf16(z, V::N);
     uint32_t m = 0;
 #pragma unroll
     for (int t = 0; t < V::N; ++t)
