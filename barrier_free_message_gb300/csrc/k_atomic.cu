@@ -57,6 +57,13 @@ __device__ __forceinline__ void red_add_u32(uint32_t *p, uint32_t v)
 {
     asm volatile("red.relaxed.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
+// A counter increment with release semantics: it heads a release sequence that
+// every later increment of the counter continues, so the owner's acquire load
+// that reads the count R synchronises with every contributor.
+__device__ __forceinline__ void red_release_add_u32(uint32_t *p, uint32_t v)
+{
+    asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
 __device__ __forceinline__ float ld_relaxed_f32(const float *p)
 {
     float v;
@@ -158,12 +165,11 @@ __global__ void __launch_bounds__(SFAR_THREADS, 3) k_atomic(const __grid_constan
                 }
             }
         }
-        __syncwarp();
-        fence_acq_rel_gpu();
+        __syncwarp();                    // every lane's data reductions before the counter lanes' release
         for (unsigned long long it = it0; it < L; it += its)
             for (int p = lane; p < R; p += 32)
                 if (line_valid(p, it))
-                    red_add_u32(reinterpret_cast<uint32_t *>(acc_line(p, it)), 1u);
+                    red_release_add_u32(reinterpret_cast<uint32_t *>(acc_line(p, it)), 1u);
     }
     sfar_stamp(cl, TP_SENT);
     sfar_mid_delay<TEST>(cl);
@@ -180,7 +186,7 @@ __global__ void __launch_bounds__(SFAR_THREADS, 3) k_atomic(const __grid_constan
         for (unsigned long long m = lane; m < nl && lok; m += 32) {
             const uint32_t *cnt = reinterpret_cast<const uint32_t *>(acc_line(r, it0 + m * its));
             SfarWaiter w;
-            while (ld_relaxed_u32(cnt) != (uint32_t)R) {
+            while (ld_acquire_u32(cnt) != (uint32_t)R) {
                 if (w.tick(a.ctl)) {
                     sfar_record_fault(a.ctl, r, k, -1, e, SFAR_WAIT_COUNTER);
                     lok = 0;
@@ -189,7 +195,7 @@ __global__ void __launch_bounds__(SFAR_THREADS, 3) k_atomic(const __grid_constan
             }
         }
         ok = __all_sync(SFAR_FULL, lok) != 0;
-        fence_acq_rel_gpu();
+        __syncwarp();                           // each lane's acquisition, passed on to the warp
     }
     for (unsigned long long m = 0; m < nl && ok; ++m) {
         const unsigned long long it = it0 + m * its;
@@ -210,10 +216,9 @@ __global__ void __launch_bounds__(SFAR_THREADS, 3) k_atomic(const __grid_constan
     }
     if (ok && !cl.drop) {
         __syncwarp();
-        fence_acq_rel_gpu();
         for (unsigned long long m = 0; m < nl; ++m)
             for (int i = lane; i < R - 1; i += 32)
-                st_relaxed_u32(ag_line(peer_of(r, i), r, it0 + m * its), e);
+                st_release_u32(ag_line(peer_of(r, i), r, it0 + m * its), e);
     }
 
     // 3. all-gather receive: the warp polls the flags of every (owner, line)
@@ -233,7 +238,7 @@ __global__ void __launch_bounds__(SFAR_THREADS, 3) k_atomic(const __grid_constan
                 continue;
             const uint32_t *f = ag_line(r, p, it);
             SfarWaiter w(true);
-            while (ld_relaxed_u32(f) != e) {
+            while (ld_acquire_u32(f) != e) {
                 if (w.tick(a.ctl)) {
                     sfar_record_fault(a.ctl, r, k, p, e, SFAR_WAIT_AG);
                     lok = 0;
@@ -242,7 +247,7 @@ __global__ void __launch_bounds__(SFAR_THREADS, 3) k_atomic(const __grid_constan
             }
         }
         ok = __all_sync(SFAR_FULL, lok) != 0;
-        fence_acq_rel_gpu();
+        __syncwarp();
     }
     for (unsigned long long m = 0; m < na && ok; ++m) {
         const unsigned long long it = it0 + m * its;
