@@ -22,7 +22,7 @@
 //
 // Layout: receive region [receiver][parity][sender][lines * 128 bytes];
 // CTA (r, k), warp w handles iterations k*8 + w + j*K*8 of rank r's data.
-#include "sfar_prims.cuh"
+#include "sfar_lineflags.cuh"
 
 template <int DT, int RB, bool TEST>
 __global__ void __launch_bounds__(SFAR_THREADS) k_ll128(const __grid_constant__ SfarArgs a)
@@ -79,23 +79,11 @@ __global__ void __launch_bounds__(SFAR_THREADS) k_ll128(const __grid_constant__ 
     bool ok = true;
     for (unsigned long long it = it0; it < nit; it += its) {
         const size_t loff = (it * 4ull + g) * 128ull;
-        int lok = 1;
-        for (int i = m; i < R - 1 && lok; i += 8) {
-            const int q = peer_of(r, i);
-            const uint32_t *f = (const uint32_t *)(mine + (size_t)q * slot + loff);
-            SfarWaiter w;
-            while (ld_acquire_u32(f) != e) {
-                if (w.tick(a.ctl)) {
-                    sfar_record_fault(a.ctl, r, k, q, e, SFAR_WAIT_LL128);
-                    lok = 0;
-                    break;
-                }
-            }
-        }
+        const int lok = wait_line_flags<RB>(mine, slot, loff, r, R, m, e, a.ctl, k, SFAR_WAIT_LL128, false) ? 1 : 0;
         ok = __all_sync(SFAR_FULL, lok) != 0;
         if (!ok)
             break;
-        __syncwarp();
+        __syncwarp();                   // each lane's acquisition, passed on to the warp
         const uint4 x = it == it0 ? x0 : (lane < 31 ? load_vec<ES>(a.in[r], it * 31ull + lane, nbytes) : zero);
         const uint4 own = ll128_pack(x, lane);
         uint4 y[RB];

@@ -24,7 +24,7 @@
 // Double buffering: parity e & 1; the argument of the one-shot kernels holds
 // for both regions because every CTA finishes all three phases of epoch e
 // before any of its epoch e + 1 sends.
-#include "sfar_prims.cuh"
+#include "sfar_lineflags.cuh"
 
 template <int DT, int RB, bool TEST>
 __global__ void __launch_bounds__(SFAR_THREADS) k_twoshot(const __grid_constant__ SfarArgs a)
@@ -84,19 +84,7 @@ __global__ void __launch_bounds__(SFAR_THREADS) k_twoshot(const __grid_constant_
     bool ok = true;
     for (unsigned long long it = it0; it < nitc; it += its) {
         const size_t loff = (it * 4ull + g) * 128ull;
-        int lok = 1;
-        for (int i = m; i < R - 1 && lok; i += 8) {
-            const int q = peer_of(r, i);
-            const uint32_t *f = (const uint32_t *)(rs_mine + (size_t)q * slot + loff);
-            SfarWaiter w;
-            while (ld_acquire_u32(f) != e) {
-                if (w.tick(a.ctl)) {
-                    sfar_record_fault(a.ctl, r, k, q, e, SFAR_WAIT_RS);
-                    lok = 0;
-                    break;
-                }
-            }
-        }
+        const int lok = wait_line_flags<RB>(rs_mine, slot, loff, r, R, m, e, a.ctl, k, SFAR_WAIT_RS, false) ? 1 : 0;
         ok = __all_sync(SFAR_FULL, lok) != 0;
         if (!ok)
             break;
@@ -144,19 +132,7 @@ __global__ void __launch_bounds__(SFAR_THREADS) k_twoshot(const __grid_constant_
     const uint8_t *ag_mine = ag + (size_t)(r * 2 + c.par) * R * slot;
     for (unsigned long long it = it0; it < nitc && ok; it += its) {
         const size_t loff = (it * 4ull + g) * 128ull;
-        int lok = 1;
-        for (int i = m; i < R - 1 && lok; i += 8) {
-            const int j = peer_of(r, i);
-            const uint32_t *f = (const uint32_t *)(ag_mine + (size_t)j * slot + loff);
-            SfarWaiter w(true);
-            while (ld_acquire_u32(f) != e) {
-                if (w.tick(a.ctl)) {
-                    sfar_record_fault(a.ctl, r, k, j, e, SFAR_WAIT_AG);
-                    lok = 0;
-                    break;
-                }
-            }
-        }
+        const int lok = wait_line_flags<RB>(ag_mine, slot, loff, r, R, m, e, a.ctl, k, SFAR_WAIT_AG, true) ? 1 : 0;
         ok = __all_sync(SFAR_FULL, lok) != 0;
         if (!ok)
             break;
